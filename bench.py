@@ -1,0 +1,412 @@
+#!/usr/bin/env python
+"""Benchmark of one Beam MoE block forward pass on B300 (tokens/s and roofline fraction).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|prefill|skewed]
+                    [--impl ours|reference]
+
+A step is one moe_forward call (router -> permute -> expert GEMM1+SwiGLU ->
+expert GEMM2 -> combine) over one batch of seeded synthetic inputs with the
+Beam layer's shapes (release article, section "Mixture of Experts": 256
+experts in 8 groups of 32, top-4 groups, top-8 experts, SwiGLU 5120 -> 2560 ->
+5120, combine x2.5). Random-init weights (no checkpoint). Prints one JSON line.
+
+Under torchrun (N > 1) every rank runs an independent replica of the layer on
+its own batch (the block has no cross-token exchange on one GPU's data), so
+the work per GPU is fixed: weak scaling, no data-path collective.
+
+--impl reference times the CPU oracle (plain C, fp64) on the host cores on a
+bounded sample of the same workload; it exists to be compared against.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workload as W  # noqa: E402  (seeded input generators only)
+
+METRIC = "MoE-layer tokens/s at Beam shape (T=64 decode, T=4096 prefill); % of roofline"
+KERNELS_PER_STEP = 10  # router logits, router select, bitmap, column scan, offsets, gather, schedule, GEMM1, GEMM2, combine
+
+# small cases of the same kernels, sized for ncu captures (a few GB on the device)
+PROFILE_CASES = {
+    "profile_decode": W.MoEConfig("profile_decode", T=8, d=5120, E=32, n_groups=8, topk_groups=4, top_k=8, inter=2560),
+    "profile_prefill": W.MoEConfig("profile_prefill", T=512, d=5120, E=32, n_groups=8, topk_groups=4, top_k=8,
+                                   inter=2560),
+}
+
+DEFAULT_STEPS = {"decode": 300, "prefill": 200, "skewed": 40, "nvfp4": 200, "profile_decode": 20,
+                 "profile_prefill": 20}
+
+
+def workload_cfg(name):
+    return W.CONFIGS[name] if name in W.CONFIGS else PROFILE_CASES[name]
+
+
+def describe(cfg):
+    s = (f"{cfg.name}: T={cfg.T} tokens, d={cfg.d}, E={cfg.E} experts in {cfg.n_groups} groups of "
+         f"{cfg.E // cfg.n_groups}, top-{cfg.topk_groups} groups, top-{cfg.top_k} experts, SwiGLU inter={cfg.inter}, "
+         f"{cfg.wfmt} expert weights, fp32 router, combine x{cfg.routed_scale}")
+    if cfg.skew:
+        s += ", 16 hot experts at ~4x mean load"
+    return s
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons, kept with timestamps."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index=0, period_ms=50):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", f"-lms={period_ms}"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 7:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        inside = [p for (t, p) in self.samples if t0 <= t <= t1]
+        window = "timed region"
+        if not inside:  # region shorter than the sampling period: take the nearest samples
+            near = sorted(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))[:3]
+            inside = [p for (_, p) in near]
+            window = "nearest samples (timed region shorter than the sampling period)"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[0]) for p in inside if num(p[0]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for p in inside:
+            for name, v in zip(names, p[3:7]):
+                if v.strip().lower() in ("active", "1", "yes"):
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": num(inside[0][1]),
+                "power_w_max": max((num(p[2]) or 0.0) for p in inside), "reasons": sorted(reasons),
+                "samples": len(inside), "window": window}
+
+
+# ----------------------------------------------------------------------------- ours
+
+def make_device_weights(cfg, seed, torch, keep_host):
+    """Seeded bf16 expert weights generated expert by expert on the host and copied to the device."""
+    import sparse_moe_layer_14_b300 as bm
+    host = {}
+    tens = {}
+    for which in ("gate", "up", "down"):
+        N_, K_ = W.weight_shape(cfg, which)
+        t = torch.empty((cfg.E, N_, K_), dtype=torch.bfloat16, device="cuda")
+        h = np.empty((cfg.E, N_, K_), np.uint16) if keep_host else None
+        step = max(1, (1 << 28) // (N_ * K_))
+        buf = torch.empty((step, N_, K_), dtype=torch.int16).pin_memory()
+        for e0 in range(0, cfg.E, step):
+            e1 = min(cfg.E, e0 + step)
+            chunk = buf[: e1 - e0].numpy().view(np.uint16)
+            W.gen_expert_bf16(cfg, seed, which, e0, e1, out=chunk)
+            t[e0:e1].copy_(buf[: e1 - e0].view(torch.bfloat16))
+            if keep_host:
+                h[e0:e1] = chunk
+        tens[which] = t
+        if keep_host:
+            host[which] = h
+    return bm.ExpertWeights(tens["gate"], tens["up"], tens["down"]), host
+
+
+def roofline_numbers(cfg, touched, peaks):
+    """Algorithmic bytes and FLOPs of the layer and of each expert GEMM launch."""
+    R = cfg.T * cfg.top_k
+    d, I, E = cfg.d, cfg.inter, cfg.E
+    w_bytes_expert = 3 * d * I * 2
+    gemm1 = {"bytes": touched * 2 * I * d * 2 + R * d * 2 + R * I * 2, "flops": 2.0 * R * d * 2 * I}
+    gemm2 = {"bytes": touched * d * I * 2 + R * I * 2 + R * d * 4, "flops": 2.0 * R * I * d}
+    layer = {"bytes": touched * w_bytes_expert + d * E * 4 + cfg.T * d * 2 * 2,
+             "flops": 2.0 * R * 3 * d * I + 2.0 * cfg.T * d * E}
+    for x in (gemm1, gemm2, layer):
+        t_mem = x["bytes"] / (peaks["hbm_gbs"] * 1e9)
+        t_flop = x["flops"] / (peaks["bf16_tflops"] * 1e12)
+        x["bound"] = "hbm" if t_mem >= t_flop else "tensor"
+        x["t_roof_s"] = max(t_mem, t_flop)
+    return gemm1, gemm2, layer
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import sparse_moe_layer_14_b300 as bm
+
+    torch.cuda.set_device(local_rank)
+    cfg = workload_cfg(args.workload)
+    if cfg.wfmt != "bf16":
+        raise SystemExit("the NVFP4 expert path is not built in this library version")
+    peaks = load_peaks()
+    want_cpu = (rank == 0 and world == 1 and not args.no_cpu_baseline)
+    dims = bm.Dims.from_config(cfg)
+
+    t_setup = time.time()
+    weights, host_w = make_device_weights(cfg, args.seed, torch, keep_host=want_cpu)
+    x_h = W.gen_x(cfg, args.seed + 1000 * rank)
+    wr_h = W.gen_wr(cfg, args.seed)
+    x = torch.from_numpy(x_h).view(torch.int16).view(torch.bfloat16).cuda()
+    w_r = torch.from_numpy(wr_h).cuda()
+    out = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device="cuda")
+    counts = torch.empty(cfg.E, dtype=torch.int32, device="cuda")
+    ws = bm.allocate_workspace(dims)
+    stream = torch.cuda.current_stream()
+    setup_s = time.time() - t_setup
+
+    def step():
+        bm.moe_forward(dims, x, w_r, weights, out, ws, counts=counts)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if bm.moe_get_device_status(ws) != bm.MOE_DEV_OK:
+        raise RuntimeError("device status set during warm-up")
+
+    K = args.steps
+    ev_sets = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    for evs in ev_sets:  # create the CUDA handles before the timed region
+        for ev in evs:
+            ev.record(stream)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local_rank) if rank == 0 else None
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    start.record(stream)
+    for i in range(K):
+        bm.moe_set_stage_events(ev_sets[i])
+        step()
+    end.record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    bm.moe_set_stage_events(None)
+    elapsed_ms = start.elapsed_time(end)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    stage_ms = np.zeros(5)
+    for evs in ev_sets:
+        stage_ms += np.array([evs[j].elapsed_time(evs[j + 1]) for j in range(5)])
+    stage_ms /= K
+    if bm.moe_get_device_status(ws) != bm.MOE_DEV_OK:
+        raise RuntimeError("device status set during the timed region")
+    clk = clocks.summary(wall0, wall1) if clocks else None
+
+    # end to end through the public API: pinned host x -> device, forward, device out -> pinned host
+    x_pin = torch.from_numpy(x_h).view(torch.int16).pin_memory()
+    out_pin = torch.empty((cfg.T, cfg.d), dtype=torch.int16).pin_memory()
+    x_dev = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device="cuda")
+
+    def e2e_step():
+        x_dev.view(torch.int16).copy_(x_pin, non_blocking=True)
+        bm.moe_forward(dims, x_dev, w_r, weights, out, ws)
+        out_pin.copy_(out.view(torch.int16), non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    if clocks:
+        clocks.stop()
+
+    c = counts.cpu().numpy()
+    touched = int((c > 0).sum())
+    g1, g2, layer = roofline_numbers(cfg, touched, peaks)
+    ms_per_step = elapsed_ms / K
+    tokens_per_s = world * cfg.T / (ms_per_step / 1e3)
+    if rank != 0:
+        return None
+
+    gemm1_s = stage_ms[2] / 1e3
+    bound = g1["bound"]
+    if bound == "hbm":
+        achieved, peak, unit = g1["bytes"] / gemm1_s / 1e9, peaks["hbm_gbs"], "GB/s"
+    else:
+        achieved, peak, unit = g1["flops"] / gemm1_s / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+    line = {
+        "metric": METRIC, "value": round(tokens_per_s, 1), "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) activations, N(0,1/fan_in) weights)",
+        "impl": "ours",
+        "config": {"workload": describe(cfg), "T": cfg.T, "d": cfg.d, "E": cfg.E, "inter": cfg.inter,
+                   "top_k": cfg.top_k, "parallelism": f"replicas x{world}",
+                   "l2": f"no flush: {touched} experts x {3 * cfg.d * cfg.inter * 2 / 1e6:.1f} MB of weights streamed "
+                         f"per step exceed the 126 MB L2"},
+        "roofline": {"kernel": "expert_gemm_kernel<GLU> (GEMM1 + SwiGLU)", "bound": bound,
+                     "achieved": round(achieved, 1), "peak": peak, "unit": unit, "frac": round(achieved / peak, 4),
+                     "peak_source": f"{peaks['source']} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops'})",
+                     "traffic": None, "algorithmic_bytes": g1["bytes"], "algorithmic_flops": g1["flops"],
+                     "avg_launch_ms": round(stage_ms[2], 4)},
+        "layer_roofline": {"bound": layer["bound"], "roofline_ms": round(layer["t_roof_s"] * 1e3, 4),
+                           "frac": round(layer["t_roof_s"] * 1e3 / ms_per_step, 4), "algorithmic_bytes": layer["bytes"],
+                           "algorithmic_flops": layer["flops"], "experts_touched": touched},
+        "stages_ms": {"router": round(stage_ms[0], 4), "permute": round(stage_ms[1], 4),
+                      "schedule+gemm1": round(stage_ms[2], 4), "gemm2": round(stage_ms[3], 4),
+                      "combine": round(stage_ms[4], 4)},
+        "gemm2_roofline": {"bound": g2["bound"], "frac": round(g2["t_roof_s"] / (stage_ms[3] / 1e3), 4)},
+        "e2e": {"value": round(world * cfg.T / (e2e_ms / K / 1e3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": cfg.T * cfg.d * 2, "d2h_bytes_per_step": cfg.T * cfg.d * 2,
+                "ms_per_step": round(e2e_ms / K, 4)},
+        "gpu_launches": KERNELS_PER_STEP * K,
+        "clocks": clk,
+        "setup_s": round(setup_s, 1),
+    }
+    if want_cpu:
+        line["cpu_baseline"] = cpu_baseline(cfg, args, x_h, wr_h, host_w)
+    return line
+
+
+# ----------------------------------------------------------------------------- oracle legs
+
+def cpu_sample_tokens(cfg):
+    return min(cfg.T, 64)
+
+
+def cpu_baseline(cfg, args, x_h, wr_h, host_w, n_tok=None):
+    """The CPU oracle, as it stands, on a bounded token sample of the same workload."""
+    import oracle as O
+    n = n_tok or cpu_sample_tokens(cfg)
+    sub = cfg.with_tokens(n)
+    t0 = time.time()
+    r = O.route(sub, x_h[:n], wr_h)
+    O.forward_tokens(sub, x_h[:n], r["idx"], r["w"], np.arange(n), host_w)
+    dt = time.time() - t0
+    return {"value": round(n / dt, 3), "unit": "tokens/s", "cores": O.num_threads(), "kind": "oracle",
+            "sample": f"first {n} of the {cfg.T} tokens of the same seeded batch (routing + all {cfg.top_k} experts "
+                      f"per token + combine, fp64 accumulation)", "seconds": round(dt, 2)}
+
+
+def run_reference(args):
+    import oracle as O
+    cfg = workload_cfg(args.workload)
+    host = {}
+    for which in ("gate", "up", "down"):
+        host[which] = W.gen_expert_bf16(cfg, args.seed, which, 0, cfg.E)
+    x_h = W.gen_x(cfg, args.seed)
+    wr_h = W.gen_wr(cfg, args.seed)
+    n = min(cfg.T, args.ref_tokens)
+
+    def step(i):
+        t0 = (i * n) % max(1, cfg.T - n + 1)
+        sub = cfg.with_tokens(n)
+        xs = np.ascontiguousarray(x_h[t0:t0 + n])
+        r = O.route(sub, xs, wr_h)
+        O.forward_tokens(sub, xs, r["idx"], r["w"], np.arange(n), host)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.time()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    dt = time.time() - t0
+    value = n * args.steps / dt
+    return {"metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": describe(cfg), "T": cfg.T, "d": cfg.d, "E": cfg.E, "inter": cfg.inter,
+                       "top_k": cfg.top_k, "parallelism": "host cores"},
+            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": O.num_threads(), "kind": "oracle",
+                             "sample": f"{n} tokens of the {cfg.T}-token batch per step (routing + experts + combine)"},
+            "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="decode", choices=sorted(list(W.CONFIGS) + list(PROFILE_CASES)))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-tokens", type=int, default=16, help="tokens per reference-arm step")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.steps is None:
+        args.steps = DEFAULT_STEPS.get(args.workload, 50) if args.impl == "ours" else 5
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args)), flush=True)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    line = run_ours(args, rank, world, local_rank)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

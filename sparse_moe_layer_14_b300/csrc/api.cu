@@ -1,0 +1,305 @@
+// C ABI of the Beam MoE block (declared in include/beammoe.h): argument
+// validation, the workspace layout, and the launch sequence of each step.
+// No call allocates memory or synchronises the host except
+// moe_get_device_status().
+#include <cmath>
+#include <cstring>
+
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace beammoe;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr long long kDefaultSpins = 1ll << 40;  // pipeline waits are bounded by time by default
+long long g_wait_spins = kDefaultSpins;
+cudaEvent_t g_stage_events[6] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+bool g_stage_events_on = false;
+
+cudaError_t mark(int i, cudaStream_t s) {
+  return g_stage_events_on ? cudaEventRecord(g_stage_events[i], s) : cudaSuccess;
+}
+
+size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
+
+enum Region {
+  R_HDR, R_PART, R_BITMAP, R_WPRE, R_COUNTS, R_OFFS, R_IDX, R_W, R_ROWTOK, R_INVROW,
+  R_ITEMS1, R_ITEMS2, R_XPERM, R_H, R_Y, R_NUM
+};
+
+struct Layout {
+  size_t off[R_NUM];
+  size_t total;
+};
+
+// Upper bound of SMs used to size the router's split-K buffer (the split
+// factor grows with the SM count, so this bounds every device).
+constexpr int kMaxSmsForLayout = 1024;
+
+Layout make_layout(const moe_dims_t& d) {
+  const int64_t T = d.T, R = T * d.top_k;
+  const int Tc = d.T > 0 ? d.T : 1;
+  const int splits = router_splits(Tc, d.d, d.E, kMaxSmsForLayout);
+  const ExpertPlan pl = plan_experts(d.T, d.d, d.E, d.top_k, d.inter);
+  const int64_t nw = bitmap_words(d.T);
+  size_t sz[R_NUM];
+  sz[R_HDR] = sizeof(WsHeader);
+  sz[R_PART] = sizeof(float) * static_cast<size_t>(splits) * T * d.E;
+  sz[R_BITMAP] = sizeof(uint32_t) * static_cast<size_t>(d.E) * nw;
+  sz[R_WPRE] = sizeof(int32_t) * static_cast<size_t>(d.E) * nw;
+  sz[R_COUNTS] = sizeof(int32_t) * d.E;
+  sz[R_OFFS] = sizeof(int32_t) * (d.E + 1);
+  sz[R_IDX] = sizeof(int32_t) * R;
+  sz[R_W] = sizeof(float) * R;
+  sz[R_ROWTOK] = sizeof(int32_t) * R;
+  sz[R_INVROW] = sizeof(int32_t) * R;
+  sz[R_ITEMS1] = sizeof(int4) * static_cast<size_t>(pl.max_items1);
+  sz[R_ITEMS2] = sizeof(int4) * static_cast<size_t>(pl.max_items2);
+  sz[R_XPERM] = sizeof(uint16_t) * R * d.d;
+  sz[R_H] = sizeof(uint16_t) * R * d.inter;
+  sz[R_Y] = sizeof(float) * R * d.d;
+  Layout L;
+  size_t o = 0;
+  for (int i = 0; i < R_NUM; ++i) {
+    L.off[i] = o;
+    o = align_up(o + sz[i]);
+  }
+  L.total = o;
+  return L;
+}
+
+template <typename P>
+P* region(void* ws, const Layout& L, Region r) {
+  return reinterpret_cast<P*>(static_cast<uint8_t*>(ws) + L.off[r]);
+}
+
+moe_status_t check_dims(const moe_dims_t* d) {
+  if (!d) return MOE_ERR_INVALID_ARG;
+  if (d->T < 0 || d->d <= 0 || d->E <= 0 || d->n_groups <= 0 || d->topk_groups <= 0 || d->top_k <= 0 ||
+      d->inter <= 0 || !std::isfinite(d->routed_scale))
+    return MOE_ERR_INVALID_ARG;
+  if (d->E % d->n_groups != 0 || d->topk_groups > d->n_groups || d->top_k > d->topk_groups * (d->E / d->n_groups))
+    return MOE_ERR_INVALID_ARG;
+  if (d->wfmt != MOE_W_BF16 && d->wfmt != MOE_W_NVFP4) return MOE_ERR_INVALID_ARG;
+  if (d->T > 4194304 || d->d % 64 || d->inter % 64 || d->d > 16384 || d->inter > 16384 || d->E > 256 ||
+      d->n_groups > 32 || d->top_k > 32)
+    return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+moe_status_t check_ws(const moe_dims_t* d, void* ws, size_t ws_bytes) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return MOE_ERR_WORKSPACE;
+  if (ws_bytes < make_layout(*d).total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+moe_status_t check_weights(const moe_dims_t* d, const moe_expert_weights_t* w) {
+  if (!w || !aligned16(w->gate) || !aligned16(w->up) || !aligned16(w->down)) return MOE_ERR_INVALID_ARG;
+  if (d->wfmt == MOE_W_NVFP4) {
+    if (!aligned16(w->gate_sf) || !aligned16(w->up_sf) || !aligned16(w->down_sf) || !w->gate_ts || !w->up_ts ||
+        !w->down_ts)
+      return MOE_ERR_INVALID_ARG;
+  }
+  return MOE_OK;
+}
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
+  if (dev < 64 && cache[dev]) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  if (dev < 64) cache[dev] = n;
+  return n;
+}
+
+moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+int32_t* status_word(void* ws) { return ws ? &reinterpret_cast<WsHeader*>(ws)->status : nullptr; }
+
+moe_status_t do_route(const moe_dims_t* d, const uint16_t* x, const float* w_r, int32_t* idx, float* w,
+                      void* ws, const Layout& L, cudaStream_t s) {
+  const int splits = router_splits(d->T, d->d, d->E, num_sms());
+  float* part = region<float>(ws, L, R_PART);
+  cudaError_t e = launch_router_logits(x, w_r, part, d->T, d->d, d->E, splits, s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  e = launch_router_select(part, splits, d->T, d->E, d->n_groups, d->topk_groups, d->top_k, d->routed_scale, idx, w,
+                           status_word(ws), s);
+  return cuda_status(e);
+}
+
+moe_status_t do_permute(const moe_dims_t* d, const uint16_t* x, const int32_t* idx, int32_t* counts,
+                        int32_t* offsets, int32_t* row_token, int32_t* inv_row, uint16_t* x_perm, void* ws,
+                        const Layout& L, cudaStream_t s) {
+  cudaError_t e = launch_permute(x, idx, d->T, d->d, d->E, d->top_k, region<uint32_t>(ws, L, R_BITMAP),
+                                 region<int32_t>(ws, L, R_WPRE), counts, offsets, row_token, inv_row, x_perm,
+                                 status_word(ws), s);
+  return cuda_status(e);
+}
+
+moe_status_t do_ffn(const moe_dims_t* d, const uint16_t* x_perm, const int32_t* offsets,
+                    const moe_expert_weights_t* w, float* y, void* ws, const Layout& L, cudaStream_t s,
+                    cudaEvent_t after_gemm1 = nullptr) {
+  const ExpertPlan pl = plan_experts(d->T, d->d, d->E, d->top_k, d->inter);
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+  ExpertBuffers b;
+  b.x_perm = x_perm;
+  b.offsets = offsets;
+  b.h = region<uint16_t>(ws, L, R_H);
+  b.y = y;
+  b.items1 = region<int4>(ws, L, R_ITEMS1);
+  b.items2 = region<int4>(ws, L, R_ITEMS2);
+  b.n_items = hdr->n_items;
+  b.status = &hdr->status;
+  b.timeout_where = &hdr->timeout_where;
+  ExpertWeightsDev wd;
+  wd.wfmt = d->wfmt;
+  wd.gate = w->gate;
+  wd.up = w->up;
+  wd.down = w->down;
+  wd.gate_sf = w->gate_sf;
+  wd.up_sf = w->up_sf;
+  wd.down_sf = w->down_sf;
+  wd.gate_ts = w->gate_ts;
+  wd.up_ts = w->up_ts;
+  wd.down_ts = w->down_ts;
+  int cu_err = 0;
+  const cudaError_t e = launch_expert_ffn(pl, b, wd, d->T, d->d, d->E, d->top_k, d->inter, num_sms(), g_wait_spins,
+                                          s, &cu_err, after_gemm1);
+  if (e == cudaErrorNotSupported) return MOE_ERR_UNSUPPORTED;
+  return cuda_status(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_workspace_bytes(const moe_dims_t* dims) {
+  if (check_dims(dims) != MOE_OK) return 0;
+  return make_layout(*dims).total;
+}
+
+moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+  if (!ws || ws_bytes < sizeof(WsHeader) || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0)
+    return MOE_ERR_WORKSPACE;
+  return cuda_status(cudaMemsetAsync(ws, 0, sizeof(WsHeader), static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_route(const moe_dims_t* dims, const moe_bf16_t* x, const float* w_r, int32_t* topk_idx,
+                       float* topk_w, void* ws, size_t ws_bytes, void* stream) {
+  moe_status_t st = check_dims(dims);
+  if (st != MOE_OK) return st;
+  if (dims->T == 0) return MOE_OK;
+  if (!aligned16(x) || !aligned16(w_r) || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
+  if ((st = check_ws(dims, ws, ws_bytes)) != MOE_OK) return st;
+  return do_route(dims, x, w_r, topk_idx, topk_w, ws, make_layout(*dims), static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_permute(const moe_dims_t* dims, const moe_bf16_t* x, const int32_t* topk_idx, int32_t* counts,
+                         int32_t* offsets, int32_t* row_token, int32_t* inv_row, moe_bf16_t* x_perm, void* ws,
+                         size_t ws_bytes, void* stream) {
+  moe_status_t st = check_dims(dims);
+  if (st != MOE_OK) return st;
+  if (dims->T == 0) return MOE_OK;
+  if (!aligned16(x) || !topk_idx || !counts || !offsets || !row_token || !inv_row || !aligned16(x_perm))
+    return MOE_ERR_INVALID_ARG;
+  if ((st = check_ws(dims, ws, ws_bytes)) != MOE_OK) return st;
+  return do_permute(dims, x, topk_idx, counts, offsets, row_token, inv_row, x_perm, ws, make_layout(*dims),
+                    static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_expert_ffn(const moe_dims_t* dims, const moe_bf16_t* x_perm, const int32_t* offsets,
+                            const moe_expert_weights_t* weights, float* y_perm, void* ws, size_t ws_bytes,
+                            void* stream) {
+  moe_status_t st = check_dims(dims);
+  if (st != MOE_OK) return st;
+  if (dims->T == 0) return MOE_OK;
+  if (!aligned16(x_perm) || !offsets || !aligned16(y_perm)) return MOE_ERR_INVALID_ARG;
+  if ((st = check_weights(dims, weights)) != MOE_OK) return st;
+  if ((st = check_ws(dims, ws, ws_bytes)) != MOE_OK) return st;
+  return do_ffn(dims, x_perm, offsets, weights, y_perm, ws, make_layout(*dims), static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_combine(const moe_dims_t* dims, const float* y_perm, const int32_t* inv_row, const float* topk_w,
+                         moe_bf16_t* out, void* ws, size_t ws_bytes, void* stream) {
+  moe_status_t st = check_dims(dims);
+  if (st != MOE_OK) return st;
+  if (dims->T == 0) return MOE_OK;
+  if (!aligned16(y_perm) || !inv_row || !topk_w || !out || (reinterpret_cast<uintptr_t>(out) & 7u))
+    return MOE_ERR_INVALID_ARG;
+  if (ws && ws_bytes < sizeof(WsHeader)) return MOE_ERR_WORKSPACE;
+  return cuda_status(launch_combine(y_perm, inv_row, topk_w, out, dims->T, dims->d, dims->top_k, status_word(ws),
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_forward(const moe_dims_t* dims, const moe_bf16_t* x, const float* w_r,
+                         const moe_expert_weights_t* weights, moe_bf16_t* out, int32_t* topk_idx, int32_t* counts,
+                         void* ws, size_t ws_bytes, void* stream) {
+  moe_status_t st = check_dims(dims);
+  if (st != MOE_OK) return st;
+  if (dims->T == 0) return MOE_OK;
+  if (!aligned16(x) || !aligned16(w_r) || !out || (reinterpret_cast<uintptr_t>(out) & 7u))
+    return MOE_ERR_INVALID_ARG;
+  if ((st = check_weights(dims, weights)) != MOE_OK) return st;
+  if ((st = check_ws(dims, ws, ws_bytes)) != MOE_OK) return st;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Layout L = make_layout(*dims);
+  int32_t* idx = topk_idx ? topk_idx : region<int32_t>(ws, L, R_IDX);
+  float* w = region<float>(ws, L, R_W);
+  int32_t* cnt = counts ? counts : region<int32_t>(ws, L, R_COUNTS);
+  int32_t* offs = region<int32_t>(ws, L, R_OFFS);
+  int32_t* row_token = region<int32_t>(ws, L, R_ROWTOK);
+  int32_t* inv_row = region<int32_t>(ws, L, R_INVROW);
+  uint16_t* x_perm = region<uint16_t>(ws, L, R_XPERM);
+  float* y = region<float>(ws, L, R_Y);
+  if (mark(0, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if ((st = do_route(dims, x, w_r, idx, w, ws, L, s)) != MOE_OK) return st;
+  if (mark(1, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if ((st = do_permute(dims, x, idx, cnt, offs, row_token, inv_row, x_perm, ws, L, s)) != MOE_OK) return st;
+  if (mark(2, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if ((st = do_ffn(dims, x_perm, offs, weights, y, ws, L, s, g_stage_events_on ? g_stage_events[3] : nullptr)) !=
+      MOE_OK)
+    return st;
+  if (mark(4, s) != cudaSuccess) return MOE_ERR_CUDA;
+  st = cuda_status(launch_combine(y, inv_row, w, out, dims->T, dims->d, dims->top_k, status_word(ws), s));
+  if (st != MOE_OK) return st;
+  return mark(5, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status_t moe_get_device_status(void* ws, void* stream, int32_t clear, int32_t* code) {
+  if (!ws || !code) return MOE_ERR_INVALID_ARG;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, ws, sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  *code = v;
+  if (clear) {
+    if (cudaMemsetAsync(ws, 0, 2 * sizeof(int32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+moe_status_t moe_set_stage_events(void* const* events, int32_t n) {
+  if (!events || n < 6) {
+    g_stage_events_on = false;
+    return MOE_OK;
+  }
+  for (int i = 0; i < 6; ++i) {
+    if (!events[i]) return MOE_ERR_INVALID_ARG;
+  }
+  for (int i = 0; i < 6; ++i) g_stage_events[i] = static_cast<cudaEvent_t>(events[i]);
+  g_stage_events_on = true;
+  return MOE_OK;
+}
+
+void moe_set_wait_bound(int64_t spins) { g_wait_spins = spins > 0 ? spins : kDefaultSpins; }
+
+const char* moe_version(void) { return "beammoe 0.1 sm_103a (tcgen05 bf16 grouped SwiGLU)"; }
+
+}  // extern "C"

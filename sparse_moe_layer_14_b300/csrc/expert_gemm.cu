@@ -1,0 +1,457 @@
+// Expert SwiGLU MLPs of the Beam MoE block as two grouped GEMMs on the
+// sm_103a tensor cores (release article, section "Mixture of Experts": each
+// expert is a SwiGLU MLP with intermediate size 2,560; section "Residual
+// stream": the SwiGLU product is computed in FP32).
+//
+//   GEMM1 + SwiGLU:  h[r][i] = bf16( silu(x_perm[r].Wg_e[i]) * (x_perm[r].Wu_e[i]) )
+//   GEMM2:           y[r][n] = h[r] . Wd_e[n]                                   (fp32)
+//
+// Design (weight-stationary, "swap AB"): the MMA's M operand is a 128-row
+// tile of one expert's weights (K-major, straight from the checkpoint
+// layout) and its N operand is the expert's tokens (rows of x_perm / h),
+// N = the tile's token count rounded up to 16, so a decode batch with two or
+// three tokens per expert does no padded tensor work and every weight byte is
+// streamed from HBM once per token tile. Accumulators live in TMEM:
+// D[weight row][token], fp32.
+//
+// One persistent CTA per SM, 192 threads:
+//   warp 0      TMA producer: weight tile(s) + token rows per 64-wide K slice
+//   warp 1      TMEM allocator and single-thread tcgen05.mma issuer
+//   warps 2..5  epilogue: tcgen05.ld, SwiGLU in FP32 (GEMM1) or fp32 store
+// Work items {expert, weight tile, first row, tokens} are built on the device
+// from the expert offsets (no host synchronisation) and taken round-robin.
+// Every mbarrier wait is bounded; on expiry the CTA latches MOE_DEV_TIMEOUT,
+// waits (bounded) for its own copies and MMAs in flight, frees TMEM, returns.
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace beammoe {
+
+namespace {
+
+constexpr int BM = 128;       // weight rows per tile = MMA M
+constexpr int BK = 64;        // K elements per pipeline stage (128 bytes of bf16)
+constexpr int TOK_BOX = 16;   // token rows per TMA box
+constexpr int kMaxStages = 8;
+constexpr int kMaxAcc = 4;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kATileBytes = BM * BK * 2;            // 16 KB
+constexpr uint32_t kTokBoxBytes = TOK_BOX * BK * 2;      // 2 KB
+constexpr uint64_t kDrainNs = 1000000000ull;             // 1 s bound for draining on abort
+constexpr uint64_t kWaitNs = 2000000000ull;              // 2 s bound of a pipeline wait
+constexpr int kSmemLimit = 232448;                       // 227 KB opt-in per block
+
+struct GemmArgs {
+  const int4* items;
+  const int32_t* n_items;
+  int K;           // reduction length
+  int Nw;          // weight rows per expert = output columns
+  int n_max;       // max tokens per item (multiple of 16)
+  int stages;
+  int acc_bufs;
+  int acc_cols;    // TMEM columns per accumulator buffer
+  uint32_t stage_bytes;
+  uint32_t b_offset;  // token tile offset inside a stage
+  uint16_t* h_out;    // GEMM1 output [R][Nw] bf16
+  float* y_out;       // GEMM2 output [R][Nw] fp32
+  const float* ts0;   // per-expert scale applied to accumulator 0 (NVFP4), or null
+  const float* ts1;
+  int32_t* status;
+  int32_t* timeout_where;
+  long long wait_spins;
+};
+
+__device__ __forceinline__ void fail(const GemmArgs& p, volatile int* abort, int where) {
+  latch_status(p.status, MOE_DEV_TIMEOUT);
+  if (p.timeout_where) atomicCAS(p.timeout_where, 0, where);
+  *abort = 1;
+}
+
+template <bool kGLU>
+__global__ void __launch_bounds__(kThreads, 1)
+    expert_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
+                       const __grid_constant__ CUtensorMap tmB, const GemmArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t accf_bar[kMaxAcc];
+  __shared__ __align__(8) uint64_t acce_bar[kMaxAcc];
+  __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int* abort = &abort_flag;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int a = 0; a < p.acc_bufs; ++a) {
+      mbar_init(&accf_bar[a], 1);
+      mbar_init(&acce_bar[a], 128);
+    }
+    mbar_init(&drain_bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA0);
+    if (kGLU) tma_prefetch_desc(&tmA1);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const uint32_t tmem_base = tmem_slot;
+  const int n_items = *p.n_items;
+  const int kblocks = p.K / BK;
+  long long fills = 0;  // TMA stage fills issued (thread 0 only)
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+        const int4 item = p.items[it];
+        const int a_row = item.x * p.Nw + item.y * BM;
+        const int nbox = (item.w + TOK_BOX - 1) / TOK_BOX;
+        const uint32_t bytes = kATileBytes * (kGLU ? 2u : 1u) + static_cast<uint32_t>(nbox) * kTokBoxBytes;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, p.wait_spins, kWaitNs, abort)) {
+            if (!*abort) fail(p, abort, 1);
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + static_cast<size_t>(stage) * p.stage_bytes;
+          mbar_arrive_expect_tx(&full_bar[stage], bytes);
+          tma_load_2d(st, &tmA0, kb * BK, a_row, &full_bar[stage]);
+          if (kGLU) tma_load_2d(st + kATileBytes, &tmA1, kb * BK, a_row, &full_bar[stage]);
+          uint8_t* sb = st + p.b_offset;
+          for (int j = 0; j < nbox; ++j)
+            tma_load_2d(sb + j * kTokBoxBytes, &tmB, kb * BK, item.z + j * TOK_BOX, &full_bar[stage]);
+          ++fills;
+          if (++stage == p.stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+        const int4 item = p.items[it];
+        const int n_mma = (item.w + 15) & ~15;
+        const uint32_t idesc = idesc_bf16_f32(BM, n_mma);
+        if (!mbar_wait_bounded(&acce_bar[acc], acc_phase ^ 1u, p.wait_spins, kWaitNs, abort)) {
+          if (!*abort) fail(p, abort, 2);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * p.acc_cols);
+        const uint32_t d1 = d0 + static_cast<uint32_t>(p.n_max);
+        bool ok = true;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait_bounded(&full_bar[stage], phase, p.wait_spins, kWaitNs, abort)) {
+            if (!*abort) fail(p, abort, 3);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + static_cast<size_t>(stage) * p.stage_bytes);
+          const uint32_t sb = sa + p.b_offset;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint64_t bdesc = sdesc_kmajor_sw128(sb + k * 32);
+            const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
+            mma_bf16_ss(d0, sdesc_kmajor_sw128(sa + k * 32), bdesc, idesc, accum);
+            if (kGLU) mma_bf16_ss(d1, sdesc_kmajor_sw128(sa + kATileBytes + k * 32), bdesc, idesc, accum);
+          }
+          mma_commit(&empty_bar[stage]);
+          if (++stage == p.stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&accf_bar[acc]);
+        if (++acc == p.acc_bufs) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int r = q * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+      const int4 item = p.items[it];
+      // tcgen05.ld is warp-collective: the whole warp proceeds or stops together
+      const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&accf_bar[acc], acc_phase, p.wait_spins, kWaitNs, abort));
+      if (!ok) {
+        if (lane == 0 && !*abort) fail(p, abort, 4);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * p.acc_cols);
+      const int col = item.y * BM + r;
+      const bool valid = col < p.Nw;
+      const int ntok = item.w;
+      const float s0 = p.ts0 ? p.ts0[item.x] : 1.0f;
+      const float s1 = (kGLU && p.ts1) ? p.ts1[item.x] : 1.0f;
+      for (int c = 0; c < ntok; c += 16) {
+        uint32_t g[16], u[16];
+        tmem_ld_32x32b_x16(tb + c, g);
+        if (kGLU) tmem_ld_32x32b_x16(tb + p.n_max + c, u);
+        tmem_ld_wait();
+        if (valid) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int tok = c + j;
+            if (tok < ntok) {
+              const size_t off = static_cast<size_t>(item.z + tok) * p.Nw + col;
+              if (kGLU) {
+                const float gv = __uint_as_float(g[j]) * s0;
+                const float uv = __uint_as_float(u[j]) * s1;
+                const float silu = gv / (1.0f + expf(-gv));
+                p.h_out[off] = __bfloat16_as_ushort(__float2bfloat16_rn(silu * uv));
+              } else {
+                p.y_out[off] = __uint_as_float(g[j]) * s0;
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&acce_bar[acc]);
+      if (++acc == p.acc_bufs) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (*abort) {
+    // Every role has stopped. Let the copies and MMAs this CTA issued land
+    // before its shared memory and TMEM are released.
+    if (threadIdx.x == 0) {
+      for (int s = 0; s < p.stages; ++s) {
+        if (fills > s) {
+          const long long f = s + static_cast<long long>(p.stages) * ((fills - 1 - s) / p.stages);
+          mbar_wait_bounded(&full_bar[s], static_cast<uint32_t>((f / p.stages) & 1), 1ll << 40, kDrainNs, nullptr);
+        }
+      }
+    }
+    if (warp == 1 && lane == 0) {
+      mma_commit(&drain_bar);
+      mbar_wait_bounded(&drain_bar, 0, 1ll << 40, kDrainNs, nullptr);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  }
+  if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+// Work items from the expert offsets: one thread per expert (E <= 256).
+// Tokens of an expert are split into ceil(n/n_max) tiles of near-equal size
+// (multiples of 16). Items are ordered expert, weight tile, token tile so the
+// token tiles of one weight tile run side by side and share it through L2.
+__global__ void __launch_bounds__(256) schedule_kernel(const int32_t* __restrict__ offsets, int E, int R, int n_max,
+                                                       int wt1, int wt2, int4* __restrict__ items1,
+                                                       int4* __restrict__ items2, int32_t* __restrict__ n_items,
+                                                       int32_t* status) {
+  __shared__ int warp_sums[8];
+  const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
+  int n = 0, row0 = 0, ntiles = 0, tsz = 16;
+  if (e < E) {
+    const int a = offsets[e], b = offsets[e + 1];
+    if (a < 0 || b < a || b > R) {
+      latch_status(status, MOE_DEV_BAD_ROW);
+    } else {
+      n = b - a;
+      row0 = a;
+    }
+    if (n > 0) {
+      ntiles = (n + n_max - 1) / n_max;
+      tsz = ((n + ntiles - 1) / ntiles + 15) & ~15;
+      if (tsz > n_max) tsz = n_max;
+      ntiles = (n + tsz - 1) / tsz;
+    }
+  }
+  int incl = ntiles;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  int base = 0, total = 0;
+  for (int w = 0; w < 8; ++w) {
+    if (w < warp) base += warp_sums[w];
+    total += warp_sums[w];
+  }
+  const int tile0 = base + incl - ntiles;  // tiles before this expert
+  for (int wt = 0; wt < wt1; ++wt)
+    for (int j = 0; j < ntiles; ++j)
+      items1[static_cast<size_t>(tile0) * wt1 + wt * ntiles + j] =
+          make_int4(e, wt, row0 + j * tsz, min(tsz, n - j * tsz));
+  for (int wt = 0; wt < wt2; ++wt)
+    for (int j = 0; j < ntiles; ++j)
+      items2[static_cast<size_t>(tile0) * wt2 + wt * ntiles + j] =
+          make_int4(e, wt, row0 + j * tsz, min(tsz, n - j * tsz));
+  if (threadIdx.x == 0) {
+    n_items[0] = total * wt1;
+    n_items[1] = total * wt2;
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  return fn;
+}
+
+// 2-D bf16 tensor [outer][inner] (inner contiguous), box [box_outer][64],
+// 128-byte swizzle, zero fill out of bounds.
+int encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (!fn) return -1;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : static_cast<int>(r);
+}
+
+struct StageShape {
+  int stages, acc_bufs, acc_cols;
+  uint32_t stage_bytes, b_offset;
+  size_t smem;
+};
+
+StageShape stage_shape(bool glu, int n_max) {
+  StageShape s;
+  s.b_offset = kATileBytes * (glu ? 2u : 1u);
+  s.stage_bytes = s.b_offset + static_cast<uint32_t>(n_max) * BK * 2;
+  const int budget = kSmemLimit - 1024 - 512;  // alignment slack + static barriers
+  s.stages = std::min(kMaxStages, budget / static_cast<int>(s.stage_bytes));
+  s.acc_cols = glu ? 2 * n_max : n_max;
+  s.acc_bufs = std::min(kMaxAcc, static_cast<int>(kTmemCols) / s.acc_cols);
+  s.smem = 1024 + static_cast<size_t>(s.stages) * s.stage_bytes;
+  return s;
+}
+
+template <bool kGLU>
+cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b, GemmArgs args,
+                        int n_max, int grid, cudaStream_t stream) {
+  const StageShape s = stage_shape(kGLU, n_max);
+  args.stages = s.stages;
+  args.acc_bufs = s.acc_bufs;
+  args.acc_cols = s.acc_cols;
+  args.stage_bytes = s.stage_bytes;
+  args.b_offset = s.b_offset;
+  args.n_max = n_max;
+  cudaError_t err = cudaFuncSetAttribute(expert_gemm_kernel<kGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(s.smem));
+  if (err != cudaSuccess) return err;
+  expert_gemm_kernel<kGLU><<<grid, kThreads, s.smem, stream>>>(a0, a1, b, args);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+ExpertPlan plan_experts(int T, int d, int E, int top_k, int inter) {
+  ExpertPlan p;
+  const int tok = ((std::max(T, 1) + 15) / 16) * 16;  // an expert sees a token at most once
+  p.n_max = std::min(256, tok);
+  const int64_t R = static_cast<int64_t>(T) * top_k;
+  p.max_tiles = static_cast<int>(E + (R + p.n_max - 1) / p.n_max);
+  p.wtiles1 = (inter + BM - 1) / BM;
+  p.wtiles2 = (d + BM - 1) / BM;
+  p.max_items1 = static_cast<int64_t>(p.max_tiles) * p.wtiles1;
+  p.max_items2 = static_cast<int64_t>(p.max_tiles) * p.wtiles2;
+  return p;
+}
+
+cudaError_t launch_expert_ffn(const ExpertPlan& plan, const ExpertBuffers& buf, const ExpertWeightsDev& w, int T,
+                              int d, int E, int top_k, int inter, int num_sms, long long wait_spins,
+                              cudaStream_t stream, int* cu_error, cudaEvent_t after_gemm1) {
+  *cu_error = 0;
+  const int R = T * top_k;
+  schedule_kernel<<<1, 256, 0, stream>>>(buf.offsets, E, R, plan.n_max, plan.wtiles1, plan.wtiles2, buf.items1,
+                                         buf.items2, buf.n_items, buf.status);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  if (w.wfmt != MOE_W_BF16) return cudaErrorNotSupported;
+
+  CUtensorMap tg, tu, tx, td, th;
+  int rc = 0;
+  rc |= encode_bf16_2d(&tg, w.gate, d, static_cast<uint64_t>(E) * inter, BM);
+  rc |= encode_bf16_2d(&tu, w.up, d, static_cast<uint64_t>(E) * inter, BM);
+  rc |= encode_bf16_2d(&tx, buf.x_perm, d, R, TOK_BOX);
+  rc |= encode_bf16_2d(&td, w.down, inter, static_cast<uint64_t>(E) * d, BM);
+  rc |= encode_bf16_2d(&th, buf.h, inter, R, TOK_BOX);
+  if (rc) {
+    *cu_error = rc;
+    return cudaErrorInvalidValue;
+  }
+  GemmArgs a1{};
+  a1.items = buf.items1;
+  a1.n_items = buf.n_items;
+  a1.K = d;
+  a1.Nw = inter;
+  a1.h_out = buf.h;
+  a1.status = buf.status;
+  a1.timeout_where = buf.timeout_where;
+  a1.wait_spins = wait_spins;
+  err = launch_gemm<true>(tg, tu, tx, a1, plan.n_max, num_sms, stream);
+  if (err != cudaSuccess) return err;
+  if (after_gemm1 && (err = cudaEventRecord(after_gemm1, stream)) != cudaSuccess) return err;
+  GemmArgs a2{};
+  a2.items = buf.items2;
+  a2.n_items = buf.n_items + 1;
+  a2.K = inter;
+  a2.Nw = d;
+  a2.y_out = buf.y;
+  a2.status = buf.status;
+  a2.timeout_where = buf.timeout_where;
+  a2.wait_spins = wait_spins;
+  return launch_gemm<false>(td, td, th, a2, plan.n_max, num_sms, stream);
+}
+
+}  // namespace beammoe

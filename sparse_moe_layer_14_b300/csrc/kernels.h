@@ -1,0 +1,66 @@
+// Host-side launchers of the Beam MoE kernels (internal to the library).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace beammoe {
+
+// ---- router (router.cu) ----
+// Split-K factor of the router logits GEMM for a batch of T tokens.
+int router_splits(int T, int d, int E, int num_sms);
+// partial[s][t][e] = sum over k in split s of x[t][k] * w_r[k][e]  (fp32)
+cudaError_t launch_router_logits(const uint16_t* x, const float* w_r, float* partial, int T, int d, int E,
+                                 int splits, cudaStream_t stream);
+// sigmoid scores, group-limited top-k, normalised weights; sets the expert
+// bitmap bits when `bitmap` is non-null.
+cudaError_t launch_router_select(const float* partial, int splits, int T, int E, int n_groups, int topk_groups,
+                                 int top_k, float routed_scale, int32_t* topk_idx, float* topk_w,
+                                 int32_t* status, cudaStream_t stream);
+
+// ---- permutation (permute.cu) ----
+int bitmap_words(int T);
+cudaError_t launch_permute(const uint16_t* x, const int32_t* topk_idx, int T, int d, int E, int top_k,
+                           uint32_t* bitmap, int32_t* word_prefix, int32_t* counts, int32_t* offsets,
+                           int32_t* row_token, int32_t* inv_row, uint16_t* x_perm, int32_t* status,
+                           cudaStream_t stream);
+
+// ---- expert FFN (expert_gemm.cu) ----
+struct ExpertPlan {
+  int n_max;        // max tokens per work item (multiple of 16, <= 256)
+  int max_tiles;    // upper bound of (expert, token tile) pairs
+  int wtiles1;      // 128-row weight tiles per expert in GEMM1 (ceil(inter/128))
+  int wtiles2;      // ... in GEMM2 (ceil(d/128))
+  int64_t max_items1, max_items2;
+};
+ExpertPlan plan_experts(int T, int d, int E, int top_k, int inter);
+
+struct ExpertBuffers {
+  const uint16_t* x_perm;  // [R][d]
+  const int32_t* offsets;  // [E+1]
+  uint16_t* h;             // [R][inter]
+  float* y;                // [R][d]
+  int4* items1;            // GEMM1 work items {e, wtile, row0, ntok}
+  int4* items2;
+  int32_t* n_items;        // [2]
+  int32_t* status;
+  int32_t* timeout_where;
+};
+
+struct ExpertWeightsDev {
+  int wfmt;
+  const void *gate, *up, *down;
+  const uint8_t *gate_sf, *up_sf, *down_sf;
+  const float *gate_ts, *up_ts, *down_ts;
+};
+
+cudaError_t launch_expert_ffn(const ExpertPlan& plan, const ExpertBuffers& buf, const ExpertWeightsDev& w, int T,
+                              int d, int E, int top_k, int inter, int num_sms, long long wait_spins,
+                              cudaStream_t stream, int* cu_error, cudaEvent_t after_gemm1 = nullptr);
+
+// ---- combine (combine.cu) ----
+cudaError_t launch_combine(const float* y_perm, const int32_t* inv_row, const float* topk_w, uint16_t* out,
+                           int T, int d, int top_k, int32_t* status, cudaStream_t stream);
+
+}  // namespace beammoe
