@@ -57,7 +57,8 @@ typedef enum {
   MOE_ERR_WORKSPACE = 3,     /* workspace null, misaligned or smaller than moe_workspace_bytes() */
   MOE_ERR_CUDA = 4,          /* a CUDA runtime/driver call or launch failed */
   MOE_ERR_DEVICE_STATUS = 5, /* reserved for callers that fold the device code into one status */
-  MOE_ERR_DEVICE_TIMEOUT = 6 /* device code: a bounded wait inside a kernel expired */
+  MOE_ERR_DEVICE_TIMEOUT = 6, /* device code: a bounded wait inside a kernel expired */
+  MOE_ERR_SCRATCH_LIMIT = 7   /* moe_permute_noalloc: sizes beyond its fixed device scratch */
 } moe_status_t;
 
 /* Codes latched in the workspace header by kernels (read by moe_get_device_status). */
@@ -160,6 +161,27 @@ moe_status_t moe_combine(const moe_dims_t* dims, const float* y_perm, const int3
 moe_status_t moe_forward(const moe_dims_t* dims, const moe_bf16_t* x, const float* w_r,
                          const moe_expert_weights_t* weights, moe_bf16_t* out, int32_t* topk_idx,
                          int32_t* counts, void* ws, size_t ws_bytes, void* stream);
+
+/* Allocation-free permutation. The paper has no counterpart: this entry point
+ * exists for callers that cannot allocate device memory -- code running while
+ * a CUDA graph is captured, serving loops that must never call cudaMalloc, or
+ * plugins whose host framework owns all device memory. It computes exactly
+ * what moe_permute computes, with the same arguments except the workspace:
+ * its scratch (a token x expert bitmap and per-word prefix counts, plus a
+ * status word) lives in one fixed device array of about 1 MiB inside the
+ * library, which every GPU that loads the library keeps until the process
+ * exits. Nothing is allocated and no allocating routine is called.
+ * Limits: T <= 16384 and E <= 256; larger sizes return MOE_ERR_SCRATCH_LIMIT
+ * before any work. The first call on each device looks up the array's device
+ * address (one-time set-up), so make that first call before any stream
+ * capture. All calls share the array and it keeps the last call's contents:
+ * every call clears its status word and bitmap first, and calls that overlap
+ * on the GPU (other streams, other host threads) race on it -- issue them on
+ * one stream. device_status (device int32, nullable) receives this call's
+ * moe_device_code_t (MOE_DEV_BAD_EXPERT if an index was out of range). */
+moe_status_t moe_permute_noalloc(const moe_dims_t* dims, const moe_bf16_t* x, const int32_t* topk_idx,
+                                 int32_t* counts, int32_t* offsets, int32_t* row_token, int32_t* inv_row,
+                                 moe_bf16_t* x_perm, int32_t* device_status, void* stream);
 
 /* Read (and with clear != 0, reset) the device code latched in the workspace
  * header. Synchronises `stream`. *code receives a moe_device_code_t. */

@@ -24,7 +24,7 @@ from ._native import (MOE_DEV_BAD_EXPERT, MOE_DEV_BAD_ROW, MOE_DEV_OK, MOE_DEV_T
                       MOE_DEV_ZERO_SUM, MOE_W_BF16, MOE_W_NVFP4, MoeDims, MoeExpertWeights)
 
 __all__ = ["MoEError", "Dims", "ExpertWeights", "moe_workspace_bytes", "moe_workspace_init", "moe_route",
-           "moe_permute", "moe_expert_ffn", "moe_combine", "moe_forward", "moe_get_device_status",
+           "moe_permute", "moe_permute_noalloc", "moe_expert_ffn", "moe_combine", "moe_forward", "moe_get_device_status",
            "moe_set_wait_bound", "moe_set_stage_events", "moe_version", "allocate_workspace", "library_path"]
 
 
@@ -162,6 +162,26 @@ def moe_permute(dims: Dims, x, topk_idx, counts, offsets, row_token, inv_row, x_
     _check("moe_permute", _lib().moe_permute(ctypes.byref(dims.c()), _ptr(x), _ptr(topk_idx), _ptr(counts),
                                              _ptr(offsets), _ptr(row_token), _ptr(inv_row), _ptr(x_perm), _ptr(ws),
                                              ws.numel(), _stream(stream)))
+
+
+def moe_permute_noalloc(dims: Dims, x, topk_idx, counts, offsets, row_token, inv_row, x_perm, device_status=None,
+                        stream=None):
+    """moe_permute without a workspace, for callers that cannot allocate device memory:
+    the library's fixed ~1 MiB device scratch is used instead (T <= 16384, E <= 256).
+    The first call on a device does a one-time set-up; make it before any stream
+    capture. Calls share the scratch, so do not overlap them on the GPU."""
+    R = dims.T * dims.top_k
+    _expect(x, _BF16, (dims.T, dims.d), "x")
+    _expect(topk_idx, (torch.int32,), (dims.T, dims.top_k), "topk_idx")
+    _expect(counts, (torch.int32,), (dims.E,), "counts")
+    _expect(offsets, (torch.int32,), (dims.E + 1,), "offsets")
+    _expect(row_token, (torch.int32,), (R,), "row_token")
+    _expect(inv_row, (torch.int32,), (R,), "inv_row")
+    _expect(x_perm, _BF16, (R, dims.d), "x_perm")
+    _expect(device_status, (torch.int32,), (1,), "device_status")
+    _check("moe_permute_noalloc", _lib().moe_permute_noalloc(
+        ctypes.byref(dims.c()), _ptr(x), _ptr(topk_idx), _ptr(counts), _ptr(offsets), _ptr(row_token),
+        _ptr(inv_row), _ptr(x_perm), _ptr(device_status), _stream(stream)))
 
 
 def _check_weights(dims: Dims, w: ExpertWeights):

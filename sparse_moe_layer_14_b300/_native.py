@@ -9,9 +9,10 @@ LIB_PATH = os.path.join(HERE, "libbeammoe.so")
 
 # moe_status_t
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA = 0, 1, 2, 3, 4
-MOE_ERR_DEVICE_STATUS, MOE_ERR_DEVICE_TIMEOUT = 5, 6
+MOE_ERR_DEVICE_STATUS, MOE_ERR_DEVICE_TIMEOUT, MOE_ERR_SCRATCH_LIMIT = 5, 6, 7
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
-                4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE_STATUS", 6: "MOE_ERR_DEVICE_TIMEOUT"}
+                4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE_STATUS", 6: "MOE_ERR_DEVICE_TIMEOUT",
+                7: "MOE_ERR_SCRATCH_LIMIT"}
 # moe_device_code_t
 MOE_DEV_OK, MOE_DEV_BAD_EXPERT, MOE_DEV_BAD_ROW, MOE_DEV_TIMEOUT, MOE_DEV_ZERO_SUM = 0, 1, 2, 6, 7
 # moe_wfmt_t
@@ -19,7 +20,7 @@ MOE_W_BF16, MOE_W_NVFP4 = 0, 1
 
 EXPORTS = ["moe_workspace_bytes", "moe_workspace_init", "moe_route", "moe_permute", "moe_expert_ffn",
            "moe_combine", "moe_forward", "moe_get_device_status", "moe_set_wait_bound", "moe_set_stage_events",
-           "moe_version"]
+           "moe_version", "moe_permute_noalloc"]
 
 
 class MoeDims(ctypes.Structure):
@@ -65,6 +66,8 @@ def load(path: str = LIB_PATH):
     L.moe_get_device_status.restype = st
     L.moe_set_wait_bound.argtypes = [ctypes.c_int64]
     L.moe_set_wait_bound.restype = None
+    L.moe_permute_noalloc.argtypes = [pd, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.moe_permute_noalloc.restype = st
     L.moe_set_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int32]
     L.moe_set_stage_events.restype = st
     L.moe_version.argtypes = []
