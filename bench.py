@@ -36,7 +36,36 @@ sys.path.insert(0, ROOT)
 import workload as W  # noqa: E402  (seeded input generators only)
 
 METRIC = "MoE-layer tokens/s at Beam shape (T=64 decode, T=4096 prefill); % of roofline"
-KERNELS_PER_STEP = 10  # router logits, router select, bitmap, column scan, offsets, gather, schedule, GEMM1, GEMM2, combine
+# router logits, (split reduce), router select, bitmap, column scan, offsets, gather, schedule, GEMM1, GEMM2, combine
+
+
+def router_splits(T, d, E, num_sms):
+    """The library's split of the router's hidden dimension (same rule as router.cu)."""
+    tiles = -(-T // 64) * -(-E // 128)
+    target = -(-num_sms // tiles)
+    chunks = d // 32
+    best = 1
+    for s in range(1, chunks + 1):
+        if chunks % s or d // s < 64:
+            continue
+        best = s
+        if s >= target:
+            break
+    return best
+
+
+def kernels_per_step(cfg, num_sms):
+    return 10 + (1 if router_splits(cfg.T, cfg.d, cfg.E, num_sms) > 1 else 0)
+
+
+def max_over_ranks(value, world, device):
+    """Max of a float over all ranks (the job is as slow as its slowest rank)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
 
 # small cases of the same kernels, sized for ncu captures (a few GB on the device)
 PROFILE_CASES = {
@@ -69,6 +98,27 @@ def load_peaks():
         return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
                 "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
     return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+
+
+def profiled_traffic(kernel, algorithmic_bytes):
+    """DRAM bytes of one launch of `kernel`, from the committed ncu capture of a smaller case
+    scaled by algorithmic bytes (weights of touched experts + activations); None when the
+    kernel's sources changed since the capture."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None, "no capture"
+    rec = json.load(open(p)).get(kernel)
+    if not rec:
+        return None, "no capture"
+    h = hashlib.sha256()
+    for src in rec["sources"]:
+        h.update(open(os.path.join(ROOT, src), "rb").read())
+    if h.hexdigest() != rec["source_sha256"]:
+        return None, "kernel changed since the capture"
+    measured = rec["dram_bytes_read"] + rec["dram_bytes_write"]
+    return int(round(measured * algorithmic_bytes / rec["algorithmic_bytes"])), (
+        f"ncu dram__bytes_read+write of {rec['capture']}, scaled by algorithmic bytes")
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -231,11 +281,7 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         torch.distributed.barrier()
     bm.moe_set_stage_events(None)
-    elapsed_ms = start.elapsed_time(end)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(start.elapsed_time(end), world, "cuda")
     stage_ms = np.zeros(5)
     for evs in ev_sets:
         stage_ms += np.array([evs[j].elapsed_time(evs[j + 1]) for j in range(5)])
@@ -263,11 +309,7 @@ def run_ours(args, rank, world, local_rank):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, "cuda")
     if clocks:
         clocks.stop()
 
@@ -285,6 +327,7 @@ def run_ours(args, rank, world, local_rank):
         achieved, peak, unit = g1["bytes"] / gemm1_s / 1e9, peaks["hbm_gbs"], "GB/s"
     else:
         achieved, peak, unit = g1["flops"] / gemm1_s / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+    traffic, traffic_src = profiled_traffic("expert_gemm_kernel<GLU>", g1["bytes"])
     line = {
         "metric": METRIC, "value": round(tokens_per_s, 1), "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
@@ -297,7 +340,7 @@ def run_ours(args, rank, world, local_rank):
         "roofline": {"kernel": "expert_gemm_kernel<GLU> (GEMM1 + SwiGLU)", "bound": bound,
                      "achieved": round(achieved, 1), "peak": peak, "unit": unit, "frac": round(achieved / peak, 4),
                      "peak_source": f"{peaks['source']} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops'})",
-                     "traffic": None, "algorithmic_bytes": g1["bytes"], "algorithmic_flops": g1["flops"],
+                     "traffic": traffic, "traffic_source": traffic_src, "algorithmic_bytes": g1["bytes"], "algorithmic_flops": g1["flops"],
                      "avg_launch_ms": round(stage_ms[2], 4)},
         "layer_roofline": {"bound": layer["bound"], "roofline_ms": round(layer["t_roof_s"] * 1e3, 4),
                            "frac": round(layer["t_roof_s"] * 1e3 / ms_per_step, 4), "algorithmic_bytes": layer["bytes"],
@@ -309,7 +352,7 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": round(world * cfg.T / (e2e_ms / K / 1e3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": cfg.T * cfg.d * 2, "d2h_bytes_per_step": cfg.T * cfg.d * 2,
                 "ms_per_step": round(e2e_ms / K, 4)},
-        "gpu_launches": KERNELS_PER_STEP * K,
+        "gpu_launches": kernels_per_step(cfg, torch.cuda.get_device_properties(local_rank).multi_processor_count) * K,
         "clocks": clk,
         "setup_s": round(setup_s, 1),
     }

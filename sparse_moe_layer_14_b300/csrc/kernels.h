@@ -13,9 +13,9 @@ int router_splits(int T, int d, int E, int num_sms);
 // partial[s][t][e] = sum over k in split s of x[t][k] * w_r[k][e]  (fp32)
 cudaError_t launch_router_logits(const uint16_t* x, const float* w_r, float* partial, int T, int d, int E,
                                  int splits, cudaStream_t stream);
-// sigmoid scores, group-limited top-k, normalised weights; sets the expert
-// bitmap bits when `bitmap` is non-null.
-cudaError_t launch_router_select(const float* partial, int splits, int T, int E, int n_groups, int topk_groups,
+// sums the split partials (in place into split 0), then sigmoid scores,
+// group-limited top-k and normalised weights.
+cudaError_t launch_router_select(float* partial, int splits, int T, int E, int n_groups, int topk_groups,
                                  int top_k, float routed_scale, int32_t* topk_idx, float* topk_w,
                                  int32_t* status, cudaStream_t stream);
 

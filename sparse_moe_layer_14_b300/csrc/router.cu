@@ -4,13 +4,14 @@
 // chosen, weights normalised then scaled by 2.5; FP32 router per section
 // "Residual stream").
 //
-// Two kernels:
+// Kernels:
 //  router_logits_kernel  FP32 SIMT GEMM, logits = x . W_r, with a split over
 //                        the hidden dimension when the batch is small so the
 //                        whole GPU streams W_r (decode batches).
-//  router_select_kernel  one warp per token: sums the split partials in a
-//                        fixed order, sigmoid, group top-2 sums, top groups,
-//                        top experts, normalisation.
+//  split_reduce_kernel   (split batches only) sums the split partials of each
+//                        logit in a fixed order, in place into split 0.
+//  router_select_kernel  one warp per token: sigmoid, group top-2 sums, top
+//                        groups, top experts, normalisation.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -90,6 +91,15 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const uint16_t* __re
   }
 }
 
+// part[0][t][e] = sum over s of part[s][t][e], s ascending.
+__global__ void __launch_bounds__(256) split_reduce_kernel(float* __restrict__ part, int splits, int64_t n) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  float l = part[i];
+  for (int sp = 1; sp < splits; ++sp) l += part[static_cast<size_t>(sp) * n + i];
+  part[i] = l;
+}
+
 // (value, index) order of the selection: larger value first, ties to the
 // lower index.
 __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
@@ -110,7 +120,7 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
 
 constexpr int kMaxPerLane = 8;  // E <= 256
 
-__global__ void __launch_bounds__(256) router_select_kernel(const float* __restrict__ part, int splits, int T,
+__global__ void __launch_bounds__(256) router_select_kernel(const float* __restrict__ logits, int T,
                                                             int E, int G, int Gk, int K, float scale,
                                                             int32_t* __restrict__ topk_idx,
                                                             float* __restrict__ topk_w, int32_t* status) {
@@ -125,11 +135,7 @@ __global__ void __launch_bounds__(256) router_select_kernel(const float* __restr
   for (int i = 0; i < kMaxPerLane; ++i) {
     const int e = lane + 32 * i;
     s[i] = kMasked;
-    if (e < E) {
-      float l = 0.f;
-      for (int sp = 0; sp < splits; ++sp) l += part[(static_cast<size_t>(sp) * T + t) * E + e];
-      s[i] = 1.0f / (1.0f + expf(-l));
-    }
+    if (e < E) s[i] = 1.0f / (1.0f + expf(-logits[static_cast<size_t>(t) * E + e]));
   }
 
   // group score: sum of the two largest scores of the group (lane g keeps group g's)
@@ -215,13 +221,15 @@ __global__ void __launch_bounds__(256) router_select_kernel(const float* __restr
 
 }  // namespace
 
+// Smallest split of the hidden dimension (into >= 64-element slices) that
+// gives at least one block per SM.
 int router_splits(int T, int d, int E, int num_sms) {
   const int tiles = ((T + RT - 1) / RT) * ((E + RE - 1) / RE);
-  const int target = (2 * num_sms + tiles - 1) / tiles;
+  const int target = (num_sms + tiles - 1) / tiles;
   const int chunks = d / RK;
   int best = 1;
   for (int s = 1; s <= chunks; ++s) {
-    if (chunks % s) continue;
+    if (chunks % s || d / s < 64) continue;
     best = s;
     if (s >= target) break;
   }
@@ -235,11 +243,15 @@ cudaError_t launch_router_logits(const uint16_t* x, const float* w_r, float* par
   return cudaGetLastError();
 }
 
-cudaError_t launch_router_select(const float* partial, int splits, int T, int E, int n_groups, int topk_groups,
+cudaError_t launch_router_select(float* partial, int splits, int T, int E, int n_groups, int topk_groups,
                                  int top_k, float routed_scale, int32_t* topk_idx, float* topk_w,
                                  int32_t* status, cudaStream_t stream) {
-  router_select_kernel<<<(T + 7) / 8, 256, 0, stream>>>(partial, splits, T, E, n_groups, topk_groups, top_k,
-                                                         routed_scale, topk_idx, topk_w, status);
+  if (splits > 1) {
+    const int64_t n = static_cast<int64_t>(T) * E;
+    split_reduce_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(partial, splits, n);
+  }
+  router_select_kernel<<<(T + 7) / 8, 256, 0, stream>>>(partial, T, E, n_groups, topk_groups, top_k, routed_scale,
+                                                         topk_idx, topk_w, status);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,88 @@
+"""Host logic of bench.py that needs no GPU: the multi-rank aggregation (world size 2,
+gloo on CPU), the reference arm's rank handling, clock-sample parsing and the
+roofline arithmetic."""
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+import workload as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        got = bench.max_over_ranks(10.0 + 5.0 * rank, world, "cpu")
+        q.put((rank, got))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_world2_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    res = dict(q.get(timeout=10) for _ in range(2))
+    assert res == {0: 15.0, 1: 15.0}
+    assert bench.max_over_ranks(3.5, 1, "cpu") == 3.5
+
+
+def test_reference_arm_only_rank0_runs():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1"],
+                       env=env, capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_clock_summary_flags_throttle():
+    cs = bench.ClockSampler.__new__(bench.ClockSampler)
+    cs.samples = [(1.0, ["1900", "2032", "700.5", "Not Active", "Not Active", "Not Active", "Active"]),
+                  (1.1, ["1950", "2032", "710.0", "Not Active", "Active", "Not Active", "Not Active"]),
+                  (5.0, ["300", "2032", "100.0", "Not Active", "Not Active", "Not Active", "Not Active"])]
+    s = cs.summary(0.5, 2.0)
+    assert s["samples"] == 2 and s["sm_mhz"] == 1925.0 and s["sm_max_mhz"] == 2032.0
+    assert s["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
+    s2 = cs.summary(4.0, 4.01)  # shorter than the sampling period: nearest samples
+    assert s2["samples"] == 3 and "nearest" in s2["window"]
+
+
+def test_roofline_arithmetic():
+    cfg = W.CONFIGS["decode"]
+    peaks = {"hbm_gbs": 6500.0, "bf16_tflops": 1800.0}
+    g1, g2, layer = bench.roofline_numbers(cfg, 222, peaks)
+    R = 64 * 8
+    assert layer["flops"] == 2.0 * R * 3 * 5120 * 2560 + 2.0 * 64 * 5120 * 256
+    assert layer["bytes"] == 222 * 3 * 5120 * 2560 * 2 + 5120 * 256 * 4 + 64 * 5120 * 2 * 2
+    assert g1["bound"] == g2["bound"] == layer["bound"] == "hbm"
+    big = bench.roofline_numbers(W.CONFIGS["skewed"], 256, peaks)
+    assert big[0]["bound"] == "tensor"
+
+
+def test_router_split_rule():
+    # decode: 2 tiles of 64 tokens x 128 experts -> split the hidden dim 80 ways (64-element slices)
+    assert bench.router_splits(64, 5120, 256, 148) == 80
+    assert bench.router_splits(4096, 5120, 256, 148) == 2
+    assert bench.router_splits(32768, 5120, 256, 148) == 1
+    assert bench.kernels_per_step(W.CONFIGS["skewed"], 148) == 10
+    assert bench.kernels_per_step(W.CONFIGS["decode"], 148) == 11
