@@ -36,7 +36,6 @@ sys.path.insert(0, ROOT)
 import workload as W  # noqa: E402  (seeded input generators only)
 
 METRIC = "MoE-layer tokens/s at Beam shape (T=64 decode, T=4096 prefill); % of roofline"
-# router logits, (split reduce), router select, bitmap, column scan, offsets, gather, schedule, GEMM1, GEMM2, combine
 
 
 def router_splits(T, d, E, num_sms):
@@ -54,8 +53,18 @@ def router_splits(T, d, E, num_sms):
     return best
 
 
+ROUTER_TC_MIN_TOKENS = 1024  # the library routes batches this large on the tensor cores
+
+
 def kernels_per_step(cfg, num_sms):
-    return 10 + (1 if router_splits(cfg.T, cfg.d, cfg.E, num_sms) > 1 else 0)
+    """Kernels one moe_forward launches: router (tensor-core: W_r split, tensor-core selection,
+    fp32 refinement, narrow-margin recompute; SIMT: logits [+ split reduce] + select),
+    permute (4), schedule, GEMM1, GEMM2, combine."""
+    if cfg.T >= ROUTER_TC_MIN_TOKENS:
+        router = 4
+    else:
+        router = 2 + (1 if router_splits(cfg.T, cfg.d, cfg.E, num_sms) > 1 else 0)
+    return router + 4 + 1 + 2 + 1
 
 
 def max_over_ranks(value, world, device):
@@ -186,10 +195,20 @@ class ClockSampler:
 # ----------------------------------------------------------------------------- ours
 
 def make_device_weights(cfg, seed, torch, keep_host):
-    """Seeded bf16 expert weights generated expert by expert on the host and copied to the device."""
+    """Seeded expert weights generated expert by expert on the host and copied to the device
+    (NVFP4: quantised from the same seeded bf16 draws)."""
     import sparse_moe_layer_14_b300 as bm
     host = {}
     tens = {}
+    if cfg.wfmt == "nvfp4":
+        for which in ("gate", "up", "down"):
+            p, s, ts = W.gen_expert_nvfp4(cfg, seed, which, 0, cfg.E)
+            tens[which] = torch.from_numpy(p).cuda()
+            tens[which + "_sf"] = torch.from_numpy(s).cuda()
+            tens[which + "_ts"] = torch.from_numpy(ts).cuda()
+            if keep_host:
+                host[which], host[which + "_sf"], host[which + "_ts"] = p, s, ts
+        return bm.ExpertWeights(**tens), host
     for which in ("gate", "up", "down"):
         N_, K_ = W.weight_shape(cfg, which)
         t = torch.empty((cfg.E, N_, K_), dtype=torch.bfloat16, device="cuda")
@@ -209,13 +228,19 @@ def make_device_weights(cfg, seed, torch, keep_host):
     return bm.ExpertWeights(tens["gate"], tens["up"], tens["down"]), host
 
 
+def weight_bytes_per_param(cfg):
+    """bf16: 2 B; NVFP4: 0.5 B of e2m1 code + 1/16 B of e4m3 block scale."""
+    return 2.0 if cfg.wfmt == "bf16" else 0.5 + 1.0 / 16
+
+
 def roofline_numbers(cfg, touched, peaks):
     """Algorithmic bytes and FLOPs of the layer and of each expert GEMM launch."""
     R = cfg.T * cfg.top_k
     d, I, E = cfg.d, cfg.inter, cfg.E
-    w_bytes_expert = 3 * d * I * 2
-    gemm1 = {"bytes": touched * 2 * I * d * 2 + R * d * 2 + R * I * 2, "flops": 2.0 * R * d * 2 * I}
-    gemm2 = {"bytes": touched * d * I * 2 + R * I * 2 + R * d * 4, "flops": 2.0 * R * I * d}
+    bpp = weight_bytes_per_param(cfg)
+    w_bytes_expert = 3 * d * I * bpp
+    gemm1 = {"bytes": touched * 2 * I * d * bpp + R * d * 2 + R * I * 2, "flops": 2.0 * R * d * 2 * I}
+    gemm2 = {"bytes": touched * d * I * bpp + R * I * 2 + R * d * 4, "flops": 2.0 * R * I * d}
     layer = {"bytes": touched * w_bytes_expert + d * E * 4 + cfg.T * d * 2 * 2,
              "flops": 2.0 * R * 3 * d * I + 2.0 * cfg.T * d * E}
     for x in (gemm1, gemm2, layer):
@@ -232,8 +257,6 @@ def run_ours(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     cfg = workload_cfg(args.workload)
-    if cfg.wfmt != "bf16":
-        raise SystemExit("the NVFP4 expert path is not built in this library version")
     peaks = load_peaks()
     want_cpu = (rank == 0 and world == 1 and not args.no_cpu_baseline)
     dims = bm.Dims.from_config(cfg)
@@ -327,16 +350,17 @@ def run_ours(args, rank, world, local_rank):
         achieved, peak, unit = g1["bytes"] / gemm1_s / 1e9, peaks["hbm_gbs"], "GB/s"
     else:
         achieved, peak, unit = g1["flops"] / gemm1_s / 1e12, peaks["bf16_tflops"], "TFLOP/s"
-    traffic, traffic_src = profiled_traffic("expert_gemm_kernel<GLU>", g1["bytes"])
+    traffic, traffic_src = (profiled_traffic("expert_gemm_kernel<GLU>", g1["bytes"]) if cfg.wfmt == "bf16"
+                            else (None, "no capture of the NVFP4 kernel"))
     line = {
         "metric": METRIC, "value": round(tokens_per_s, 1), "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) activations, N(0,1/fan_in) weights)",
+        "vs_baseline": None, "dtype": "bf16" if cfg.wfmt == "bf16" else "bf16 (NVFP4 weights decoded to bf16)", "data": "synthetic (seeded N(0,1) activations, N(0,1/fan_in) weights)",
         "impl": "ours",
         "config": {"workload": describe(cfg), "T": cfg.T, "d": cfg.d, "E": cfg.E, "inter": cfg.inter,
                    "top_k": cfg.top_k, "parallelism": f"replicas x{world}",
-                   "l2": f"no flush: {touched} experts x {3 * cfg.d * cfg.inter * 2 / 1e6:.1f} MB of weights streamed "
-                         f"per step exceed the 126 MB L2"},
+                   "l2": f"no flush: {touched} experts x {3 * cfg.d * cfg.inter * weight_bytes_per_param(cfg) / 1e6:.1f} MB "
+                         f"of weights streamed per step exceed the 126 MB L2"},
         "roofline": {"kernel": "expert_gemm_kernel<GLU> (GEMM1 + SwiGLU)", "bound": bound,
                      "achieved": round(achieved, 1), "peak": peak, "unit": unit, "frac": round(achieved / peak, 4),
                      "peak_source": f"{peaks['source']} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops'})",
@@ -352,6 +376,7 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": round(world * cfg.T / (e2e_ms / K / 1e3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": cfg.T * cfg.d * 2, "d2h_bytes_per_step": cfg.T * cfg.d * 2,
                 "ms_per_step": round(e2e_ms / K, 4)},
+        "router_fp32_recomputed_tokens": int(ws[16:20].view(torch.int32).item()) if cfg.T >= ROUTER_TC_MIN_TOKENS else None,
         "gpu_launches": kernels_per_step(cfg, torch.cuda.get_device_properties(local_rank).multi_processor_count) * K,
         "clocks": clk,
         "setup_s": round(setup_s, 1),

@@ -43,6 +43,7 @@ def build(force: bool = False, verbose: bool = False, extra: list[str] | None = 
         return LIB
     tmp = LIB + f".tmp{os.getpid()}"
     cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "--shared", "-Xcompiler", "-fPIC,-O3",
+           "-Xlinker", "--no-undefined",
            "-I", os.path.join(ROOT, "include"), "-o", tmp, *[os.path.join(CSRC, s) for s in SOURCES]]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")

@@ -25,7 +25,7 @@ cudaError_t mark(int i, cudaStream_t s) {
 size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 
 enum Region {
-  R_HDR, R_PART, R_BITMAP, R_WPRE, R_COUNTS, R_OFFS, R_IDX, R_W, R_ROWTOK, R_INVROW,
+  R_HDR, R_PART, R_WSPLIT, R_BITMAP, R_WPRE, R_COUNTS, R_OFFS, R_IDX, R_W, R_ROWTOK, R_INVROW,
   R_ITEMS1, R_ITEMS2, R_XPERM, R_H, R_Y, R_NUM
 };
 
@@ -47,6 +47,7 @@ Layout make_layout(const moe_dims_t& d) {
   size_t sz[R_NUM];
   sz[R_HDR] = sizeof(WsHeader);
   sz[R_PART] = sizeof(float) * static_cast<size_t>(splits) * T * d.E;
+  sz[R_WSPLIT] = router_uses_tensor_cores(d.T, d.E) ? router_tc_scratch_bytes(d.T, d.d, d.E) : 0;
   sz[R_BITMAP] = sizeof(uint32_t) * static_cast<size_t>(d.E) * nw;
   sz[R_WPRE] = sizeof(int32_t) * static_cast<size_t>(d.E) * nw;
   sz[R_COUNTS] = sizeof(int32_t) * d.E;
@@ -124,6 +125,11 @@ int32_t* status_word(void* ws) { return ws ? &reinterpret_cast<WsHeader*>(ws)->s
 
 moe_status_t do_route(const moe_dims_t* d, const uint16_t* x, const float* w_r, int32_t* idx, float* w,
                       void* ws, const Layout& L, cudaStream_t s) {
+  if (router_uses_tensor_cores(d->T, d->E))
+    return cuda_status(launch_router_tc(x, w_r, region<uint8_t>(ws, L, R_WSPLIT),
+                                        &reinterpret_cast<WsHeader*>(ws)->router_flagged, d->T, d->d, d->E, d->n_groups,
+                                        d->topk_groups, d->top_k, d->routed_scale, idx, w, status_word(ws),
+                                        num_sms(), s));
   const int splits = router_splits(d->T, d->d, d->E, num_sms());
   float* part = region<float>(ws, L, R_PART);
   cudaError_t e = launch_router_logits(x, w_r, part, d->T, d->d, d->E, splits, s);

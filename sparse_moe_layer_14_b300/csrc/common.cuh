@@ -18,7 +18,8 @@ struct WsHeader {
   int32_t status;        // first moe_device_code_t latched by any kernel
   int32_t timeout_where; // role id of the first wait that expired (diagnostics)
   int32_t n_items[2];    // expert-GEMM work items (GEMM1, GEMM2) built on the device
-  int32_t pad[60];
+  int32_t router_flagged; // tokens the tensor-core router recomputed in fp32 (last call)
+  int32_t pad[59];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 

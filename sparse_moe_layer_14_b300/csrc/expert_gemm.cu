@@ -1,6 +1,7 @@
 // Expert SwiGLU MLPs of the Beam MoE block as two grouped GEMMs on the
 // sm_103a tensor cores (release article, section "Mixture of Experts": each
-// expert is a SwiGLU MLP with intermediate size 2,560; section "Residual
+// expert is a SwiGLU MLP with intermediate size 2,560; the NVFP4 checkpoint
+// stores most parameters in 4-bit precision for Blackwell; section "Residual
 // stream": the SwiGLU product is computed in FP32).
 //
 //   GEMM1 + SwiGLU:  h[r][i] = bf16( silu(x_perm[r].Wg_e[i]) * (x_perm[r].Wu_e[i]) )
@@ -14,10 +15,14 @@
 // streamed from HBM once per token tile. Accumulators live in TMEM:
 // D[weight row][token], fp32.
 //
-// One persistent CTA per SM, 192 threads:
+// One persistent CTA per SM:
 //   warp 0      TMA producer: weight tile(s) + token rows per 64-wide K slice
 //   warp 1      TMEM allocator and single-thread tcgen05.mma issuer
 //   warps 2..5  epilogue: tcgen05.ld, SwiGLU in FP32 (GEMM1) or fp32 store
+//   warps 6..9  (NVFP4 weights only) converters: e2m1 codes times their e4m3
+//               block scale, which is exact in bf16, written in the 128-byte
+//               swizzled operand layout the MMA reads; the fp32 tensor scale
+//               is applied to the accumulator in the epilogue.
 // Work items {expert, weight tile, first row, tokens} are built on the device
 // from the expert offsets (no host synchronisation) and taken round-robin.
 // Every mbarrier wait is bounded; on expiry the CTA latches MOE_DEV_TIMEOUT,
@@ -36,29 +41,35 @@ constexpr int BK = 64;        // K elements per pipeline stage (128 bytes of bf1
 constexpr int TOK_BOX = 16;   // token rows per TMA box
 constexpr int kMaxStages = 8;
 constexpr int kMaxAcc = 4;
-constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kATileBytes = BM * BK * 2;            // 16 KB
+constexpr uint32_t kATileBytes = BM * BK * 2;            // 16 KB bf16 weight tile
+constexpr uint32_t kPTileBytes = BM * BK / 2;            // 4 KB packed e2m1 weight tile
 constexpr uint32_t kTokBoxBytes = TOK_BOX * BK * 2;      // 2 KB
 constexpr uint64_t kDrainNs = 1000000000ull;             // 1 s bound for draining on abort
 constexpr uint64_t kWaitNs = 2000000000ull;              // 2 s bound of a pipeline wait
 constexpr int kSmemLimit = 232448;                       // 227 KB opt-in per block
+
+constexpr int threads_for(bool w4) { return w4 ? 320 : 192; }
 
 struct GemmArgs {
   const int4* items;
   const int32_t* n_items;
   int K;           // reduction length
   int Nw;          // weight rows per expert = output columns
+  int E;           // experts
   int n_max;       // max tokens per item (multiple of 16)
   int stages;
   int acc_bufs;
   int acc_cols;    // TMEM columns per accumulator buffer
   uint32_t stage_bytes;
   uint32_t b_offset;  // token tile offset inside a stage
+  uint32_t p_offset;  // packed weight tile offset inside a stage (NVFP4)
   uint16_t* h_out;    // GEMM1 output [R][Nw] bf16
   float* y_out;       // GEMM2 output [R][Nw] fp32
   const float* ts0;   // per-expert scale applied to accumulator 0 (NVFP4), or null
   const float* ts1;
+  const uint8_t* sf0;  // e4m3 block scales [E*Nw][K/16] of matrix 0 (NVFP4)
+  const uint8_t* sf1;
   int32_t* status;
   int32_t* timeout_where;
   long long wait_spins;
@@ -70,12 +81,69 @@ __device__ __forceinline__ void fail(const GemmArgs& p, volatile int* abort, int
   *abort = 1;
 }
 
-template <bool kGLU>
-__global__ void __launch_bounds__(kThreads, 1)
+__device__ __forceinline__ void fence_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 8 e2m1 codes (one 32-bit word, element 2j in the low nibble of byte j) times
+// one e4m3 scale (broadcast in both halves of `scale2`, as f16x2) -> 8 bf16,
+// returned as four bf16x2 words in element order. Every product has at most
+// 6 significant bits, so f16 and bf16 represent it exactly.
+__device__ __forceinline__ uint4 decode8(uint32_t codes, uint32_t scale2) {
+  uint32_t h[4];
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}\n"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(codes));
+  uint32_t out[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t prod;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(prod) : "r"(h[i]), "r"(scale2));
+    const __half2 ph = *reinterpret_cast<const __half2*>(&prod);
+    const __nv_bfloat162 b = __floats2bfloat162_rn(__low2float(ph), __high2float(ph));
+    out[i] = *reinterpret_cast<const uint32_t*>(&b);
+  }
+  return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+// e4m3 scale byte -> (s, s) as f16x2.
+__device__ __forceinline__ uint32_t scale_pair(uint32_t byte) {
+  const uint16_t two = static_cast<uint16_t>(byte * 0x0101u);
+  uint32_t s;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s) : "h"(two));
+  return s;
+}
+
+// Decode row r of one packed 128 x 64 weight tile into the 128-byte swizzled
+// bf16 tile: 16-byte chunk c of row r lives at chunk (c ^ (r & 7)).
+// `sc` holds the row's four block scales of this K slice (byte j: elements
+// 16j..16j+15).
+__device__ __forceinline__ void decode_row(const uint8_t* packed_tile, uint8_t* bf16_tile, int r, uint32_t sc) {
+  const uint4 p0 = *reinterpret_cast<const uint4*>(packed_tile + r * 32);
+  const uint4 p1 = *reinterpret_cast<const uint4*>(packed_tile + r * 32 + 16);
+  const uint32_t w[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+  uint8_t* row = bf16_tile + r * 128;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t s2 = scale_pair((sc >> (8 * j)) & 0xFFu);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int c = 2 * j + h;
+      *reinterpret_cast<uint4*>(row + ((c ^ (r & 7)) << 4)) = decode8(w[c], s2);
+    }
+  }
+}
+
+template <bool kGLU, bool kW4>
+__global__ void __launch_bounds__(threads_for(kW4), 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
-                       const __grid_constant__ CUtensorMap tmB, const GemmArgs p) {
+                       const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB64,
+                       const __grid_constant__ CUtensorMap tmB128, const GemmArgs p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t conv_bar[kMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
   __shared__ __align__(8) uint64_t accf_bar[kMaxAcc];
   __shared__ __align__(8) uint64_t acce_bar[kMaxAcc];
@@ -90,6 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(&full_bar[s], 1);
+      mbar_init(&conv_bar[s], 128);
       mbar_init(&empty_bar[s], 1);
     }
     for (int a = 0; a < p.acc_bufs; ++a) {
@@ -102,6 +171,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmA0);
     if (kGLU) tma_prefetch_desc(&tmA1);
     tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmB64);
+    tma_prefetch_desc(&tmB128);
   }
   if (warp == 1) {
     tmem_alloc(&tmem_slot, kTmemCols);
@@ -114,6 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = tmem_slot;
   const int n_items = *p.n_items;
   const int kblocks = p.K / BK;
+  constexpr int nA = kGLU ? 2 : 1;
   long long fills = 0;  // TMA stage fills issued (thread 0 only)
 
   if (warp == 0) {
@@ -126,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int4 item = p.items[it];
         const int a_row = item.x * p.Nw + item.y * BM;
         const int nbox = (item.w + TOK_BOX - 1) / TOK_BOX;
-        const uint32_t bytes = kATileBytes * (kGLU ? 2u : 1u) + static_cast<uint32_t>(nbox) * kTokBoxBytes;
+        const uint32_t bytes = (kW4 ? kPTileBytes : kATileBytes) * nA + static_cast<uint32_t>(nbox) * kTokBoxBytes;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, p.wait_spins, kWaitNs, abort)) {
             if (!*abort) fail(p, abort, 1);
@@ -135,11 +207,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint8_t* st = smem + static_cast<size_t>(stage) * p.stage_bytes;
           mbar_arrive_expect_tx(&full_bar[stage], bytes);
-          tma_load_2d(st, &tmA0, kb * BK, a_row, &full_bar[stage]);
-          if (kGLU) tma_load_2d(st + kATileBytes, &tmA1, kb * BK, a_row, &full_bar[stage]);
+          if (kW4) {
+            // packed codes: 32 bytes (64 elements) per row
+            tma_load_2d(st + p.p_offset, &tmA0, kb * (BK / 2), a_row, &full_bar[stage]);
+            if (kGLU) tma_load_2d(st + p.p_offset + kPTileBytes, &tmA1, kb * (BK / 2), a_row, &full_bar[stage]);
+          } else {
+            tma_load_2d(st, &tmA0, kb * BK, a_row, &full_bar[stage]);
+            if (kGLU) tma_load_2d(st + kATileBytes, &tmA1, kb * BK, a_row, &full_bar[stage]);
+          }
+          // token rows in boxes of 128, 64 and 16 rows (fewest copies); the
+          // stacked boxes form one 128-byte-swizzled K-major tile
           uint8_t* sb = st + p.b_offset;
-          for (int j = 0; j < nbox; ++j)
-            tma_load_2d(sb + j * kTokBoxBytes, &tmB, kb * BK, item.z + j * TOK_BOX, &full_bar[stage]);
+          int row = item.z, left = nbox * TOK_BOX;
+          for (; left >= 128; left -= 128, row += 128, sb += 128 * BK * 2)
+            tma_load_2d(sb, &tmB128, kb * BK, row, &full_bar[stage]);
+          if (left >= 64) {
+            tma_load_2d(sb, &tmB64, kb * BK, row, &full_bar[stage]);
+            left -= 64;
+            row += 64;
+            sb += 64 * BK * 2;
+          }
+          for (; left > 0; left -= TOK_BOX, row += TOK_BOX, sb += kTokBoxBytes)
+            tma_load_2d(sb, &tmB, kb * BK, row, &full_bar[stage]);
           ++fills;
           if (++stage == p.stages) {
             stage = 0;
@@ -153,6 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
+      uint64_t* ready = kW4 ? conv_bar : full_bar;
       for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
         const int4 item = p.items[it];
         const int n_mma = (item.w + 15) & ~15;
@@ -166,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t d1 = d0 + static_cast<uint32_t>(p.n_max);
         bool ok = true;
         for (int kb = 0; kb < kblocks; ++kb) {
-          if (!mbar_wait_bounded(&full_bar[stage], phase, p.wait_spins, kWaitNs, abort)) {
+          if (!mbar_wait_bounded(&ready[stage], phase, p.wait_spins, kWaitNs, abort)) {
             if (!*abort) fail(p, abort, 3);
             ok = false;
             break;
@@ -196,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else {
+  } else if (warp < 6) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int r = q * 32 + lane;
@@ -245,6 +335,56 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (++acc == p.acc_bufs) {
         acc = 0;
         acc_phase ^= 1u;
+      }
+    }
+  } else if (kW4) {
+    // ------------------------------------------------------------ NVFP4 converters
+    // Thread r decodes weight row r of every K slice. Block scales (4 per
+    // slice per row) are read 16 bytes (four slices) at a time from global
+    // memory, one group ahead, so the load latency hides behind decoding.
+    const int r = threadIdx.x - 192;
+    const int sf_ld = p.K / 16;        // bytes of block scales per weight row
+    const int64_t rows_total = static_cast<int64_t>(p.E) * p.Nw;
+    int stage = 0;
+    uint32_t phase = 0;
+    auto load_group = [&](int it, int g, uint4& s0, uint4& s1) {
+      s0 = make_uint4(0, 0, 0, 0);
+      s1 = make_uint4(0, 0, 0, 0);
+      if (it >= n_items) return;
+      const int4 item = p.items[it];
+      const int64_t row = static_cast<int64_t>(item.x) * p.Nw + item.y * BM + r;
+      if (row >= rows_total) return;  // padding rows past the last expert decode to zero
+      s0 = __ldg(reinterpret_cast<const uint4*>(p.sf0 + row * sf_ld + g * 16));
+      if (kGLU) s1 = __ldg(reinterpret_cast<const uint4*>(p.sf1 + row * sf_ld + g * 16));
+    };
+    uint4 cur0, cur1, nxt0, nxt1;
+    load_group(blockIdx.x, 0, nxt0, nxt1);
+    bool ok = true;
+    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if ((kb & 3) == 0) {
+          cur0 = nxt0;
+          cur1 = nxt1;
+          if (kb + 4 < kblocks) load_group(it, (kb >> 2) + 1, nxt0, nxt1);
+          else load_group(it + gridDim.x, 0, nxt0, nxt1);
+        }
+        if (!mbar_wait_bounded(&full_bar[stage], phase, p.wait_spins, kWaitNs, abort)) {
+          if (!*abort) fail(p, abort, 5);
+          ok = false;
+          break;
+        }
+        uint8_t* st = smem + static_cast<size_t>(stage) * p.stage_bytes;
+        const int q = kb & 3;
+        decode_row(st + p.p_offset, st, r, q == 0 ? cur0.x : q == 1 ? cur0.y : q == 2 ? cur0.z : cur0.w);
+        if (kGLU)
+          decode_row(st + p.p_offset + kPTileBytes, st + kATileBytes, r,
+                     q == 0 ? cur1.x : q == 1 ? cur1.y : q == 2 ? cur1.z : cur1.w);
+        fence_async_shared();  // generic-proxy writes -> visible to tcgen05.mma
+        mbar_arrive(&conv_bar[stage]);
+        if (++stage == p.stages) {
+          stage = 0;
+          phase ^= 1u;
+        }
       }
     }
   }
@@ -358,16 +498,34 @@ int encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t 
   return r == CUDA_SUCCESS ? 0 : static_cast<int>(r);
 }
 
+// 2-D byte tensor [outer][inner_bytes] of packed e2m1 codes, box [128][32 bytes]
+// (one 64-element K slice of 128 weight rows), no swizzle.
+int encode_packed_2d(CUtensorMap* map, const void* base, uint64_t inner_bytes, uint64_t outer) {
+  auto fn = encode_fn();
+  if (!fn) return -1;
+  cuuint64_t dims[2] = {inner_bytes, outer};
+  cuuint64_t strides[1] = {inner_bytes};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(BK / 2), static_cast<cuuint32_t>(BM)};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : static_cast<int>(r);
+}
+
 struct StageShape {
   int stages, acc_bufs, acc_cols;
-  uint32_t stage_bytes, b_offset;
+  uint32_t stage_bytes, b_offset, p_offset;
   size_t smem;
 };
 
-StageShape stage_shape(bool glu, int n_max) {
+StageShape stage_shape(bool glu, bool w4, int n_max) {
   StageShape s;
-  s.b_offset = kATileBytes * (glu ? 2u : 1u);
-  s.stage_bytes = s.b_offset + static_cast<uint32_t>(n_max) * BK * 2;
+  const uint32_t nA = glu ? 2u : 1u;
+  s.b_offset = kATileBytes * nA;
+  s.p_offset = s.b_offset + static_cast<uint32_t>(n_max) * BK * 2;
+  s.stage_bytes = s.p_offset + (w4 ? kPTileBytes * nA : 0u);
+  s.stage_bytes = (s.stage_bytes + 1023u) & ~1023u;
   const int budget = kSmemLimit - 1024 - 512;  // alignment slack + static barriers
   s.stages = std::min(kMaxStages, budget / static_cast<int>(s.stage_bytes));
   s.acc_cols = glu ? 2 * n_max : n_max;
@@ -376,20 +534,21 @@ StageShape stage_shape(bool glu, int n_max) {
   return s;
 }
 
-template <bool kGLU>
-cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b, GemmArgs args,
+template <bool kGLU, bool kW4>
+cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap (&b)[3], GemmArgs args,
                         int n_max, int grid, cudaStream_t stream) {
-  const StageShape s = stage_shape(kGLU, n_max);
+  const StageShape s = stage_shape(kGLU, kW4, n_max);
   args.stages = s.stages;
   args.acc_bufs = s.acc_bufs;
   args.acc_cols = s.acc_cols;
   args.stage_bytes = s.stage_bytes;
   args.b_offset = s.b_offset;
+  args.p_offset = s.p_offset;
   args.n_max = n_max;
-  cudaError_t err = cudaFuncSetAttribute(expert_gemm_kernel<kGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(s.smem));
+  cudaError_t err = cudaFuncSetAttribute(expert_gemm_kernel<kGLU, kW4>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s.smem));
   if (err != cudaSuccess) return err;
-  expert_gemm_kernel<kGLU><<<grid, kThreads, s.smem, stream>>>(a0, a1, b, args);
+  expert_gemm_kernel<kGLU, kW4><<<grid, threads_for(kW4), s.smem, stream>>>(a0, a1, b[0], b[1], b[2], args);
   return cudaGetLastError();
 }
 
@@ -397,9 +556,16 @@ cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUte
 
 ExpertPlan plan_experts(int T, int d, int E, int top_k, int inter) {
   ExpertPlan p;
-  const int tok = ((std::max(T, 1) + 15) / 16) * 16;  // an expert sees a token at most once
-  p.n_max = std::min(256, tok);
+  // Token tile: a quarter above the mean tokens per expert, at least 64 and at
+  // most 256 (the MMA's largest N), never above the batch (an expert sees a
+  // token at most once). Smaller tiles leave shared memory for more pipeline
+  // stages; experts above the tile are split into near-equal tiles.
   const int64_t R = static_cast<int64_t>(T) * top_k;
+  const int64_t mean = (R + E - 1) / std::max(E, 1);
+  int64_t n = ((mean + mean / 4 + 15) / 16) * 16;
+  n = std::max<int64_t>(64, std::min<int64_t>(256, n));
+  const int tok = ((std::max(T, 1) + 15) / 16) * 16;
+  p.n_max = static_cast<int>(std::min<int64_t>(n, tok));
   p.max_tiles = static_cast<int>(E + (R + p.n_max - 1) / p.n_max);
   p.wtiles1 = (inter + BM - 1) / BM;
   p.wtiles2 = (d + BM - 1) / BM;
@@ -413,19 +579,29 @@ cudaError_t launch_expert_ffn(const ExpertPlan& plan, const ExpertBuffers& buf, 
                               cudaStream_t stream, int* cu_error, cudaEvent_t after_gemm1) {
   *cu_error = 0;
   const int R = T * top_k;
+  const bool w4 = w.wfmt == MOE_W_NVFP4;
+  if (w4 && ((d % 256) || (inter % 256))) return cudaErrorNotSupported;
   schedule_kernel<<<1, 256, 0, stream>>>(buf.offsets, E, R, plan.n_max, plan.wtiles1, plan.wtiles2, buf.items1,
                                          buf.items2, buf.n_items, buf.status);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  if (w.wfmt != MOE_W_BF16) return cudaErrorNotSupported;
 
-  CUtensorMap tg, tu, tx, td, th;
+  CUtensorMap tg, tu, td, tx[3], th[3];
   int rc = 0;
-  rc |= encode_bf16_2d(&tg, w.gate, d, static_cast<uint64_t>(E) * inter, BM);
-  rc |= encode_bf16_2d(&tu, w.up, d, static_cast<uint64_t>(E) * inter, BM);
-  rc |= encode_bf16_2d(&tx, buf.x_perm, d, R, TOK_BOX);
-  rc |= encode_bf16_2d(&td, w.down, inter, static_cast<uint64_t>(E) * d, BM);
-  rc |= encode_bf16_2d(&th, buf.h, inter, R, TOK_BOX);
+  if (w4) {
+    rc |= encode_packed_2d(&tg, w.gate, d / 2, static_cast<uint64_t>(E) * inter);
+    rc |= encode_packed_2d(&tu, w.up, d / 2, static_cast<uint64_t>(E) * inter);
+    rc |= encode_packed_2d(&td, w.down, inter / 2, static_cast<uint64_t>(E) * d);
+  } else {
+    rc |= encode_bf16_2d(&tg, w.gate, d, static_cast<uint64_t>(E) * inter, BM);
+    rc |= encode_bf16_2d(&tu, w.up, d, static_cast<uint64_t>(E) * inter, BM);
+    rc |= encode_bf16_2d(&td, w.down, inter, static_cast<uint64_t>(E) * d, BM);
+  }
+  const uint32_t boxes[3] = {TOK_BOX, 64, 128};
+  for (int i = 0; i < 3; ++i) {
+    rc |= encode_bf16_2d(&tx[i], buf.x_perm, d, R, boxes[i]);
+    rc |= encode_bf16_2d(&th[i], buf.h, inter, R, boxes[i]);
+  }
   if (rc) {
     *cu_error = rc;
     return cudaErrorInvalidValue;
@@ -435,11 +611,20 @@ cudaError_t launch_expert_ffn(const ExpertPlan& plan, const ExpertBuffers& buf, 
   a1.n_items = buf.n_items;
   a1.K = d;
   a1.Nw = inter;
+  a1.E = E;
   a1.h_out = buf.h;
   a1.status = buf.status;
   a1.timeout_where = buf.timeout_where;
   a1.wait_spins = wait_spins;
-  err = launch_gemm<true>(tg, tu, tx, a1, plan.n_max, num_sms, stream);
+  if (w4) {
+    a1.ts0 = w.gate_ts;
+    a1.ts1 = w.up_ts;
+    a1.sf0 = w.gate_sf;
+    a1.sf1 = w.up_sf;
+    err = launch_gemm<true, true>(tg, tu, tx, a1, plan.n_max, num_sms, stream);
+  } else {
+    err = launch_gemm<true, false>(tg, tu, tx, a1, plan.n_max, num_sms, stream);
+  }
   if (err != cudaSuccess) return err;
   if (after_gemm1 && (err = cudaEventRecord(after_gemm1, stream)) != cudaSuccess) return err;
   GemmArgs a2{};
@@ -447,11 +632,17 @@ cudaError_t launch_expert_ffn(const ExpertPlan& plan, const ExpertBuffers& buf, 
   a2.n_items = buf.n_items + 1;
   a2.K = inter;
   a2.Nw = d;
+  a2.E = E;
   a2.y_out = buf.y;
   a2.status = buf.status;
   a2.timeout_where = buf.timeout_where;
   a2.wait_spins = wait_spins;
-  return launch_gemm<false>(td, td, th, a2, plan.n_max, num_sms, stream);
+  if (w4) {
+    a2.ts0 = w.down_ts;
+    a2.sf0 = w.down_sf;
+    return launch_gemm<false, true>(td, td, th, a2, plan.n_max, num_sms, stream);
+  }
+  return launch_gemm<false, false>(td, td, th, a2, plan.n_max, num_sms, stream);
 }
 
 }  // namespace beammoe

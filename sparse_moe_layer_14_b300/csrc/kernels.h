@@ -19,6 +19,19 @@ cudaError_t launch_router_select(float* partial, int splits, int T, int E, int n
                                  int top_k, float routed_scale, int32_t* topk_idx, float* topk_w,
                                  int32_t* status, cudaStream_t stream);
 
+// Tensor-core router for large batches (T >= kRouterTcMinTokens): W_r split
+// into three bf16 terms, logits and a provisional selection per 128 tokens on
+// the tensor cores, then an fp32 FFMA refinement (chosen experts' logits for
+// every token; all logits for tokens with a narrow tensor-core margin).
+// `scratch` holds router_tc_scratch_bytes(T, d, E) bytes.
+constexpr int kRouterTcMinTokens = 1024;
+int router_epad(int E);
+bool router_uses_tensor_cores(int T, int E);
+size_t router_tc_scratch_bytes(int T, int d, int E);
+cudaError_t launch_router_tc(const uint16_t* x, const float* w_r, void* scratch, int32_t* flagged_count, int T,
+                             int d, int E, int n_groups, int topk_groups, int top_k, float routed_scale,
+                             int32_t* topk_idx, float* topk_w, int32_t* status, int num_sms, cudaStream_t stream);
+
 // ---- permutation (permute.cu) ----
 int bitmap_words(int T);
 cudaError_t launch_permute(const uint16_t* x, const int32_t* topk_idx, int T, int d, int E, int top_k,

@@ -4,14 +4,35 @@
 // chosen, weights normalised then scaled by 2.5; FP32 router per section
 // "Residual stream").
 //
-// Kernels:
+// Small batches (decode):
 //  router_logits_kernel  FP32 SIMT GEMM, logits = x . W_r, with a split over
-//                        the hidden dimension when the batch is small so the
-//                        whole GPU streams W_r (decode batches).
-//  split_reduce_kernel   (split batches only) sums the split partials of each
-//                        logit in a fixed order, in place into split 0.
+//                        the hidden dimension so the whole GPU streams W_r.
+//  split_reduce_kernel   sums the split partials of each logit in a fixed
+//                        order, in place into split 0.
 //  router_select_kernel  one warp per token: sigmoid, group top-2 sums, top
 //                        groups, top experts, normalisation.
+// Large batches (prefill):
+//  wr_split_kernel       W_r (fp32, [d][E]) -> three bf16 matrices hi, mid,
+//                        lo ([E_pad][d], K-contiguous) with hi + mid + lo = W_r
+//                        (8 + 8 + 8 significant bits cover fp32's 24).
+//  router_tc_kernel      per 128 tokens: logits = x.hi + x.mid + x.lo on the
+//                        tcgen05 tensor cores (x is exact in bf16, so every
+//                        product is exact in fp32), then in the epilogue each
+//                        thread takes one token: sigmoid, group scores, kept
+//                        groups, chosen experts, and the two decision margins.
+//                        The tensor cores' fp32 accumulation is measurably
+//                        coarser than FFMA (logit errors up to ~4e-5 with the
+//                        small mid/lo products in their own accumulator, ~5e-6
+//                        for FFMA, on Beam-shape inputs), so this pass only
+//                        picks the expert set, and only where both margins
+//                        are wide:
+//  router_refine_kernel  one warp per token: the chosen experts' logits again,
+//                        as FFMA dot products in fp32; their scores give the
+//                        slot order and the weights.
+//  router_flagged_kernel tokens whose tensor-core margin was narrow: all
+//                        logits in fp32 FFMA and the full warp selection.
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -120,23 +141,13 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
 
 constexpr int kMaxPerLane = 8;  // E <= 256
 
-__global__ void __launch_bounds__(256) router_select_kernel(const float* __restrict__ logits, int T,
-                                                            int E, int G, int Gk, int K, float scale,
-                                                            int32_t* __restrict__ topk_idx,
-                                                            float* __restrict__ topk_w, int32_t* status) {
-  const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (t >= T) return;
+// Group-limited selection of one token by one warp. Lane l holds the scores
+// of experts l, l+32, l+64, ... in s[]; writes the token's K expert ids (slot
+// order: descending score, ties to the lower id) and weights.
+__device__ void warp_select(const float (&s)[kMaxPerLane], int lane, int t, int E, int G, int Gk, int K, float scale,
+                            int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int32_t* status) {
   const int gsz = E / G;
   constexpr float kMasked = -1.0f;  // below every sigmoid score
-
-  float s[kMaxPerLane];
-#pragma unroll
-  for (int i = 0; i < kMaxPerLane; ++i) {
-    const int e = lane + 32 * i;
-    s[i] = kMasked;
-    if (e < E) s[i] = 1.0f / (1.0f + expf(-logits[static_cast<size_t>(t) * E + e]));
-  }
 
   // group score: sum of the two largest scores of the group (lane g keeps group g's)
   float my_gs = kMasked;
@@ -219,7 +230,499 @@ __global__ void __launch_bounds__(256) router_select_kernel(const float* __restr
   }
 }
 
+__global__ void __launch_bounds__(256) router_select_kernel(const float* __restrict__ logits, int T,
+                                                            int E, int G, int Gk, int K, float scale,
+                                                            int32_t* __restrict__ topk_idx,
+                                                            float* __restrict__ topk_w, int32_t* status) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= T) return;
+  float s[kMaxPerLane];
+#pragma unroll
+  for (int i = 0; i < kMaxPerLane; ++i) {
+    const int e = lane + 32 * i;
+    s[i] = (e < E) ? 1.0f / (1.0f + expf(-logits[static_cast<size_t>(t) * E + e])) : -1.0f;
+  }
+  warp_select(s, lane, t, E, G, Gk, K, scale, topk_idx, topk_w, status);
+}
+
+// ---------------------------------------------------------------- tensor-core path
+
+constexpr int kTcTokens = 128;  // tokens per CTA (MMA M)
+constexpr int kTcBK = 64;       // hidden elements per pipeline stage
+constexpr int kTcStages = 2;
+constexpr uint64_t kTcWaitNs = 2000000000ull;
+constexpr uint64_t kTcDrainNs = 1000000000ull;
+
+// out[s][e][k] = bf16 split s of W_r[k][e] (rows e >= E are zero);
+// wt[e][k] = W_r[k][e] in fp32. Also resets the flagged-token count.
+__global__ void __launch_bounds__(256) wr_split_kernel(const float* __restrict__ wr, int d, int E, int E_pad,
+                                                       uint16_t* __restrict__ out, float* __restrict__ wt,
+                                                       int32_t* __restrict__ flagged_count) {
+  __shared__ float tile[32][33];
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *flagged_count = 0;
+  const int k0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
+  for (int i = ty; i < 32; i += 8) {
+    const int e = e0 + tx;
+    tile[i][tx] = (e < E) ? wr[static_cast<size_t>(k0 + i) * E + e] : 0.f;
+  }
+  __syncthreads();
+  for (int i = ty; i < 32; i += 8) {
+    const int e = e0 + i, k = k0 + tx;
+    if (e >= E_pad) continue;
+    const float w = tile[tx][i];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+    const float r1 = w - __bfloat162float(hi);
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+    const size_t o = static_cast<size_t>(e) * d + k;
+    const size_t plane = static_cast<size_t>(E_pad) * d;
+    out[o] = __bfloat16_as_ushort(hi);
+    out[plane + o] = __bfloat16_as_ushort(mid);
+    out[2 * plane + o] = __bfloat16_as_ushort(lo);
+    if (e < E) wt[static_cast<size_t>(e) * d + k] = w;
+  }
+}
+
+struct TcArgs {
+  int T, d, E, E_pad, G, Gk, K;
+  float scale;
+  int32_t* topk_idx;
+  float* topk_w;
+  int32_t* status;
+  int32_t* flags;          // [T]: 1 = narrow tensor-core margin, recomputed in full
+  int32_t* flagged;        // [T]: list of flagged tokens
+  int32_t* flagged_count;
+  uint32_t stage_bytes;
+  uint32_t tmem_cols;
+};
+
+__global__ void __launch_bounds__(192, 1) router_tc_kernel(const __grid_constant__ CUtensorMap tmX,
+                                                           const __grid_constant__ CUtensorMap tmW, const TcArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[kTcStages];
+  __shared__ __align__(8) uint64_t empty_bar[kTcStages];
+  __shared__ __align__(8) uint64_t accf_bar;
+  __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int* abort = &abort_flag;
+  const int t0 = blockIdx.x * kTcTokens;
+  const int kblocks = a.d / kTcBK;
+  const uint32_t wtile = static_cast<uint32_t>(a.E_pad) * kTcBK * 2;  // one split's tile
+  constexpr uint32_t kXTile = kTcTokens * kTcBK * 2;                  // 16 KB
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kTcStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    mbar_init(&accf_bar, 1);
+    mbar_init(&drain_bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmX);
+    tma_prefetch_desc(&tmW);
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_slot, a.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = tmem_slot;
+  long long fills = 0;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, 1ll << 40, kTcWaitNs, abort)) {
+          if (!*abort) {
+            latch_status(a.status, MOE_DEV_TIMEOUT);
+            *abort = 1;
+          }
+          break;
+        }
+        uint8_t* st = smem + static_cast<size_t>(stage) * a.stage_bytes;
+        mbar_arrive_expect_tx(&full_bar[stage], kXTile + 3 * wtile);
+        tma_load_2d(st, &tmX, kb * kTcBK, t0, &full_bar[stage]);
+        for (int sp = 0; sp < 3; ++sp)
+          tma_load_2d(st + kXTile + sp * wtile, &tmW, kb * kTcBK, sp * a.E_pad, &full_bar[stage]);
+        ++fills;
+        if (++stage == kTcStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      const uint32_t idesc = idesc_bf16_f32(kTcTokens, a.E_pad);
+      bool ok = true;
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!mbar_wait_bounded(&full_bar[stage], phase, 1ll << 40, kTcWaitNs, abort)) {
+          if (!*abort) {
+            latch_status(a.status, MOE_DEV_TIMEOUT);
+            *abort = 1;
+          }
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sx = smem_u32(smem + static_cast<size_t>(stage) * a.stage_bytes);
+        // hi products accumulate in D1 (columns [0, E_pad)), the small mid and lo
+        // products in D2 (columns [E_pad, 2 E_pad)), so they do not lose bits
+        // against the large running sum
+#pragma unroll
+        for (int k = 0; k < kTcBK / 16; ++k) {
+          const uint64_t adesc = sdesc_kmajor_sw128(sx + k * 32);
+          const uint32_t first = (kb | k) != 0 ? 1u : 0u;
+          mma_bf16_ss(tmem_base, adesc, sdesc_kmajor_sw128(sx + kXTile + k * 32), idesc, first);
+          mma_bf16_ss(tmem_base + a.E_pad, adesc, sdesc_kmajor_sw128(sx + kXTile + wtile + k * 32), idesc, first);
+          mma_bf16_ss(tmem_base + a.E_pad, adesc, sdesc_kmajor_sw128(sx + kXTile + 2 * wtile + k * 32), idesc, 1u);
+        }
+        mma_commit(&empty_bar[stage]);
+        if (++stage == kTcStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (ok) mma_commit(&accf_bar);
+    }
+    __syncwarp();
+  } else {
+    // epilogue: thread r owns token t0 + r (TMEM lane r)
+    const int q = warp & 3, r = q * 32 + lane;
+    const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&accf_bar, 0, 1ll << 40, kTcWaitNs, abort));
+    if (ok) {
+      tc_fence_after();
+      const int stride = a.E_pad + 33;  // scores, then group scores; odd stride: no bank conflicts
+      float* srow = reinterpret_cast<float*>(smem) + static_cast<size_t>(r) * stride;
+      float* gsr = srow + a.E_pad;
+      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+      float lmax = 0.f;
+      for (int c = 0; c < a.E_pad; c += 16) {
+        uint32_t v[16], v2[16];
+        tmem_ld_32x32b_x16(tb + c, v);
+        tmem_ld_32x32b_x16(tb + a.E_pad + c, v2);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float l = __uint_as_float(v[j]) + __uint_as_float(v2[j]);
+          if (c + j < a.E) lmax = fmaxf(lmax, fabsf(l));
+          srow[c + j] = 1.0f / (1.0f + expf(-l));
+        }
+      }
+      const int t = t0 + r;
+      if (t < a.T) {
+        const int gsz = a.E / a.G;
+        for (int g = 0; g < a.G; ++g) {
+          float m1 = -1.f, m2 = -1.f;
+          for (int e = g * gsz; e < (g + 1) * gsz; ++e) {
+            const float v = srow[e];
+            if (v > m1) {
+              m2 = m1;
+              m1 = v;
+            } else if (v > m2) {
+              m2 = v;
+            }
+          }
+          gsr[g] = (gsz >= 2) ? (m1 + m2) : m1;
+        }
+        uint32_t kept = 0;
+        int last_kept = 0;
+        for (int rr = 0; rr < a.Gk; ++rr) {
+          int best = -1;
+          for (int g = 0; g < a.G; ++g)
+            if (!((kept >> g) & 1u) && (best < 0 || gsr[g] > gsr[best])) best = g;
+          kept |= 1u << best;
+          last_kept = best;
+        }
+        float dropped = -4.f;
+        for (int g = 0; g < a.G; ++g)
+          if (!((kept >> g) & 1u)) dropped = fmaxf(dropped, gsr[g]);
+        const float margin_group = gsr[last_kept] - dropped;
+        int32_t* oi = a.topk_idx + static_cast<size_t>(t) * a.K;
+        float last_s = 0.f;
+        for (int k = 0; k < a.K; ++k) {
+          int best = -1;
+          float bv = -1.5f;  // taken experts are marked -2
+          for (int g = 0; g < a.G; ++g) {
+            if (!((kept >> g) & 1u)) continue;
+            for (int e = g * gsz; e < (g + 1) * gsz; ++e)
+              if (srow[e] > bv) {
+                bv = srow[e];
+                best = e;
+              }
+          }
+          if (best < 0) {  // only possible with NaN scores
+            latch_status(a.status, MOE_DEV_BAD_EXPERT);
+            best = 0;
+            bv = 0.f;
+          } else {
+            srow[best] = -2.f;
+          }
+          oi[k] = best;
+          last_s = bv;
+        }
+        float rest = -1.5f;
+        for (int g = 0; g < a.G; ++g) {
+          if (!((kept >> g) & 1u)) continue;
+          for (int e = g * gsz; e < (g + 1) * gsz; ++e) rest = fmaxf(rest, srow[e]);
+        }
+        const float margin_expert = (rest > -1.f) ? last_s - rest : 1.f;
+        // Flag when a margin could be within the tensor-core error of zero.
+        // Measured on Beam-shape inputs (|logit| <= 6): score errors <= 5e-6,
+        // so margin errors <= 2e-5; the threshold keeps a factor >= 4.
+        const float thr = 4e-5f + 1e-5f * lmax;
+        const bool narrow = margin_group < thr || margin_expert < thr;
+        a.flags[t] = narrow ? 1 : 0;
+        if (narrow) a.flagged[atomicAdd(a.flagged_count, 1)] = t;
+      }
+    } else if (lane == 0 && !*abort) {
+      latch_status(a.status, MOE_DEV_TIMEOUT);
+      *abort = 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (*abort) {
+    if (threadIdx.x == 0) {
+      for (int s = 0; s < kTcStages; ++s) {
+        if (fills > s) {
+          const long long f = s + static_cast<long long>(kTcStages) * ((fills - 1 - s) / kTcStages);
+          mbar_wait_bounded(&full_bar[s], static_cast<uint32_t>((f / kTcStages) & 1), 1ll << 40, kTcDrainNs, nullptr);
+        }
+      }
+    }
+    if (warp == 1 && lane == 0) {
+      mma_commit(&drain_bar);
+      mbar_wait_bounded(&drain_bar, 0, 1ll << 40, kTcDrainNs, nullptr);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  }
+  if (warp == 1) tmem_dealloc(tmem_base, a.tmem_cols);
+}
+
+// One warp per token (not flagged): FFMA dot products x[t] . W_r[:, e] for the
+// token's K chosen experts (wt = W_r transposed, rows contiguous), sigmoid,
+// slots sorted by (score desc, id asc), weights = scale * s / sum(s).
+__global__ void __launch_bounds__(256) router_refine_kernel(const uint16_t* __restrict__ x,
+                                                            const float* __restrict__ wt, int T, int d, int K,
+                                                            float scale, const int32_t* __restrict__ flags,
+                                                            int32_t* __restrict__ topk_idx,
+                                                            float* __restrict__ topk_w, int32_t* status) {
+  __shared__ float s_sorted[8][32];
+  __shared__ int e_sorted[8][32];
+  const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
+  const int t = blockIdx.x * 8 + wl;
+  if (t >= T || flags[t]) return;
+  const int my_e = (lane < K) ? topk_idx[static_cast<size_t>(t) * K + lane] : 0;
+  const uint2* xr = reinterpret_cast<const uint2*>(x + static_cast<size_t>(t) * d);  // 4 bf16 per uint2
+  float my_l = 0.f;
+  for (int k = 0; k < K; ++k) {
+    const int e = __shfl_sync(0xffffffffu, my_e, k);
+    const float4* wr = reinterpret_cast<const float4*>(wt + static_cast<size_t>(e) * d);
+    float acc = 0.f;
+    for (int c = lane; c < d / 4; c += 32) {
+      const uint2 xv = xr[c];
+      const float4 w4 = wr[c];
+      acc = fmaf(__uint_as_float(xv.x << 16), w4.x, acc);
+      acc = fmaf(__uint_as_float(xv.x & 0xFFFF0000u), w4.y, acc);
+      acc = fmaf(__uint_as_float(xv.y << 16), w4.z, acc);
+      acc = fmaf(__uint_as_float(xv.y & 0xFFFF0000u), w4.w, acc);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == k) my_l = acc;
+  }
+  const float my_s = (lane < K) ? 1.0f / (1.0f + expf(-my_l)) : -1.f;
+  int rank = 0;
+  for (int j = 0; j < K; ++j) {
+    const float sj = __shfl_sync(0xffffffffu, my_s, j);
+    const int ej = __shfl_sync(0xffffffffu, my_e, j);
+    if (lane < K && j != lane && better(sj, ej, my_s, my_e)) ++rank;
+  }
+  if (lane < K) {
+    s_sorted[wl][rank] = my_s;
+    e_sorted[wl][rank] = my_e;
+  }
+  __syncwarp();
+  float sum = 0.f;
+  for (int j = 0; j < K; ++j) sum += s_sorted[wl][j];
+  if (lane < K) {
+    const float sv = s_sorted[wl][lane];
+    topk_idx[static_cast<size_t>(t) * K + lane] = e_sorted[wl][lane];
+    topk_w[static_cast<size_t>(t) * K + lane] = (sum > 0.f) ? scale * sv / sum : 0.f;
+  }
+  if (lane == 0 && !(sum > 0.f)) latch_status(status, MOE_DEV_ZERO_SUM);
+}
+
+// Flagged tokens, kFlagTokens per CTA (looping over the flagged list): every
+// logit as an fp32 FFMA dot product, 1024 threads = 4 hidden-dimension
+// quarters x 256 experts, each quarter summed in index order and the four
+// quarters added in a fixed order; then one warp per token runs the full
+// selection.
+constexpr int kFlagTokens = 8;
+constexpr int kFlagThreads = 1024;
+
+__global__ void __launch_bounds__(kFlagThreads) router_flagged_kernel(
+    const uint16_t* __restrict__ x, const float* __restrict__ wr, int d, int E, int G, int Gk, int K, float scale,
+    int tokens_per_cta, const int32_t* __restrict__ flagged, const int32_t* __restrict__ flagged_count,
+    int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int32_t* status) {
+  extern __shared__ float xs[];                  // [tokens_per_cta][d]
+  __shared__ float part[4][kFlagTokens][256];    // per-quarter partial logits, then scores in [0]
+  const int n = *flagged_count;
+  const int e = threadIdx.x & 255, qd = threadIdx.x >> 8;
+  const int kq = d / 4;
+  for (int i0 = blockIdx.x * tokens_per_cta; i0 < n; i0 += gridDim.x * tokens_per_cta) {
+    const int nt = min(tokens_per_cta, n - i0);
+    for (int j = 0; j < nt; ++j) {
+      const int t = flagged[i0 + j];
+      for (int k = threadIdx.x; k < d; k += blockDim.x)
+        xs[j * d + k] = bf16_bits_to_float(x[static_cast<size_t>(t) * d + k]);
+    }
+    __syncthreads();
+    if (e < E) {
+      float acc[kFlagTokens];
+#pragma unroll
+      for (int j = 0; j < kFlagTokens; ++j) acc[j] = 0.f;
+      for (int k = qd * kq; k < (qd + 1) * kq; ++k) {
+        const float w = wr[static_cast<size_t>(k) * E + e];
+#pragma unroll
+        for (int j = 0; j < kFlagTokens; ++j)
+          if (j < nt) acc[j] = fmaf(xs[j * d + k], w, acc[j]);
+      }
+#pragma unroll
+      for (int j = 0; j < kFlagTokens; ++j) part[qd][j][e] = acc[j];
+    }
+    __syncthreads();
+    if (qd == 0 && e < E) {
+      for (int j = 0; j < nt; ++j) {
+        const float l = ((part[0][j][e] + part[1][j][e]) + part[2][j][e]) + part[3][j][e];
+        part[0][j][e] = 1.0f / (1.0f + expf(-l));
+      }
+    }
+    __syncthreads();
+    const int wj = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (wj < nt) {
+      float s[kMaxPerLane];
+#pragma unroll
+      for (int j = 0; j < kMaxPerLane; ++j) {
+        const int ee = lane + 32 * j;
+        s[j] = (ee < E) ? part[0][wj][ee] : -1.0f;
+      }
+      warp_select(s, lane, flagged[i0 + wj], E, G, Gk, K, scale, topk_idx, topk_w, status);
+    }
+    __syncthreads();
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 router_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  return fn;
+}
+
+int encode_router_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+  auto fn = router_encode_fn();
+  if (!fn) return -1;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kTcBK), box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : static_cast<int>(r);
+}
+
 }  // namespace
+
+int router_epad(int E) { return ((E + 15) / 16) * 16; }
+
+bool router_uses_tensor_cores(int T, int E) { return T >= kRouterTcMinTokens && router_epad(E) <= 256; }
+
+size_t router_tc_scratch_bytes(int T, int d, int E) {
+  const size_t a = sizeof(uint16_t) * 3 * router_epad(E) * static_cast<size_t>(d);
+  const size_t b = sizeof(float) * static_cast<size_t>(E) * d;
+  return ((a + 255) & ~size_t(255)) + ((b + 255) & ~size_t(255)) + 2 * ((sizeof(int32_t) * T + 255) & ~size_t(255));
+}
+
+cudaError_t launch_router_tc(const uint16_t* x, const float* w_r, void* scratch, int32_t* flagged_count, int T,
+                             int d, int E, int n_groups, int topk_groups, int top_k, float routed_scale,
+                             int32_t* topk_idx, float* topk_w, int32_t* status, int num_sms, cudaStream_t stream) {
+  const int E_pad = router_epad(E);
+  uint8_t* p = static_cast<uint8_t*>(scratch);
+  auto take = [&p](size_t bytes) {
+    uint8_t* q = p;
+    p += (bytes + 255) & ~size_t(255);
+    return q;
+  };
+  uint16_t* w_split = reinterpret_cast<uint16_t*>(take(sizeof(uint16_t) * 3 * E_pad * static_cast<size_t>(d)));
+  float* wt = reinterpret_cast<float*>(take(sizeof(float) * static_cast<size_t>(E) * d));
+  int32_t* flags = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * T));
+  int32_t* flagged = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * T));
+  wr_split_kernel<<<dim3(d / 32, (E_pad + 31) / 32), 256, 0, stream>>>(w_r, d, E, E_pad, w_split, wt,
+                                                                         flagged_count);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  CUtensorMap tmX, tmW;
+  if (encode_router_map(&tmX, x, d, T, kTcTokens) || encode_router_map(&tmW, w_split, d, 3ull * E_pad, E_pad))
+    return cudaErrorInvalidValue;
+  TcArgs a;
+  a.T = T;
+  a.d = d;
+  a.E = E;
+  a.E_pad = E_pad;
+  a.G = n_groups;
+  a.Gk = topk_groups;
+  a.K = top_k;
+  a.scale = routed_scale;
+  a.topk_idx = topk_idx;
+  a.topk_w = topk_w;
+  a.status = status;
+  a.flags = flags;
+  a.flagged = flagged;
+  a.flagged_count = flagged_count;
+  a.stage_bytes = ((kTcTokens * kTcBK * 2 + 3 * E_pad * kTcBK * 2) + 1023u) & ~1023u;
+  a.tmem_cols = 32;
+  while (a.tmem_cols < static_cast<uint32_t>(2 * E_pad)) a.tmem_cols <<= 1;
+  const size_t smem = 1024 + static_cast<size_t>(kTcStages) * a.stage_bytes;
+  err = cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  router_tc_kernel<<<(T + kTcTokens - 1) / kTcTokens, 192, smem, stream>>>(tmX, tmW, a);
+  router_refine_kernel<<<(T + 7) / 8, 256, 0, stream>>>(x, wt, T, d, top_k, routed_scale, flags, topk_idx, topk_w,
+                                                        status);
+  const int per_cta = std::max(1, std::min(kFlagTokens, static_cast<int>((160 * 1024) / (sizeof(float) * d))));
+  const size_t xs_bytes = sizeof(float) * static_cast<size_t>(d) * per_cta;
+  err = cudaFuncSetAttribute(router_flagged_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(xs_bytes));
+  if (err != cudaSuccess) return err;
+  router_flagged_kernel<<<num_sms, kFlagThreads, xs_bytes, stream>>>(x, w_r, d, E, n_groups, topk_groups, top_k,
+                                                                     routed_scale, per_cta, flagged, flagged_count,
+                                                                     topk_idx, topk_w, status);
+  return cudaGetLastError();
+}
 
 // Smallest split of the hidden dimension (into >= 64-element slices) that
 // gives at least one block per SM.

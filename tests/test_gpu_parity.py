@@ -14,7 +14,8 @@ import torch
 import oracle as O
 import workload as W
 import sparse_moe_layer_14_b300 as bm
-from support import (TOL_BF16, DeviceWeights, bf16_to_f64, check_output, compare_routing, dev, host_bits)
+from support import (TOL_BF16, TOL_NVFP4, DeviceWeights, bf16_to_f64, check_output, compare_routing, dev,
+                     host_bits)
 
 pytestmark = pytest.mark.gpu
 
@@ -47,7 +48,9 @@ def route_only(cfg, x_h, wr_h):
 # ---------------------------------------------------------------------------------------- router
 
 @pytest.mark.parametrize("name,T,seed", [("tiny", 64, 0), ("tiny", 77, 1), ("tiny", 1, 2), ("decode", 64, 0),
-                                         ("decode", 1000, 3), ("prefill", 4096, 0)])
+                                         ("decode", 1000, 3), ("prefill", 4096, 0),
+                                         # batches of >= 1024 tokens take the tensor-core router
+                                         ("tiny", 1500, 8), ("decode", 1100, 9), ("skewed", 2048, 10)])
 def test_route_parity(name, T, seed):
     cfg = W.CONFIGS[name].with_tokens(T)
     x_h, wr_h = W.gen_x(cfg, seed), W.gen_wr(cfg, seed)
@@ -119,12 +122,12 @@ def test_permute_bad_expert_latched():
 
 # ---------------------------------------------------------------------------------------- experts
 
-def _ffn_case(d, inter, E, T, K, counts_list, seed):
+def _ffn_case(d, inter, E, T, K, counts_list, seed, wfmt="bf16"):
     R = T * K
     counts_h = np.array(counts_list, np.int64)
     assert counts_h.size == E and counts_h.sum() <= R
     offsets_h = np.concatenate([[0], np.cumsum(counts_h)]).astype(np.int32)
-    cfg = W.MoEConfig("ffn", T=T, d=d, E=E, n_groups=1, topk_groups=1, top_k=K, inter=inter)
+    cfg = W.MoEConfig("ffn", T=T, d=d, E=E, n_groups=1, topk_groups=1, top_k=K, inter=inter, wfmt=wfmt)
     dw = DeviceWeights(cfg, seed)
     x_perm_h = W.normal_bf16(seed, W.TID_X, 0, R * d, 1.0).reshape(R, d)
     dims = bm.Dims.from_config(cfg)
@@ -135,12 +138,12 @@ def _ffn_case(d, inter, E, T, K, counts_list, seed):
     assert bm.moe_get_device_status(ws) == bm.MOE_DEV_OK
     n = int(offsets_h[-1])
     row_expert = np.repeat(np.arange(E, dtype=np.int32), counts_h)
-    ref = O.ffn_rows(row_expert, x_perm_h[:n], dw.host, d, inter)
+    ref = O.ffn_rows(row_expert, x_perm_h[:n], dw.host, d, inter, wfmt)
     got = y[:n].cpu().numpy().astype(np.float64)
     rms = np.sqrt(np.mean(ref ** 2))
     err = np.abs(got - ref)
     assert np.all(np.isfinite(got))
-    assert err.max() <= TOL_BF16 * rms, (err.max(), rms)
+    assert err.max() <= (TOL_BF16 if wfmt == "bf16" else TOL_NVFP4) * rms, (err.max(), rms)
     # the only rounding between the oracle and the kernel is fp32 accumulation order and
     # occasional 1-ulp flips of the bf16 h, so the typical error is far below the bar
     assert np.sqrt(np.mean(err ** 2)) <= 2e-3 * rms
@@ -161,6 +164,29 @@ def test_expert_ffn_intermediate_below_tile():
 def test_expert_ffn_beam_shape_few_rows():
     """d=5120, inter=2560: the full 80-step K loop, 20 + 40 weight tiles per expert."""
     _ffn_case(d=5120, inter=2560, E=4, T=16, K=2, counts_list=[3, 1, 0, 12], seed=23)
+
+
+def test_expert_ffn_nvfp4_tiles_and_ragged_tails():
+    """NVFP4 weights decoded on chip: same tile/ragged coverage as the bf16 case."""
+    _ffn_case(d=256, inter=256, E=8, T=710, K=2, counts_list=[0, 1, 17, 256, 257, 255, 600, 33], seed=24,
+              wfmt="nvfp4")
+
+
+def test_expert_ffn_nvfp4_beam_shape_few_rows():
+    _ffn_case(d=5120, inter=2560, E=4, T=16, K=2, counts_list=[3, 1, 0, 12], seed=25, wfmt="nvfp4")
+
+
+def test_nvfp4_needs_multiples_of_256():
+    cfg = W.MoEConfig("q", T=16, d=128, E=4, n_groups=1, topk_groups=1, top_k=2, inter=64, wfmt="nvfp4")
+    dw = DeviceWeights(cfg, 1, keep_host=False)
+    dims = bm.Dims.from_config(cfg)
+    ws = bm.allocate_workspace(dims)
+    x = torch.zeros((16, 128), dtype=torch.bfloat16, device="cuda")
+    wr = torch.zeros((128, 4), dtype=torch.float32, device="cuda")
+    out = torch.empty((16, 128), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(bm.MoEError, match="UNSUPPORTED"):
+        bm.moe_forward(dims, x, wr, dw.dev, out, ws)
+    torch.cuda.synchronize()
 
 
 # ---------------------------------------------------------------------------------------- combine
@@ -208,6 +234,22 @@ def compare_routing_idx_only(cfg, gi, orc):
     return compare_routing(cfg, gi, w_like, orc)
 
 
+SMALL_NVFP4 = W.MoEConfig("small_nvfp4", T=64, d=256, E=16, n_groups=4, topk_groups=2, top_k=4, inter=256,
+                          wfmt="nvfp4")
+
+
+@pytest.mark.parametrize("T,seed", [(64, 0), (100, 4)])
+def test_forward_nvfp4_full_parity(T, seed):
+    cfg = SMALL_NVFP4.with_tokens(T)
+    x_h, wr_h = W.gen_x(cfg, seed), W.gen_wr(cfg, seed)
+    dw = DeviceWeights(cfg, seed)
+    out, idx, counts, _ = run_forward(cfg, dev(x_h), dev(wr_h), dw.dev)
+    orc = O.route(cfg, x_h, wr_h)
+    excluded, ref_idx, ref_w = compare_routing_idx_only(cfg, idx.cpu().numpy(), orc)
+    ref = O.forward_tokens(cfg, x_h, ref_idx, ref_w, np.arange(T), dw.host)
+    check_output(host_bits(out), ref, TOL_NVFP4)
+
+
 def test_forward_deterministic():
     cfg = TINY.with_tokens(200)
     inp = W.make_host_inputs(cfg, 9)
@@ -249,6 +291,21 @@ def _sample_tokens(T, gi, n=48, seed=0):
     hot_tokens = np.nonzero((gi == hot).any(1))[0]
     picks |= set(hot_tokens[:4].tolist()) | set(hot_tokens[-4:].tolist())
     return np.array(sorted(picks), np.int32)
+
+
+@pytest.mark.slow
+def test_forward_full_size_nvfp4():
+    """The NVFP4 prefill workload (T=4096, Beam shape, weights quantised from the same seeded bf16)."""
+    cfg = W.CONFIGS["nvfp4"]
+    dw = DeviceWeights(cfg, 0)
+    x_h, wr_h = W.gen_x(cfg, 0), W.gen_wr(cfg, 0)
+    out, idx, counts, _ = run_forward(cfg, dev(x_h), dev(wr_h), dw.dev)
+    gi = idx.cpu().numpy()
+    orc = O.route(cfg, x_h, wr_h)
+    excluded, ref_idx, ref_w = compare_routing_idx_only(cfg, gi, orc)
+    toks = _sample_tokens(cfg.T, gi)
+    ref = O.forward_tokens(cfg, x_h, ref_idx, ref_w, toks, dw.host)
+    check_output(host_bits(out)[toks], ref, TOL_NVFP4)
 
 
 @pytest.mark.slow
