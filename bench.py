@@ -57,11 +57,11 @@ ROUTER_TC_MIN_TOKENS = 1024  # the library routes batches this large on the tens
 
 
 def kernels_per_step(cfg, num_sms):
-    """Kernels one moe_forward launches: router (tensor-core: W_r split, tensor-core selection,
-    fp32 refinement, narrow-margin recompute; SIMT: logits [+ split reduce] + select),
-    permute (4), schedule, GEMM1, GEMM2, combine."""
+    """Kernels one moe_forward launches: router (tensor-core: W_r split, tensor-core logits,
+    selection, fp32 refinement, narrow-margin recompute; SIMT: logits [+ split reduce] +
+    select), permute (4), schedule, GEMM1, GEMM2, combine."""
     if cfg.T >= ROUTER_TC_MIN_TOKENS:
-        router = 4
+        router = 5
     else:
         router = 2 + (1 if router_splits(cfg.T, cfg.d, cfg.E, num_sms) > 1 else 0)
     return router + 4 + 1 + 2 + 1
@@ -81,10 +81,13 @@ PROFILE_CASES = {
     "profile_decode": W.MoEConfig("profile_decode", T=8, d=5120, E=32, n_groups=8, topk_groups=4, top_k=8, inter=2560),
     "profile_prefill": W.MoEConfig("profile_prefill", T=512, d=5120, E=32, n_groups=8, topk_groups=4, top_k=8,
                                    inter=2560),
+    # ~1024 tokens per expert, like the skewed workload's compute-bound tiles
+    "profile_dense": W.MoEConfig("profile_dense", T=2048, d=5120, E=16, n_groups=4, topk_groups=4, top_k=8,
+                                 inter=2560),
 }
 
 DEFAULT_STEPS = {"decode": 300, "prefill": 200, "skewed": 40, "nvfp4": 200, "profile_decode": 20,
-                 "profile_prefill": 20}
+                 "profile_prefill": 20, "profile_dense": 20}
 
 
 def workload_cfg(name):

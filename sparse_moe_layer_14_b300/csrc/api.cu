@@ -2,6 +2,7 @@
 // validation, the workspace layout, and the launch sequence of each step.
 // No call allocates memory or synchronises the host except
 // moe_get_device_status().
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 
@@ -41,13 +42,14 @@ constexpr int kMaxSmsForLayout = 1024;
 Layout make_layout(const moe_dims_t& d) {
   const int64_t T = d.T, R = T * d.top_k;
   const int Tc = d.T > 0 ? d.T : 1;
-  const int splits = router_splits(Tc, d.d, d.E, kMaxSmsForLayout);
+  const int splits = std::max(router_splits(Tc, d.d, d.E, kMaxSmsForLayout),
+                              router_uses_tensor_cores(d.T, d.E, d.d) ? router_tc_splits(Tc, d.d, kMaxSmsForLayout) : 1);
   const ExpertPlan pl = plan_experts(d.T, d.d, d.E, d.top_k, d.inter);
   const int64_t nw = bitmap_words(d.T);
   size_t sz[R_NUM];
   sz[R_HDR] = sizeof(WsHeader);
   sz[R_PART] = sizeof(float) * static_cast<size_t>(splits) * T * d.E;
-  sz[R_WSPLIT] = router_uses_tensor_cores(d.T, d.E) ? router_tc_scratch_bytes(d.T, d.d, d.E) : 0;
+  sz[R_WSPLIT] = router_uses_tensor_cores(d.T, d.E, d.d) ? router_tc_scratch_bytes(d.T, d.d, d.E) : 0;
   sz[R_BITMAP] = sizeof(uint32_t) * static_cast<size_t>(d.E) * nw;
   sz[R_WPRE] = sizeof(int32_t) * static_cast<size_t>(d.E) * nw;
   sz[R_COUNTS] = sizeof(int32_t) * d.E;
@@ -125,8 +127,8 @@ int32_t* status_word(void* ws) { return ws ? &reinterpret_cast<WsHeader*>(ws)->s
 
 moe_status_t do_route(const moe_dims_t* d, const uint16_t* x, const float* w_r, int32_t* idx, float* w,
                       void* ws, const Layout& L, cudaStream_t s) {
-  if (router_uses_tensor_cores(d->T, d->E))
-    return cuda_status(launch_router_tc(x, w_r, region<uint8_t>(ws, L, R_WSPLIT),
+  if (router_uses_tensor_cores(d->T, d->E, d->d))
+    return cuda_status(launch_router_tc(x, w_r, region<uint8_t>(ws, L, R_WSPLIT), region<float>(ws, L, R_PART),
                                         &reinterpret_cast<WsHeader*>(ws)->router_flagged, d->T, d->d, d->E, d->n_groups,
                                         d->topk_groups, d->top_k, d->routed_scale, idx, w, status_word(ws),
                                         num_sms(), s));

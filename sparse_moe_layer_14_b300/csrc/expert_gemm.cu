@@ -7,6 +7,11 @@
 //   GEMM1 + SwiGLU:  h[r][i] = bf16( silu(x_perm[r].Wg_e[i]) * (x_perm[r].Wu_e[i]) )
 //   GEMM2:           y[r][n] = h[r] . Wd_e[n]                                   (fp32)
 //
+// Every work item runs two 128-row weight tiles against the same token tile
+// (two MMAs per K step sharing the token operand): the gate and up tiles of
+// the same 128 intermediate rows in GEMM1, two consecutive 128-row tiles of
+// W_down (256 output columns) in GEMM2.
+//
 // Design (weight-stationary, "swap AB"): the MMA's M operand is a 128-row
 // tile of one expert's weights (K-major, straight from the checkpoint
 // layout) and its N operand is the expert's tokens (rows of x_perm / h),
@@ -169,7 +174,7 @@ __global__ void __launch_bounds__(threads_for(kW4), 1)
     abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA0);
-    if (kGLU) tma_prefetch_desc(&tmA1);
+    tma_prefetch_desc(&tmA1);
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmB64);
     tma_prefetch_desc(&tmB128);
@@ -185,7 +190,9 @@ __global__ void __launch_bounds__(threads_for(kW4), 1)
   const uint32_t tmem_base = tmem_slot;
   const int n_items = *p.n_items;
   const int kblocks = p.K / BK;
-  constexpr int nA = kGLU ? 2 : 1;
+  constexpr int nA = 2;                       // weight tiles per item
+  constexpr int kItemRows = kGLU ? BM : 2 * BM;  // weight rows an item covers
+  constexpr int kRow1 = kGLU ? 0 : BM;          // row offset of tile 1 (up tile / second down tile)
   long long fills = 0;  // TMA stage fills issued (thread 0 only)
 
   if (warp == 0) {
@@ -196,7 +203,7 @@ __global__ void __launch_bounds__(threads_for(kW4), 1)
       bool ok = true;
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
         const int4 item = p.items[it];
-        const int a_row = item.x * p.Nw + item.y * BM;
+        const int a_row = item.x * p.Nw + item.y * kItemRows;
         const int nbox = (item.w + TOK_BOX - 1) / TOK_BOX;
         const uint32_t bytes = (kW4 ? kPTileBytes : kATileBytes) * nA + static_cast<uint32_t>(nbox) * kTokBoxBytes;
         for (int kb = 0; kb < kblocks; ++kb) {
@@ -210,10 +217,10 @@ __global__ void __launch_bounds__(threads_for(kW4), 1)
           if (kW4) {
             // packed codes: 32 bytes (64 elements) per row
             tma_load_2d(st + p.p_offset, &tmA0, kb * (BK / 2), a_row, &full_bar[stage]);
-            if (kGLU) tma_load_2d(st + p.p_offset + kPTileBytes, &tmA1, kb * (BK / 2), a_row, &full_bar[stage]);
+            tma_load_2d(st + p.p_offset + kPTileBytes, &tmA1, kb * (BK / 2), a_row + kRow1, &full_bar[stage]);
           } else {
             tma_load_2d(st, &tmA0, kb * BK, a_row, &full_bar[stage]);
-            if (kGLU) tma_load_2d(st + kATileBytes, &tmA1, kb * BK, a_row, &full_bar[stage]);
+            tma_load_2d(st + kATileBytes, &tmA1, kb * BK, a_row + kRow1, &full_bar[stage]);
           }
           // token rows in boxes of 128, 64 and 16 rows (fewest copies); the
           // stacked boxes form one 128-byte-swizzled K-major tile
@@ -269,7 +276,7 @@ __global__ void __launch_bounds__(threads_for(kW4), 1)
             const uint64_t bdesc = sdesc_kmajor_sw128(sb + k * 32);
             const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
             mma_bf16_ss(d0, sdesc_kmajor_sw128(sa + k * 32), bdesc, idesc, accum);
-            if (kGLU) mma_bf16_ss(d1, sdesc_kmajor_sw128(sa + kATileBytes + k * 32), bdesc, idesc, accum);
+            mma_bf16_ss(d1, sdesc_kmajor_sw128(sa + kATileBytes + k * 32), bdesc, idesc, accum);
           }
           mma_commit(&empty_bar[stage]);
           if (++stage == p.stages) {
@@ -302,30 +309,39 @@ __global__ void __launch_bounds__(threads_for(kW4), 1)
       }
       tc_fence_after();
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * p.acc_cols);
-      const int col = item.y * BM + r;
-      const bool valid = col < p.Nw;
+      const int col0 = item.y * kItemRows + r;       // output column of accumulator 0
+      const int col1 = col0 + kRow1;                 // ... of accumulator 1 (GEMM2)
+      const bool valid0 = col0 < p.Nw, valid1 = col1 < p.Nw;
       const int ntok = item.w;
       const float s0 = p.ts0 ? p.ts0[item.x] : 1.0f;
-      const float s1 = (kGLU && p.ts1) ? p.ts1[item.x] : 1.0f;
+      const float s1 = p.ts1 ? p.ts1[item.x] : s0;
       for (int c = 0; c < ntok; c += 16) {
         uint32_t g[16], u[16];
         tmem_ld_32x32b_x16(tb + c, g);
-        if (kGLU) tmem_ld_32x32b_x16(tb + p.n_max + c, u);
+        tmem_ld_32x32b_x16(tb + p.n_max + c, u);
         tmem_ld_wait();
-        if (valid) {
+        if (kGLU) {
+          if (valid0) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int tok = c + j;
+              if (tok < ntok) {
+                const float gv = __uint_as_float(g[j]) * s0;
+                const float uv = __uint_as_float(u[j]) * s1;
+                const float silu = gv / (1.0f + expf(-gv));
+                p.h_out[static_cast<size_t>(item.z + tok) * p.Nw + col0] =
+                    __bfloat16_as_ushort(__float2bfloat16_rn(silu * uv));
+              }
+            }
+          }
+        } else {
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int tok = c + j;
             if (tok < ntok) {
-              const size_t off = static_cast<size_t>(item.z + tok) * p.Nw + col;
-              if (kGLU) {
-                const float gv = __uint_as_float(g[j]) * s0;
-                const float uv = __uint_as_float(u[j]) * s1;
-                const float silu = gv / (1.0f + expf(-gv));
-                p.h_out[off] = __bfloat16_as_ushort(__float2bfloat16_rn(silu * uv));
-              } else {
-                p.y_out[off] = __uint_as_float(g[j]) * s0;
-              }
+              float* yrow = p.y_out + static_cast<size_t>(item.z + tok) * p.Nw;
+              if (valid0) yrow[col0] = __uint_as_float(g[j]) * s0;
+              if (valid1) yrow[col1] = __uint_as_float(u[j]) * s0;
             }
           }
         }
@@ -352,10 +368,11 @@ __global__ void __launch_bounds__(threads_for(kW4), 1)
       s1 = make_uint4(0, 0, 0, 0);
       if (it >= n_items) return;
       const int4 item = p.items[it];
-      const int64_t row = static_cast<int64_t>(item.x) * p.Nw + item.y * BM + r;
-      if (row >= rows_total) return;  // padding rows past the last expert decode to zero
-      s0 = __ldg(reinterpret_cast<const uint4*>(p.sf0 + row * sf_ld + g * 16));
-      if (kGLU) s1 = __ldg(reinterpret_cast<const uint4*>(p.sf1 + row * sf_ld + g * 16));
+      const int64_t row = static_cast<int64_t>(item.x) * p.Nw + item.y * kItemRows + r;
+      const int64_t row1 = row + kRow1;
+      // padding rows past the last expert decode to zero
+      if (row < rows_total) s0 = __ldg(reinterpret_cast<const uint4*>(p.sf0 + row * sf_ld + g * 16));
+      if (row1 < rows_total) s1 = __ldg(reinterpret_cast<const uint4*>(p.sf1 + row1 * sf_ld + g * 16));
     };
     uint4 cur0, cur1, nxt0, nxt1;
     load_group(blockIdx.x, 0, nxt0, nxt1);
@@ -376,9 +393,8 @@ __global__ void __launch_bounds__(threads_for(kW4), 1)
         uint8_t* st = smem + static_cast<size_t>(stage) * p.stage_bytes;
         const int q = kb & 3;
         decode_row(st + p.p_offset, st, r, q == 0 ? cur0.x : q == 1 ? cur0.y : q == 2 ? cur0.z : cur0.w);
-        if (kGLU)
-          decode_row(st + p.p_offset + kPTileBytes, st + kATileBytes, r,
-                     q == 0 ? cur1.x : q == 1 ? cur1.y : q == 2 ? cur1.z : cur1.w);
+        decode_row(st + p.p_offset + kPTileBytes, st + kATileBytes, r,
+                   q == 0 ? cur1.x : q == 1 ? cur1.y : q == 2 ? cur1.z : cur1.w);
         fence_async_shared();  // generic-proxy writes -> visible to tcgen05.mma
         mbar_arrive(&conv_bar[stage]);
         if (++stage == p.stages) {
@@ -521,14 +537,15 @@ struct StageShape {
 
 StageShape stage_shape(bool glu, bool w4, int n_max) {
   StageShape s;
-  const uint32_t nA = glu ? 2u : 1u;
+  (void)glu;
+  const uint32_t nA = 2u;
   s.b_offset = kATileBytes * nA;
   s.p_offset = s.b_offset + static_cast<uint32_t>(n_max) * BK * 2;
   s.stage_bytes = s.p_offset + (w4 ? kPTileBytes * nA : 0u);
   s.stage_bytes = (s.stage_bytes + 1023u) & ~1023u;
   const int budget = kSmemLimit - 1024 - 512;  // alignment slack + static barriers
   s.stages = std::min(kMaxStages, budget / static_cast<int>(s.stage_bytes));
-  s.acc_cols = glu ? 2 * n_max : n_max;
+  s.acc_cols = 2 * n_max;
   s.acc_bufs = std::min(kMaxAcc, static_cast<int>(kTmemCols) / s.acc_cols);
   s.smem = 1024 + static_cast<size_t>(s.stages) * s.stage_bytes;
   return s;
@@ -568,7 +585,7 @@ ExpertPlan plan_experts(int T, int d, int E, int top_k, int inter) {
   p.n_max = static_cast<int>(std::min<int64_t>(n, tok));
   p.max_tiles = static_cast<int>(E + (R + p.n_max - 1) / p.n_max);
   p.wtiles1 = (inter + BM - 1) / BM;
-  p.wtiles2 = (d + BM - 1) / BM;
+  p.wtiles2 = (d + 2 * BM - 1) / (2 * BM);
   p.max_items1 = static_cast<int64_t>(p.max_tiles) * p.wtiles1;
   p.max_items2 = static_cast<int64_t>(p.max_tiles) * p.wtiles2;
   return p;
@@ -640,6 +657,7 @@ cudaError_t launch_expert_ffn(const ExpertPlan& plan, const ExpertBuffers& buf, 
   if (w4) {
     a2.ts0 = w.down_ts;
     a2.sf0 = w.down_sf;
+    a2.sf1 = w.down_sf;
     return launch_gemm<false, true>(td, td, th, a2, plan.n_max, num_sms, stream);
   }
   return launch_gemm<false, false>(td, td, th, a2, plan.n_max, num_sms, stream);

@@ -26,10 +26,11 @@ cudaError_t launch_router_select(float* partial, int splits, int T, int E, int n
 // `scratch` holds router_tc_scratch_bytes(T, d, E) bytes.
 constexpr int kRouterTcMinTokens = 1024;
 int router_epad(int E);
-bool router_uses_tensor_cores(int T, int E);
+bool router_uses_tensor_cores(int T, int E, int d);
 size_t router_tc_scratch_bytes(int T, int d, int E);
-cudaError_t launch_router_tc(const uint16_t* x, const float* w_r, void* scratch, int32_t* flagged_count, int T,
-                             int d, int E, int n_groups, int topk_groups, int top_k, float routed_scale,
+int router_tc_splits(int T, int d, int num_sms);  // partial-logit buffers: [splits][T][E] fp32 in `part`
+cudaError_t launch_router_tc(const uint16_t* x, const float* w_r, void* scratch, float* part, int32_t* flagged_count,
+                             int T, int d, int E, int n_groups, int topk_groups, int top_k, float routed_scale,
                              int32_t* topk_idx, float* topk_w, int32_t* status, int num_sms, cudaStream_t stream);
 
 // ---- permutation (permute.cu) ----
@@ -44,7 +45,7 @@ struct ExpertPlan {
   int n_max;        // max tokens per work item (multiple of 16, <= 256)
   int max_tiles;    // upper bound of (expert, token tile) pairs
   int wtiles1;      // 128-row weight tiles per expert in GEMM1 (ceil(inter/128))
-  int wtiles2;      // ... in GEMM2 (ceil(d/128))
+  int wtiles2;      // 256-row weight tiles per expert in GEMM2 (ceil(d/256))
   int64_t max_items1, max_items2;
 };
 ExpertPlan plan_experts(int T, int d, int E, int top_k, int inter);

@@ -15,11 +15,12 @@
 //  wr_split_kernel       W_r (fp32, [d][E]) -> three bf16 matrices hi, mid,
 //                        lo ([E_pad][d], K-contiguous) with hi + mid + lo = W_r
 //                        (8 + 8 + 8 significant bits cover fp32's 24).
-//  router_tc_kernel      per 128 tokens: logits = x.hi + x.mid + x.lo on the
-//                        tcgen05 tensor cores (x is exact in bf16, so every
-//                        product is exact in fp32), then in the epilogue each
-//                        thread takes one token: sigmoid, group scores, kept
-//                        groups, chosen experts, and the two decision margins.
+//  router_tc_kernel      per 128 tokens and one range of the hidden dimension:
+//                        partial logits x.hi + x.mid + x.lo on the tcgen05
+//                        tensor cores (x is exact in bf16, so every product is
+//                        exact in fp32).
+//  router_select_flag_kernel  one warp per token: partials summed, sigmoid,
+//                        group-limited selection and the two decision margins.
 //                        The tensor cores' fp32 accumulation is measurably
 //                        coarser than FFMA (logit errors up to ~4e-5 with the
 //                        small mid/lo products in their own accumulator, ~5e-6
@@ -143,9 +144,11 @@ constexpr int kMaxPerLane = 8;  // E <= 256
 
 // Group-limited selection of one token by one warp. Lane l holds the scores
 // of experts l, l+32, l+64, ... in s[]; writes the token's K expert ids (slot
-// order: descending score, ties to the lower id) and weights.
-__device__ void warp_select(const float (&s)[kMaxPerLane], int lane, int t, int E, int G, int Gk, int K, float scale,
-                            int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int32_t* status) {
+// order: descending score, ties to the lower id) and weights. Returns, in
+// every lane, the smaller of the two decision margins: (worst kept group
+// score - best dropped one) and (worst chosen score - best unchosen candidate).
+__device__ float warp_select(const float (&s)[kMaxPerLane], int lane, int t, int E, int G, int Gk, int K, float scale,
+                             int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int32_t* status) {
   const int gsz = E / G;
   constexpr float kMasked = -1.0f;  // below every sigmoid score
 
@@ -181,11 +184,20 @@ __device__ void warp_select(const float (&s)[kMaxPerLane], int lane, int t, int 
 
   // keep the Gk best groups (ties to the lower group index)
   uint32_t kept = 0;
+  float last_kept = 0.f;
   for (int r = 0; r < Gk; ++r) {
     float v = (lane < G && !((kept >> lane) & 1u)) ? my_gs : -2.0f;
     int i = lane;
     warp_argmax(v, i);
     kept |= 1u << i;
+    last_kept = v;
+  }
+  float margin = 1.0f;
+  {
+    float v = (lane < G && !((kept >> lane) & 1u)) ? my_gs : -2.0f;
+    int i = lane;
+    warp_argmax(v, i);
+    if (v > -1.5f) margin = last_kept - v;
   }
 
   // choose the K best experts of the kept groups (ties to the lower index)
@@ -218,6 +230,21 @@ __device__ void warp_select(const float (&s)[kMaxPerLane], int lane, int t, int 
       my_e = idx;
     }
   }
+  {
+    float v = -2.0f;
+    int idx = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < kMaxPerLane; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && ((kept >> (e / gsz)) & 1u) && !((taken >> i) & 1u) && better(s[i], e, v, idx)) {
+        v = s[i];
+        idx = e;
+      }
+    }
+    warp_argmax(v, idx);
+    const float last_s = __shfl_sync(0xffffffffu, my_s, K - 1);
+    if (v > -1.5f) margin = fminf(margin, last_s - v);
+  }
   if (lane < K) {
     float w = 0.f;
     if (sum > 0.f) {
@@ -228,6 +255,7 @@ __device__ void warp_select(const float (&s)[kMaxPerLane], int lane, int t, int 
     topk_idx[static_cast<size_t>(t) * K + lane] = my_e;
     topk_w[static_cast<size_t>(t) * K + lane] = w;
   }
+  return margin;
 }
 
 __global__ void __launch_bounds__(256) router_select_kernel(const float* __restrict__ logits, int T,
@@ -251,6 +279,7 @@ __global__ void __launch_bounds__(256) router_select_kernel(const float* __restr
 constexpr int kTcTokens = 128;  // tokens per CTA (MMA M)
 constexpr int kTcBK = 64;       // hidden elements per pipeline stage
 constexpr int kTcStages = 2;
+constexpr int kTcMaxSplits = 16;
 constexpr uint64_t kTcWaitNs = 2000000000ull;
 constexpr uint64_t kTcDrainNs = 1000000000ull;
 
@@ -286,18 +315,17 @@ __global__ void __launch_bounds__(256) wr_split_kernel(const float* __restrict__
 }
 
 struct TcArgs {
-  int T, d, E, E_pad, G, Gk, K;
-  float scale;
-  int32_t* topk_idx;
-  float* topk_w;
+  int T, d, E, E_pad;
+  int kb_per_split;  // K slices of one CTA (the hidden dimension is split over blockIdx.y)
+  float* part;       // [splits][T][E] partial logits
   int32_t* status;
-  int32_t* flags;          // [T]: 1 = narrow tensor-core margin, recomputed in full
-  int32_t* flagged;        // [T]: list of flagged tokens
-  int32_t* flagged_count;
   uint32_t stage_bytes;
   uint32_t tmem_cols;
 };
 
+// Partial logits of 128 tokens x E_pad experts over one range of the hidden
+// dimension: hi products accumulate in D1 (TMEM columns [0, E_pad)), the small
+// mid and lo products in D2 ([E_pad, 2 E_pad)), so they keep their bits.
 __global__ void __launch_bounds__(192, 1) router_tc_kernel(const __grid_constant__ CUtensorMap tmX,
                                                            const __grid_constant__ CUtensorMap tmW, const TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -311,7 +339,7 @@ __global__ void __launch_bounds__(192, 1) router_tc_kernel(const __grid_constant
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort = &abort_flag;
   const int t0 = blockIdx.x * kTcTokens;
-  const int kblocks = a.d / kTcBK;
+  const int kb0 = blockIdx.y * a.kb_per_split, kb1 = kb0 + a.kb_per_split;
   const uint32_t wtile = static_cast<uint32_t>(a.E_pad) * kTcBK * 2;  // one split's tile
   constexpr uint32_t kXTile = kTcTokens * kTcBK * 2;                  // 16 KB
 
@@ -341,7 +369,7 @@ __global__ void __launch_bounds__(192, 1) router_tc_kernel(const __grid_constant
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      for (int kb = 0; kb < kblocks; ++kb) {
+      for (int kb = kb0; kb < kb1; ++kb) {
         if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, 1ll << 40, kTcWaitNs, abort)) {
           if (!*abort) {
             latch_status(a.status, MOE_DEV_TIMEOUT);
@@ -367,7 +395,7 @@ __global__ void __launch_bounds__(192, 1) router_tc_kernel(const __grid_constant
       uint32_t phase = 0;
       const uint32_t idesc = idesc_bf16_f32(kTcTokens, a.E_pad);
       bool ok = true;
-      for (int kb = 0; kb < kblocks; ++kb) {
+      for (int kb = kb0; kb < kb1; ++kb) {
         if (!mbar_wait_bounded(&full_bar[stage], phase, 1ll << 40, kTcWaitNs, abort)) {
           if (!*abort) {
             latch_status(a.status, MOE_DEV_TIMEOUT);
@@ -378,13 +406,10 @@ __global__ void __launch_bounds__(192, 1) router_tc_kernel(const __grid_constant
         }
         tc_fence_after();
         const uint32_t sx = smem_u32(smem + static_cast<size_t>(stage) * a.stage_bytes);
-        // hi products accumulate in D1 (columns [0, E_pad)), the small mid and lo
-        // products in D2 (columns [E_pad, 2 E_pad)), so they do not lose bits
-        // against the large running sum
 #pragma unroll
         for (int k = 0; k < kTcBK / 16; ++k) {
           const uint64_t adesc = sdesc_kmajor_sw128(sx + k * 32);
-          const uint32_t first = (kb | k) != 0 ? 1u : 0u;
+          const uint32_t first = ((kb - kb0) | k) != 0 ? 1u : 0u;
           mma_bf16_ss(tmem_base, adesc, sdesc_kmajor_sw128(sx + kXTile + k * 32), idesc, first);
           mma_bf16_ss(tmem_base + a.E_pad, adesc, sdesc_kmajor_sw128(sx + kXTile + wtile + k * 32), idesc, first);
           mma_bf16_ss(tmem_base + a.E_pad, adesc, sdesc_kmajor_sw128(sx + kXTile + 2 * wtile + k * 32), idesc, 1u);
@@ -399,93 +424,24 @@ __global__ void __launch_bounds__(192, 1) router_tc_kernel(const __grid_constant
     }
     __syncwarp();
   } else {
-    // epilogue: thread r owns token t0 + r (TMEM lane r)
+    // epilogue: thread r owns token t0 + r (TMEM lane r); partial logits to global
     const int q = warp & 3, r = q * 32 + lane;
     const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&accf_bar, 0, 1ll << 40, kTcWaitNs, abort));
     if (ok) {
       tc_fence_after();
-      const int stride = a.E_pad + 33;  // scores, then group scores; odd stride: no bank conflicts
-      float* srow = reinterpret_cast<float*>(smem) + static_cast<size_t>(r) * stride;
-      float* gsr = srow + a.E_pad;
+      const int t = t0 + r;
+      float* dst = a.part + (static_cast<size_t>(blockIdx.y) * a.T + t) * a.E;
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-      float lmax = 0.f;
       for (int c = 0; c < a.E_pad; c += 16) {
         uint32_t v[16], v2[16];
         tmem_ld_32x32b_x16(tb + c, v);
         tmem_ld_32x32b_x16(tb + a.E_pad + c, v2);
         tmem_ld_wait();
+        if (t < a.T) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float l = __uint_as_float(v[j]) + __uint_as_float(v2[j]);
-          if (c + j < a.E) lmax = fmaxf(lmax, fabsf(l));
-          srow[c + j] = 1.0f / (1.0f + expf(-l));
+          for (int j = 0; j < 16; ++j)
+            if (c + j < a.E) dst[c + j] = __uint_as_float(v[j]) + __uint_as_float(v2[j]);
         }
-      }
-      const int t = t0 + r;
-      if (t < a.T) {
-        const int gsz = a.E / a.G;
-        for (int g = 0; g < a.G; ++g) {
-          float m1 = -1.f, m2 = -1.f;
-          for (int e = g * gsz; e < (g + 1) * gsz; ++e) {
-            const float v = srow[e];
-            if (v > m1) {
-              m2 = m1;
-              m1 = v;
-            } else if (v > m2) {
-              m2 = v;
-            }
-          }
-          gsr[g] = (gsz >= 2) ? (m1 + m2) : m1;
-        }
-        uint32_t kept = 0;
-        int last_kept = 0;
-        for (int rr = 0; rr < a.Gk; ++rr) {
-          int best = -1;
-          for (int g = 0; g < a.G; ++g)
-            if (!((kept >> g) & 1u) && (best < 0 || gsr[g] > gsr[best])) best = g;
-          kept |= 1u << best;
-          last_kept = best;
-        }
-        float dropped = -4.f;
-        for (int g = 0; g < a.G; ++g)
-          if (!((kept >> g) & 1u)) dropped = fmaxf(dropped, gsr[g]);
-        const float margin_group = gsr[last_kept] - dropped;
-        int32_t* oi = a.topk_idx + static_cast<size_t>(t) * a.K;
-        float last_s = 0.f;
-        for (int k = 0; k < a.K; ++k) {
-          int best = -1;
-          float bv = -1.5f;  // taken experts are marked -2
-          for (int g = 0; g < a.G; ++g) {
-            if (!((kept >> g) & 1u)) continue;
-            for (int e = g * gsz; e < (g + 1) * gsz; ++e)
-              if (srow[e] > bv) {
-                bv = srow[e];
-                best = e;
-              }
-          }
-          if (best < 0) {  // only possible with NaN scores
-            latch_status(a.status, MOE_DEV_BAD_EXPERT);
-            best = 0;
-            bv = 0.f;
-          } else {
-            srow[best] = -2.f;
-          }
-          oi[k] = best;
-          last_s = bv;
-        }
-        float rest = -1.5f;
-        for (int g = 0; g < a.G; ++g) {
-          if (!((kept >> g) & 1u)) continue;
-          for (int e = g * gsz; e < (g + 1) * gsz; ++e) rest = fmaxf(rest, srow[e]);
-        }
-        const float margin_expert = (rest > -1.f) ? last_s - rest : 1.f;
-        // Flag when a margin could be within the tensor-core error of zero.
-        // Measured on Beam-shape inputs (|logit| <= 6): score errors <= 5e-6,
-        // so margin errors <= 2e-5; the threshold keeps a factor >= 4.
-        const float thr = 4e-5f + 1e-5f * lmax;
-        const bool narrow = margin_group < thr || margin_expert < thr;
-        a.flags[t] = narrow ? 1 : 0;
-        if (narrow) a.flagged[atomicAdd(a.flagged_count, 1)] = t;
       }
     } else if (lane == 0 && !*abort) {
       latch_status(a.status, MOE_DEV_TIMEOUT);
@@ -514,6 +470,55 @@ __global__ void __launch_bounds__(192, 1) router_tc_kernel(const __grid_constant
     tc_fence_after();
   }
   if (warp == 1) tmem_dealloc(tmem_base, a.tmem_cols);
+}
+
+// One warp per token: the tensor-core logits (partials summed in a fixed
+// order), sigmoid and the group-limited selection. Where the smaller decision
+// margin could be within the tensor-core error of zero, the token is flagged
+// for an fp32 recompute of all its logits.
+__global__ void __launch_bounds__(256) router_select_flag_kernel(const float* __restrict__ part, int splits, int T,
+                                                                 int E, int G, int Gk, int K, float scale,
+                                                                 int32_t* __restrict__ topk_idx,
+                                                                 float* __restrict__ topk_w,
+                                                                 int32_t* __restrict__ flags,
+                                                                 int32_t* __restrict__ flagged,
+                                                                 int32_t* __restrict__ flagged_count,
+                                                                 int32_t* status) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= T) return;
+  float s[kMaxPerLane];
+  float lmax = 0.f;
+  float l[kMaxPerLane];
+#pragma unroll
+  for (int i = 0; i < kMaxPerLane; ++i) l[i] = 0.f;
+  for (int sp = 0; sp < splits; ++sp) {  // eight independent loads per split, summed in split order
+    const float* row = part + (static_cast<size_t>(sp) * T + t) * E;
+    float v[kMaxPerLane];
+#pragma unroll
+    for (int i = 0; i < kMaxPerLane; ++i) v[i] = (lane + 32 * i < E) ? row[lane + 32 * i] : 0.f;
+#pragma unroll
+    for (int i = 0; i < kMaxPerLane; ++i) l[i] += v[i];
+  }
+#pragma unroll
+  for (int i = 0; i < kMaxPerLane; ++i) {
+    const int e = lane + 32 * i;
+    s[i] = -1.0f;
+    if (e < E) {
+      lmax = fmaxf(lmax, fabsf(l[i]));
+      s[i] = 1.0f / (1.0f + expf(-l[i]));
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, off));
+  const float margin = warp_select(s, lane, t, E, G, Gk, K, scale, topk_idx, topk_w, status);
+  // Measured on Beam-shape inputs (|logit| <= 6): tensor-core score errors
+  // <= 5e-6, so margin errors <= 2e-5; the threshold keeps a factor >= 4.
+  const bool narrow = margin < 4e-5f + 1e-5f * lmax;
+  if (lane == 0) {
+    flags[t] = narrow ? 1 : 0;
+    if (narrow) flagged[atomicAdd(flagged_count, 1)] = t;
+  }
 }
 
 // One warp per token (not flagged): FFMA dot products x[t] . W_r[:, e] for the
@@ -570,29 +575,33 @@ __global__ void __launch_bounds__(256) router_refine_kernel(const uint16_t* __re
   if (lane == 0 && !(sum > 0.f)) latch_status(status, MOE_DEV_ZERO_SUM);
 }
 
-// Flagged tokens, kFlagTokens per CTA (looping over the flagged list): every
-// logit as an fp32 FFMA dot product, 1024 threads = 4 hidden-dimension
-// quarters x 256 experts, each quarter summed in index order and the four
-// quarters added in a fixed order; then one warp per token runs the full
-// selection.
+// Flagged tokens (looping over the flagged list): every logit as an fp32
+// FFMA dot product, 1024 threads = 4 hidden-dimension quarters x 256 experts,
+// each quarter summed in index order and the four quarters added in a fixed
+// order; then one warp per token runs the full selection. Tokens per CTA
+// (1..kFlagTokens) follow the flagged count so the work spreads over the SMs;
+// the staged activations are k-major (a token group's values at one k are
+// contiguous), so each hidden index costs one weight load and two 16-byte
+// shared loads.
 constexpr int kFlagTokens = 8;
 constexpr int kFlagThreads = 1024;
 
 __global__ void __launch_bounds__(kFlagThreads) router_flagged_kernel(
     const uint16_t* __restrict__ x, const float* __restrict__ wr, int d, int E, int G, int Gk, int K, float scale,
-    int tokens_per_cta, const int32_t* __restrict__ flagged, const int32_t* __restrict__ flagged_count,
-    int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int32_t* status) {
-  extern __shared__ float xs[];                  // [tokens_per_cta][d]
+    const int32_t* __restrict__ flagged, const int32_t* __restrict__ flagged_count, int32_t* __restrict__ topk_idx,
+    float* __restrict__ topk_w, int32_t* status) {
+  extern __shared__ float4 xs4[];                // [d][kFlagTokens / 4]: x of the group's tokens, k-major
   __shared__ float part[4][kFlagTokens][256];    // per-quarter partial logits, then scores in [0]
+  float* xs = reinterpret_cast<float*>(xs4);
   const int n = *flagged_count;
+  const int per = max(1, min(kFlagTokens, (n + gridDim.x - 1) / gridDim.x));
   const int e = threadIdx.x & 255, qd = threadIdx.x >> 8;
   const int kq = d / 4;
-  for (int i0 = blockIdx.x * tokens_per_cta; i0 < n; i0 += gridDim.x * tokens_per_cta) {
-    const int nt = min(tokens_per_cta, n - i0);
-    for (int j = 0; j < nt; ++j) {
-      const int t = flagged[i0 + j];
-      for (int k = threadIdx.x; k < d; k += blockDim.x)
-        xs[j * d + k] = bf16_bits_to_float(x[static_cast<size_t>(t) * d + k]);
+  for (int i0 = blockIdx.x * per; i0 < n; i0 += gridDim.x * per) {
+    const int nt = min(per, n - i0);
+    for (int idx = threadIdx.x; idx < d * kFlagTokens; idx += blockDim.x) {
+      const int k = idx / kFlagTokens, j = idx % kFlagTokens;
+      xs[idx] = (j < nt) ? bf16_bits_to_float(x[static_cast<size_t>(flagged[i0 + j]) * d + k]) : 0.f;
     }
     __syncthreads();
     if (e < E) {
@@ -601,9 +610,15 @@ __global__ void __launch_bounds__(kFlagThreads) router_flagged_kernel(
       for (int j = 0; j < kFlagTokens; ++j) acc[j] = 0.f;
       for (int k = qd * kq; k < (qd + 1) * kq; ++k) {
         const float w = wr[static_cast<size_t>(k) * E + e];
-#pragma unroll
-        for (int j = 0; j < kFlagTokens; ++j)
-          if (j < nt) acc[j] = fmaf(xs[j * d + k], w, acc[j]);
+        const float4 a0 = xs4[k * 2], a1 = xs4[k * 2 + 1];
+        acc[0] = fmaf(a0.x, w, acc[0]);
+        acc[1] = fmaf(a0.y, w, acc[1]);
+        acc[2] = fmaf(a0.z, w, acc[2]);
+        acc[3] = fmaf(a0.w, w, acc[3]);
+        acc[4] = fmaf(a1.x, w, acc[4]);
+        acc[5] = fmaf(a1.y, w, acc[5]);
+        acc[6] = fmaf(a1.z, w, acc[6]);
+        acc[7] = fmaf(a1.w, w, acc[7]);
       }
 #pragma unroll
       for (int j = 0; j < kFlagTokens; ++j) part[qd][j][e] = acc[j];
@@ -660,7 +675,24 @@ int encode_router_map(CUtensorMap* map, const void* base, uint64_t inner, uint64
 
 int router_epad(int E) { return ((E + 15) / 16) * 16; }
 
-bool router_uses_tensor_cores(int T, int E) { return T >= kRouterTcMinTokens && router_epad(E) <= 256; }
+// The fp32 recompute stages 8 tokens' activations (32 d bytes) in shared memory.
+bool router_uses_tensor_cores(int T, int E, int d) {
+  return T >= kRouterTcMinTokens && router_epad(E) <= 256 && d <= 5120;
+}
+
+// Split of the hidden dimension over CTAs so that the token tiles cover the SMs.
+int router_tc_splits(int T, int d, int num_sms) {
+  const int tiles = (T + kTcTokens - 1) / kTcTokens;
+  const int kblocks = d / kTcBK;
+  const int target = (num_sms + tiles - 1) / tiles;
+  int best = 1;
+  for (int s = 1; s <= kTcMaxSplits && s <= kblocks; ++s) {
+    if (kblocks % s) continue;
+    best = s;
+    if (s >= target) break;
+  }
+  return best;
+}
 
 size_t router_tc_scratch_bytes(int T, int d, int E) {
   const size_t a = sizeof(uint16_t) * 3 * router_epad(E) * static_cast<size_t>(d);
@@ -668,8 +700,8 @@ size_t router_tc_scratch_bytes(int T, int d, int E) {
   return ((a + 255) & ~size_t(255)) + ((b + 255) & ~size_t(255)) + 2 * ((sizeof(int32_t) * T + 255) & ~size_t(255));
 }
 
-cudaError_t launch_router_tc(const uint16_t* x, const float* w_r, void* scratch, int32_t* flagged_count, int T,
-                             int d, int E, int n_groups, int topk_groups, int top_k, float routed_scale,
+cudaError_t launch_router_tc(const uint16_t* x, const float* w_r, void* scratch, float* part, int32_t* flagged_count,
+                             int T, int d, int E, int n_groups, int topk_groups, int top_k, float routed_scale,
                              int32_t* topk_idx, float* topk_w, int32_t* status, int num_sms, cudaStream_t stream) {
   const int E_pad = router_epad(E);
   uint8_t* p = static_cast<uint8_t*>(scratch);
@@ -689,38 +721,34 @@ cudaError_t launch_router_tc(const uint16_t* x, const float* w_r, void* scratch,
   CUtensorMap tmX, tmW;
   if (encode_router_map(&tmX, x, d, T, kTcTokens) || encode_router_map(&tmW, w_split, d, 3ull * E_pad, E_pad))
     return cudaErrorInvalidValue;
+  const int splits = router_tc_splits(T, d, num_sms);
   TcArgs a;
   a.T = T;
   a.d = d;
   a.E = E;
   a.E_pad = E_pad;
-  a.G = n_groups;
-  a.Gk = topk_groups;
-  a.K = top_k;
-  a.scale = routed_scale;
-  a.topk_idx = topk_idx;
-  a.topk_w = topk_w;
+  a.kb_per_split = d / kTcBK / splits;
+  a.part = part;
   a.status = status;
-  a.flags = flags;
-  a.flagged = flagged;
-  a.flagged_count = flagged_count;
   a.stage_bytes = ((kTcTokens * kTcBK * 2 + 3 * E_pad * kTcBK * 2) + 1023u) & ~1023u;
   a.tmem_cols = 32;
   while (a.tmem_cols < static_cast<uint32_t>(2 * E_pad)) a.tmem_cols <<= 1;
   const size_t smem = 1024 + static_cast<size_t>(kTcStages) * a.stage_bytes;
   err = cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  router_tc_kernel<<<(T + kTcTokens - 1) / kTcTokens, 192, smem, stream>>>(tmX, tmW, a);
+  router_tc_kernel<<<dim3((T + kTcTokens - 1) / kTcTokens, splits), 192, smem, stream>>>(tmX, tmW, a);
+  router_select_flag_kernel<<<(T + 7) / 8, 256, 0, stream>>>(part, splits, T, E, n_groups, topk_groups, top_k,
+                                                             routed_scale, topk_idx, topk_w, flags, flagged,
+                                                             flagged_count, status);
   router_refine_kernel<<<(T + 7) / 8, 256, 0, stream>>>(x, wt, T, d, top_k, routed_scale, flags, topk_idx, topk_w,
                                                         status);
-  const int per_cta = std::max(1, std::min(kFlagTokens, static_cast<int>((160 * 1024) / (sizeof(float) * d))));
-  const size_t xs_bytes = sizeof(float) * static_cast<size_t>(d) * per_cta;
+  const size_t xs_bytes = sizeof(float) * static_cast<size_t>(d) * kFlagTokens;  // d <= 5120 for this path
   err = cudaFuncSetAttribute(router_flagged_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(xs_bytes));
   if (err != cudaSuccess) return err;
   router_flagged_kernel<<<num_sms, kFlagThreads, xs_bytes, stream>>>(x, w_r, d, E, n_groups, topk_groups, top_k,
-                                                                     routed_scale, per_cta, flagged, flagged_count,
-                                                                     topk_idx, topk_w, status);
+                                                                     routed_scale, flagged, flagged_count, topk_idx,
+                                                                     topk_w, status);
   return cudaGetLastError();
 }
 

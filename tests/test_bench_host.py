@@ -84,5 +84,5 @@ def test_router_split_rule():
     assert bench.router_splits(64, 5120, 256, 148) == 80
     assert bench.router_splits(4096, 5120, 256, 148) == 2
     assert bench.router_splits(32768, 5120, 256, 148) == 1
-    assert bench.kernels_per_step(W.CONFIGS["skewed"], 148) == 12   # tensor-core router: 4 kernels
+    assert bench.kernels_per_step(W.CONFIGS["skewed"], 148) == 13   # tensor-core router: 5 kernels
     assert bench.kernels_per_step(W.CONFIGS["decode"], 148) == 11   # SIMT logits + reduce + select
