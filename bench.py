@@ -58,7 +58,7 @@ ROUTER_TC_MIN_TOKENS = 1024  # the library routes batches this large on the tens
 
 def kernels_per_step(cfg, num_sms):
     """Kernels one moe_forward launches: router (tensor-core: W_r split, tensor-core logits,
-    selection, fp32 refinement, narrow-margin recompute; SIMT: logits [+ split reduce] +
+    selection, narrow-margin recompute (logits + selection); SIMT: logits [+ split reduce] +
     select), permute (4), schedule, GEMM1, GEMM2, combine."""
     if cfg.T >= ROUTER_TC_MIN_TOKENS:
         router = 5

@@ -43,7 +43,9 @@ Layout make_layout(const moe_dims_t& d) {
   const int64_t T = d.T, R = T * d.top_k;
   const int Tc = d.T > 0 ? d.T : 1;
   const int splits = std::max(router_splits(Tc, d.d, d.E, kMaxSmsForLayout),
-                              router_uses_tensor_cores(d.T, d.E, d.d) ? router_tc_splits(Tc, d.d, kMaxSmsForLayout) : 1);
+                              router_uses_tensor_cores(d.T, d.E, d.d)
+                                  ? std::max(4, router_tc_splits(Tc, d.d, kMaxSmsForLayout))  // 4: fp32 recompute
+                                  : 1);
   const ExpertPlan pl = plan_experts(d.T, d.d, d.E, d.top_k, d.inter);
   const int64_t nw = bitmap_words(d.T);
   size_t sz[R_NUM];

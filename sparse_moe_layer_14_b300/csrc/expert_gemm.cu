@@ -23,8 +23,9 @@
 // One persistent CTA per SM:
 //   warp 0      TMA producer: weight tile(s) + token rows per 64-wide K slice
 //   warp 1      TMEM allocator and single-thread tcgen05.mma issuer
-//   warps 2..5  epilogue: tcgen05.ld, SwiGLU in FP32 (GEMM1) or fp32 store
-//   warps 6..9  (NVFP4 weights only) converters: e2m1 codes times their e4m3
+//   warps 2..9  epilogue, two warpgroups splitting the token columns:
+//               tcgen05.ld, SwiGLU in FP32 (GEMM1) or fp32 store (GEMM2)
+//   warps 10..13 (NVFP4 weights only) converters: e2m1 codes times their e4m3
 //               block scale, which is exact in bf16, written in the 128-byte
 //               swizzled operand layout the MMA reads; the fp32 tensor scale
 //               is applied to the accumulator in the epilogue.
@@ -54,7 +55,9 @@ constexpr uint64_t kDrainNs = 1000000000ull;             // 1 s bound for draini
 constexpr uint64_t kWaitNs = 2000000000ull;              // 2 s bound of a pipeline wait
 constexpr int kSmemLimit = 232448;                       // 227 KB opt-in per block
 
-constexpr int threads_for(bool w4) { return w4 ? 320 : 192; }
+constexpr int kEpiThreads = 256;  // two epilogue warpgroups
+constexpr int kConvBase = 320;    // first converter thread (NVFP4)
+constexpr int threads_for(bool w4) { return w4 ? 448 : 320; }
 
 struct GemmArgs {
   const int4* items;
@@ -168,7 +171,7 @@ __global__ void __launch_bounds__(threads_for(kW4), 1)
     }
     for (int a = 0; a < p.acc_bufs; ++a) {
       mbar_init(&accf_bar[a], 1);
-      mbar_init(&acce_bar[a], 128);
+      mbar_init(&acce_bar[a], kEpiThreads);
     }
     mbar_init(&drain_bar, 1);
     abort_flag = 0;
@@ -293,10 +296,11 @@ __global__ void __launch_bounds__(threads_for(kW4), 1)
       }
     }
     __syncwarp();
-  } else if (warp < 6) {
+  } else if (warp < 10) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int r = q * 32 + lane;
+    const int eg = (warp - 2) >> 2;  // epilogue warpgroup: 16-token chunks eg, eg + 2, ...
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
@@ -315,7 +319,7 @@ __global__ void __launch_bounds__(threads_for(kW4), 1)
       const int ntok = item.w;
       const float s0 = p.ts0 ? p.ts0[item.x] : 1.0f;
       const float s1 = p.ts1 ? p.ts1[item.x] : s0;
-      for (int c = 0; c < ntok; c += 16) {
+      for (int c = eg * 16; c < ntok; c += 32) {
         uint32_t g[16], u[16];
         tmem_ld_32x32b_x16(tb + c, g);
         tmem_ld_32x32b_x16(tb + p.n_max + c, u);
@@ -328,7 +332,9 @@ __global__ void __launch_bounds__(threads_for(kW4), 1)
               if (tok < ntok) {
                 const float gv = __uint_as_float(g[j]) * s0;
                 const float uv = __uint_as_float(u[j]) * s1;
-                const float silu = gv / (1.0f + expf(-gv));
+                // silu(g) = g / (1 + e^-g); h is rounded to bf16 right after, so the
+                // fast exponential and division (relative error ~1e-7) do not show
+                const float silu = __fdividef(gv, 1.0f + __expf(-gv));
                 p.h_out[static_cast<size_t>(item.z + tok) * p.Nw + col0] =
                     __bfloat16_as_ushort(__float2bfloat16_rn(silu * uv));
               }
@@ -358,7 +364,7 @@ __global__ void __launch_bounds__(threads_for(kW4), 1)
     // Thread r decodes weight row r of every K slice. Block scales (4 per
     // slice per row) are read 16 bytes (four slices) at a time from global
     // memory, one group ahead, so the load latency hides behind decoding.
-    const int r = threadIdx.x - 192;
+    const int r = threadIdx.x - kConvBase;
     const int sf_ld = p.K / 16;        // bytes of block scales per weight row
     const int64_t rows_total = static_cast<int64_t>(p.E) * p.Nw;
     int stage = 0;

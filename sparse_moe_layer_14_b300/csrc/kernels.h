@@ -20,9 +20,9 @@ cudaError_t launch_router_select(float* partial, int splits, int T, int E, int n
                                  int32_t* status, cudaStream_t stream);
 
 // Tensor-core router for large batches (T >= kRouterTcMinTokens): W_r split
-// into three bf16 terms, logits and a provisional selection per 128 tokens on
-// the tensor cores, then an fp32 FFMA refinement (chosen experts' logits for
-// every token; all logits for tokens with a narrow tensor-core margin).
+// into three bf16 terms, partial logits on the tensor cores, a warp-per-token
+// selection that flags tokens with a narrow decision margin, and an fp32
+// FFMA recompute of all logits of the flagged tokens.
 // `scratch` holds router_tc_scratch_bytes(T, d, E) bytes.
 constexpr int kRouterTcMinTokens = 1024;
 int router_epad(int E);

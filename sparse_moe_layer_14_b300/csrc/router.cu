@@ -24,14 +24,11 @@
 //                        The tensor cores' fp32 accumulation is measurably
 //                        coarser than FFMA (logit errors up to ~4e-5 with the
 //                        small mid/lo products in their own accumulator, ~5e-6
-//                        for FFMA, on Beam-shape inputs), so this pass only
-//                        picks the expert set, and only where both margins
-//                        are wide:
-//  router_refine_kernel  one warp per token: the chosen experts' logits again,
-//                        as FFMA dot products in fp32; their scores give the
-//                        slot order and the weights.
-//  router_flagged_kernel tokens whose tensor-core margin was narrow: all
-//                        logits in fp32 FFMA and the full warp selection.
+//                        for FFMA, on Beam-shape inputs), so its decisions are
+//                        kept only where every margin is wide:
+//  router_flagged_logits_kernel, router_flagged_select_kernel: tokens with a
+//                        narrow margin get all logits in fp32 FFMA and the
+//                        full warp selection.
 #include <algorithm>
 
 #include "common.cuh"
@@ -145,12 +142,20 @@ constexpr int kMaxPerLane = 8;  // E <= 256
 // Group-limited selection of one token by one warp. Lane l holds the scores
 // of experts l, l+32, l+64, ... in s[]; writes the token's K expert ids (slot
 // order: descending score, ties to the lower id) and weights. Returns, in
-// every lane, the smaller of the two decision margins: (worst kept group
-// score - best dropped one) and (worst chosen score - best unchosen candidate).
-__device__ float warp_select(const float (&s)[kMaxPerLane], int lane, int t, int E, int G, int Gk, int K, float scale,
-                             int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int32_t* status) {
+// every lane, the decision margins: x = worst kept group score - best dropped
+// one; y = the smaller of (worst chosen score - best unchosen candidate) and
+// the gaps between consecutive slots.
+__device__ float2 warp_select(const float (&s)[kMaxPerLane], int lane, int t, int E, int G, int Gk, int K,
+                              float scale, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+                              int32_t* status) {
   const int gsz = E / G;
   constexpr float kMasked = -1.0f;  // below every sigmoid score
+  int grp[kMaxPerLane];             // group of each of this lane's experts (E = none)
+#pragma unroll
+  for (int i = 0; i < kMaxPerLane; ++i) {
+    const int e = lane + 32 * i;
+    grp[i] = (e < E) ? e / gsz : 64;
+  }
 
   // group score: sum of the two largest scores of the group (lane g keeps group g's)
   float my_gs = kMasked;
@@ -158,8 +163,7 @@ __device__ float warp_select(const float (&s)[kMaxPerLane], int lane, int t, int
     float m1 = kMasked, m2 = kMasked;
 #pragma unroll
     for (int i = 0; i < kMaxPerLane; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && e / gsz == g) {
+      if (grp[i] == g) {
         if (s[i] > m1) {
           m2 = m1;
           m1 = s[i];
@@ -192,12 +196,12 @@ __device__ float warp_select(const float (&s)[kMaxPerLane], int lane, int t, int
     kept |= 1u << i;
     last_kept = v;
   }
-  float margin = 1.0f;
+  float margin_group = 1.0f, margin = 1.0f;
   {
     float v = (lane < G && !((kept >> lane) & 1u)) ? my_gs : -2.0f;
     int i = lane;
     warp_argmax(v, i);
-    if (v > -1.5f) margin = last_kept - v;
+    if (v > -1.5f) margin_group = last_kept - v;
   }
 
   // choose the K best experts of the kept groups (ties to the lower index)
@@ -211,7 +215,7 @@ __device__ float warp_select(const float (&s)[kMaxPerLane], int lane, int t, int
 #pragma unroll
     for (int i = 0; i < kMaxPerLane; ++i) {
       const int e = lane + 32 * i;
-      if (e < E && ((kept >> (e / gsz)) & 1u) && !((taken >> i) & 1u) && better(s[i], e, v, idx)) {
+      if (grp[i] < 32 && ((kept >> grp[i]) & 1u) && !((taken >> i) & 1u) && better(s[i], e, v, idx)) {
         v = s[i];
         idx = e;
       }
@@ -236,7 +240,7 @@ __device__ float warp_select(const float (&s)[kMaxPerLane], int lane, int t, int
 #pragma unroll
     for (int i = 0; i < kMaxPerLane; ++i) {
       const int e = lane + 32 * i;
-      if (e < E && ((kept >> (e / gsz)) & 1u) && !((taken >> i) & 1u) && better(s[i], e, v, idx)) {
+      if (grp[i] < 32 && ((kept >> grp[i]) & 1u) && !((taken >> i) & 1u) && better(s[i], e, v, idx)) {
         v = s[i];
         idx = e;
       }
@@ -244,6 +248,12 @@ __device__ float warp_select(const float (&s)[kMaxPerLane], int lane, int t, int
     warp_argmax(v, idx);
     const float last_s = __shfl_sync(0xffffffffu, my_s, K - 1);
     if (v > -1.5f) margin = fminf(margin, last_s - v);
+    // gaps between consecutive slots: the slot order is a decision too
+    const float next_s = __shfl_down_sync(0xffffffffu, my_s, 1);
+    float gap = (lane + 1 < K) ? my_s - next_s : 1.0f;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) gap = fminf(gap, __shfl_xor_sync(0xffffffffu, gap, off));
+    margin = fminf(margin, gap);
   }
   if (lane < K) {
     float w = 0.f;
@@ -255,7 +265,7 @@ __device__ float warp_select(const float (&s)[kMaxPerLane], int lane, int t, int
     topk_idx[static_cast<size_t>(t) * K + lane] = my_e;
     topk_w[static_cast<size_t>(t) * K + lane] = w;
   }
-  return margin;
+  return make_float2(margin_group, margin);
 }
 
 __global__ void __launch_bounds__(256) router_select_kernel(const float* __restrict__ logits, int T,
@@ -283,11 +293,10 @@ constexpr int kTcMaxSplits = 16;
 constexpr uint64_t kTcWaitNs = 2000000000ull;
 constexpr uint64_t kTcDrainNs = 1000000000ull;
 
-// out[s][e][k] = bf16 split s of W_r[k][e] (rows e >= E are zero);
-// wt[e][k] = W_r[k][e] in fp32. Also resets the flagged-token count.
+// out[s][e][k] = bf16 split s of W_r[k][e] (rows e >= E are zero). Also
+// resets the flagged-token count.
 __global__ void __launch_bounds__(256) wr_split_kernel(const float* __restrict__ wr, int d, int E, int E_pad,
-                                                       uint16_t* __restrict__ out, float* __restrict__ wt,
-                                                       int32_t* __restrict__ flagged_count) {
+                                                       uint16_t* __restrict__ out, int32_t* __restrict__ flagged_count) {
   __shared__ float tile[32][33];
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *flagged_count = 0;
   const int k0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
@@ -310,7 +319,6 @@ __global__ void __launch_bounds__(256) wr_split_kernel(const float* __restrict__
     out[o] = __bfloat16_as_ushort(hi);
     out[plane + o] = __bfloat16_as_ushort(mid);
     out[2 * plane + o] = __bfloat16_as_ushort(lo);
-    if (e < E) wt[static_cast<size_t>(e) * d + k] = w;
   }
 }
 
@@ -473,14 +481,16 @@ __global__ void __launch_bounds__(192, 1) router_tc_kernel(const __grid_constant
 }
 
 // One warp per token: the tensor-core logits (partials summed in a fixed
-// order), sigmoid and the group-limited selection. Where the smaller decision
-// margin could be within the tensor-core error of zero, the token is flagged
-// for an fp32 recompute of all its logits.
+// order), sigmoid, the group-limited selection and its weights. Where a
+// decision margin (kept groups, chosen experts, slot order) could be within
+// the tensor-core error of zero, the token is flagged for an fp32 recompute
+// of all its logits; elsewhere the decisions equal those of exact fp32
+// logits and only the weights carry the tensor-core error (about 1e-6
+// relative).
 __global__ void __launch_bounds__(256) router_select_flag_kernel(const float* __restrict__ part, int splits, int T,
                                                                  int E, int G, int Gk, int K, float scale,
                                                                  int32_t* __restrict__ topk_idx,
                                                                  float* __restrict__ topk_w,
-                                                                 int32_t* __restrict__ flags,
                                                                  int32_t* __restrict__ flagged,
                                                                  int32_t* __restrict__ flagged_count,
                                                                  int32_t* status) {
@@ -511,137 +521,153 @@ __global__ void __launch_bounds__(256) router_select_flag_kernel(const float* __
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, off));
-  const float margin = warp_select(s, lane, t, E, G, Gk, K, scale, topk_idx, topk_w, status);
-  // Measured on Beam-shape inputs (|logit| <= 6): tensor-core score errors
-  // <= 5e-6, so margin errors <= 2e-5; the threshold keeps a factor >= 4.
-  const bool narrow = margin < 4e-5f + 1e-5f * lmax;
-  if (lane == 0) {
-    flags[t] = narrow ? 1 : 0;
-    if (narrow) flagged[atomicAdd(flagged_count, 1)] = t;
-  }
+  const float2 margin = warp_select(s, lane, t, E, G, Gk, K, scale, topk_idx, topk_w, status);
+  // Score error bound of the tensor-core logits: measured at most 4.7e-6 on
+  // Beam-shape inputs (|logit| <= 6, over a million scores); e_s keeps a factor
+  // of at least 2.5. A group score sums two scores and a group margin compares
+  // two group scores (4 e_s); expert margins and slot gaps compare two scores.
+  const float e_s = 1e-5f + 5e-7f * lmax;
+  const bool narrow = margin.x < 4.f * e_s || margin.y < 2.f * e_s;
+  if (lane == 0 && narrow) flagged[atomicAdd(flagged_count, 1)] = t;
 }
 
-// One warp per token (not flagged): FFMA dot products x[t] . W_r[:, e] for the
-// token's K chosen experts (wt = W_r transposed, rows contiguous), sigmoid,
-// slots sorted by (score desc, id asc), weights = scale * s / sum(s).
-__global__ void __launch_bounds__(256) router_refine_kernel(const uint16_t* __restrict__ x,
-                                                            const float* __restrict__ wt, int T, int d, int K,
-                                                            float scale, const int32_t* __restrict__ flags,
-                                                            int32_t* __restrict__ topk_idx,
-                                                            float* __restrict__ topk_w, int32_t* status) {
-  __shared__ float s_sorted[8][32];
-  __shared__ int e_sorted[8][32];
-  const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
-  const int t = blockIdx.x * 8 + wl;
-  if (t >= T || flags[t]) return;
-  const int my_e = (lane < K) ? topk_idx[static_cast<size_t>(t) * K + lane] : 0;
-  const uint2* xr = reinterpret_cast<const uint2*>(x + static_cast<size_t>(t) * d);  // 4 bf16 per uint2
-  float my_l = 0.f;
-  for (int k = 0; k < K; ++k) {
-    const int e = __shfl_sync(0xffffffffu, my_e, k);
-    const float4* wr = reinterpret_cast<const float4*>(wt + static_cast<size_t>(e) * d);
-    float acc = 0.f;
-    for (int c = lane; c < d / 4; c += 32) {
-      const uint2 xv = xr[c];
-      const float4 w4 = wr[c];
-      acc = fmaf(__uint_as_float(xv.x << 16), w4.x, acc);
-      acc = fmaf(__uint_as_float(xv.x & 0xFFFF0000u), w4.y, acc);
-      acc = fmaf(__uint_as_float(xv.y << 16), w4.z, acc);
-      acc = fmaf(__uint_as_float(xv.y & 0xFFFF0000u), w4.w, acc);
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == k) my_l = acc;
-  }
-  const float my_s = (lane < K) ? 1.0f / (1.0f + expf(-my_l)) : -1.f;
-  int rank = 0;
-  for (int j = 0; j < K; ++j) {
-    const float sj = __shfl_sync(0xffffffffu, my_s, j);
-    const int ej = __shfl_sync(0xffffffffu, my_e, j);
-    if (lane < K && j != lane && better(sj, ej, my_s, my_e)) ++rank;
-  }
-  if (lane < K) {
-    s_sorted[wl][rank] = my_s;
-    e_sorted[wl][rank] = my_e;
-  }
-  __syncwarp();
-  float sum = 0.f;
-  for (int j = 0; j < K; ++j) sum += s_sorted[wl][j];
-  if (lane < K) {
-    const float sv = s_sorted[wl][lane];
-    topk_idx[static_cast<size_t>(t) * K + lane] = e_sorted[wl][lane];
-    topk_w[static_cast<size_t>(t) * K + lane] = (sum > 0.f) ? scale * sv / sum : 0.f;
-  }
-  if (lane == 0 && !(sum > 0.f)) latch_status(status, MOE_DEV_ZERO_SUM);
-}
-
-// Flagged tokens (looping over the flagged list): every logit as an fp32
-// FFMA dot product, 1024 threads = 4 hidden-dimension quarters x 256 experts,
-// each quarter summed in index order and the four quarters added in a fixed
-// order; then one warp per token runs the full selection. Tokens per CTA
-// (1..kFlagTokens) follow the flagged count so the work spreads over the SMs;
-// the staged activations are k-major (a token group's values at one k are
-// contiguous), so each hidden index costs one weight load and two 16-byte
-// shared loads.
-constexpr int kFlagTokens = 8;
+// Flagged tokens: every logit as an fp32 FFMA dot product. Work items are
+// (group of up to kFlagTokens flagged tokens, quarter of the hidden
+// dimension), taken round-robin by the CTAs; an item streams its rows of W_r
+// through shared memory in chunks of kFlagRows rows by bulk-async copies (a
+// 4-deep ring), thread (q, e) of the 1024 adds rows q, q+4, ... of each chunk
+// for expert e, and the four sums are added in a fixed order into the
+// item's partial logits part[quarter][i][e].
+constexpr int kFlagTokens = 4;
 constexpr int kFlagThreads = 1024;
+constexpr int kFlagRows = 32;    // W_r rows per chunk (32 x E fp32)
+constexpr int kFlagRing = 4;
+constexpr int kFlagSplits = 4;   // hidden-dimension quarters per token group
 
-__global__ void __launch_bounds__(kFlagThreads) router_flagged_kernel(
-    const uint16_t* __restrict__ x, const float* __restrict__ wr, int d, int E, int G, int Gk, int K, float scale,
-    const int32_t* __restrict__ flagged, const int32_t* __restrict__ flagged_count, int32_t* __restrict__ topk_idx,
-    float* __restrict__ topk_w, int32_t* status) {
-  extern __shared__ float4 xs4[];                // [d][kFlagTokens / 4]: x of the group's tokens, k-major
-  __shared__ float part[4][kFlagTokens][256];    // per-quarter partial logits, then scores in [0]
-  float* xs = reinterpret_cast<float*>(xs4);
+__global__ void __launch_bounds__(kFlagThreads) router_flagged_logits_kernel(
+    const uint16_t* __restrict__ x, const float* __restrict__ wr, int d, int E,
+    const int32_t* __restrict__ flagged, const int32_t* __restrict__ flagged_count, float* __restrict__ part_out,
+    int32_t* status) {
+  extern __shared__ __align__(16) uint8_t fsm[];
+  float4* xs4 = reinterpret_cast<float4*>(fsm);                      // [d / kFlagSplits]: x of <= 4 tokens at k
+  float* wring = reinterpret_cast<float*>(fsm + sizeof(float4) * (d / kFlagSplits));  // [ring][rows][E]
+  __shared__ float part[4][kFlagTokens][256];
+  __shared__ __align__(8) uint64_t bar[kFlagRing];
+  __shared__ int abort_flag;
+  volatile int* abort = &abort_flag;
   const int n = *flagged_count;
-  const int per = max(1, min(kFlagTokens, (n + gridDim.x - 1) / gridDim.x));
-  const int e = threadIdx.x & 255, qd = threadIdx.x >> 8;
-  const int kq = d / 4;
-  for (int i0 = blockIdx.x * per; i0 < n; i0 += gridDim.x * per) {
-    const int nt = min(per, n - i0);
-    for (int idx = threadIdx.x; idx < d * kFlagTokens; idx += blockDim.x) {
-      const int k = idx / kFlagTokens, j = idx % kFlagTokens;
-      xs[idx] = (j < nt) ? bf16_bits_to_float(x[static_cast<size_t>(flagged[i0 + j]) * d + k]) : 0.f;
-    }
-    __syncthreads();
-    if (e < E) {
-      float acc[kFlagTokens];
+  if (n == 0) return;
+  const int groups = (n + kFlagTokens - 1) / kFlagTokens;
+  const int e = threadIdx.x & 255, q = threadIdx.x >> 8;
+  const uint32_t chunk_bytes = static_cast<uint32_t>(kFlagRows) * E * sizeof(float);
+  const int kq = d / kFlagSplits;         // hidden elements of one item
+  const int nchunks = kq / kFlagRows;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kFlagRing; ++i) mbar_init(&bar[i], 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  uint32_t issued = 0, consumed = 0;  // chunk copies issued (thread 0) / waited
+  for (int item = blockIdx.x; item < groups * kFlagSplits; item += gridDim.x) {
+    const int i0 = (item / kFlagSplits) * kFlagTokens, z = item % kFlagSplits;
+    const int nt = min(kFlagTokens, n - i0);
+    const int k0 = z * kq;
+    const float* wsrc = wr + static_cast<size_t>(k0) * E;
+    for (int k = threadIdx.x; k < kq; k += blockDim.x) {
+      float v[kFlagTokens];
 #pragma unroll
-      for (int j = 0; j < kFlagTokens; ++j) acc[j] = 0.f;
-      for (int k = qd * kq; k < (qd + 1) * kq; ++k) {
-        const float w = wr[static_cast<size_t>(k) * E + e];
-        const float4 a0 = xs4[k * 2], a1 = xs4[k * 2 + 1];
-        acc[0] = fmaf(a0.x, w, acc[0]);
-        acc[1] = fmaf(a0.y, w, acc[1]);
-        acc[2] = fmaf(a0.z, w, acc[2]);
-        acc[3] = fmaf(a0.w, w, acc[3]);
-        acc[4] = fmaf(a1.x, w, acc[4]);
-        acc[5] = fmaf(a1.y, w, acc[5]);
-        acc[6] = fmaf(a1.z, w, acc[6]);
-        acc[7] = fmaf(a1.w, w, acc[7]);
-      }
-#pragma unroll
-      for (int j = 0; j < kFlagTokens; ++j) part[qd][j][e] = acc[j];
+      for (int j = 0; j < kFlagTokens; ++j)
+        v[j] = (j < nt) ? bf16_bits_to_float(x[static_cast<size_t>(flagged[i0 + j]) * d + k0 + k]) : 0.f;
+      xs4[k] = make_float4(v[0], v[1], v[2], v[3]);
     }
-    __syncthreads();
-    if (qd == 0 && e < E) {
-      for (int j = 0; j < nt; ++j) {
-        const float l = ((part[0][j][e] + part[1][j][e]) + part[2][j][e]) + part[3][j][e];
-        part[0][j][e] = 1.0f / (1.0f + expf(-l));
+    if (threadIdx.x == 0) {
+      for (int c = 0; c < kFlagRing - 1 && c < nchunks; ++c) {
+        const uint32_t slot = issued % kFlagRing;
+        mbar_arrive_expect_tx(&bar[slot], chunk_bytes);
+        bulk_load(wring + static_cast<size_t>(slot) * kFlagRows * E, wsrc + static_cast<size_t>(c) * kFlagRows * E,
+                  chunk_bytes, &bar[slot]);
+        ++issued;
       }
     }
     __syncthreads();
-    const int wj = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (wj < nt) {
-      float s[kMaxPerLane];
-#pragma unroll
-      for (int j = 0; j < kMaxPerLane; ++j) {
-        const int ee = lane + 32 * j;
-        s[j] = (ee < E) ? part[0][wj][ee] : -1.0f;
+    float acc[kFlagTokens] = {0.f, 0.f, 0.f, 0.f};
+    for (int c = 0; c < nchunks; ++c) {
+      if (threadIdx.x == 0 && c + kFlagRing - 1 < nchunks) {
+        const uint32_t slot = issued % kFlagRing;  // its previous chunk was consumed before the last barrier
+        mbar_arrive_expect_tx(&bar[slot], chunk_bytes);
+        bulk_load(wring + static_cast<size_t>(slot) * kFlagRows * E,
+                  wsrc + static_cast<size_t>(c + kFlagRing - 1) * kFlagRows * E, chunk_bytes, &bar[slot]);
+        ++issued;
       }
-      warp_select(s, lane, flagged[i0 + wj], E, G, Gk, K, scale, topk_idx, topk_w, status);
+      const uint32_t slot = consumed % kFlagRing;
+      // On a timeout every later wait returns at once (the loop stays the same
+      // for all threads, so the barriers below match); the status is latched.
+      if (!mbar_wait_bounded(&bar[slot], (consumed / kFlagRing) & 1u, 1ll << 40, 2000000000ull, abort) && !*abort) {
+        latch_status(status, MOE_DEV_TIMEOUT);
+        *abort = 1;
+      }
+      ++consumed;
+      const float* wc = wring + static_cast<size_t>(slot) * kFlagRows * E;
+      if (e < E) {
+#pragma unroll
+        for (int rr = q; rr < kFlagRows; rr += 4) {
+          const float w = wc[rr * E + e];
+          const float4 a = xs4[c * kFlagRows + rr];
+          acc[0] = fmaf(a.x, w, acc[0]);
+          acc[1] = fmaf(a.y, w, acc[1]);
+          acc[2] = fmaf(a.z, w, acc[2]);
+          acc[3] = fmaf(a.w, w, acc[3]);
+        }
+      }
+      __syncthreads();  // the slot may be refilled after every thread is done with it
+    }
+#pragma unroll
+    for (int j = 0; j < kFlagTokens; ++j) part[q][j][e] = acc[j];
+    __syncthreads();
+    if (q == 0 && e < E) {
+      for (int j = 0; j < nt; ++j)
+        part_out[(static_cast<size_t>(z) * n + i0 + j) * E + e] =
+            ((part[0][j][e] + part[1][j][e]) + part[2][j][e]) + part[3][j][e];
     }
     __syncthreads();
+  }
+  // After an abort some waits returned early: let every copy issued into each
+  // slot land (bounded) before the CTA exits.
+  if (*abort && threadIdx.x == 0) {
+    for (uint32_t sl = 0; sl < kFlagRing; ++sl) {
+      if (issued > sl) {
+        const uint32_t f = sl + kFlagRing * ((issued - 1 - sl) / kFlagRing);
+        mbar_wait_bounded(&bar[sl], (f / kFlagRing) & 1u, 1ll << 40, 1000000000ull, nullptr);
+      }
+    }
+  }
+  __syncthreads();
+}
+
+// One warp per flagged token: the quarters' partial logits summed in order,
+// sigmoid and the full selection.
+__global__ void __launch_bounds__(256) router_flagged_select_kernel(const float* __restrict__ part, int E, int G,
+                                                                   int Gk, int K, float scale,
+                                                                   const int32_t* __restrict__ flagged,
+                                                                   const int32_t* __restrict__ flagged_count,
+                                                                   int32_t* __restrict__ topk_idx,
+                                                                   float* __restrict__ topk_w, int32_t* status) {
+  const int n = *flagged_count;
+  const int lane = threadIdx.x & 31;
+  for (int i = blockIdx.x * 8 + (threadIdx.x >> 5); i < n; i += gridDim.x * 8) {
+    float sv[kMaxPerLane];
+#pragma unroll
+    for (int j = 0; j < kMaxPerLane; ++j) {
+      const int e = lane + 32 * j;
+      sv[j] = -1.0f;
+      if (e < E) {
+        float l = 0.f;
+        for (int z = 0; z < kFlagSplits; ++z) l += part[(static_cast<size_t>(z) * n + i) * E + e];
+        sv[j] = 1.0f / (1.0f + expf(-l));
+      }
+    }
+    warp_select(sv, lane, flagged[i], E, G, Gk, K, scale, topk_idx, topk_w, status);
   }
 }
 
@@ -675,29 +701,25 @@ int encode_router_map(CUtensorMap* map, const void* base, uint64_t inner, uint64
 
 int router_epad(int E) { return ((E + 15) / 16) * 16; }
 
-// The fp32 recompute stages 8 tokens' activations (32 d bytes) in shared memory.
+// The fp32 recompute works on hidden-dimension quarters of whole 32-row chunks.
 bool router_uses_tensor_cores(int T, int E, int d) {
-  return T >= kRouterTcMinTokens && router_epad(E) <= 256 && d <= 5120;
+  return T >= kRouterTcMinTokens && router_epad(E) <= 256 && d % (kFlagSplits * kFlagRows) == 0;
 }
 
-// Split of the hidden dimension over CTAs so that the token tiles cover the SMs.
+// Split of the hidden dimension over CTAs: the largest that keeps all CTAs in
+// one wave (one CTA per SM), so small batches still use most SMs.
 int router_tc_splits(int T, int d, int num_sms) {
   const int tiles = (T + kTcTokens - 1) / kTcTokens;
   const int kblocks = d / kTcBK;
-  const int target = (num_sms + tiles - 1) / tiles;
   int best = 1;
-  for (int s = 1; s <= kTcMaxSplits && s <= kblocks; ++s) {
-    if (kblocks % s) continue;
-    best = s;
-    if (s >= target) break;
-  }
+  for (int s = 1; s <= kTcMaxSplits && s <= kblocks; ++s)
+    if (kblocks % s == 0 && tiles * s <= num_sms) best = s;
   return best;
 }
 
 size_t router_tc_scratch_bytes(int T, int d, int E) {
   const size_t a = sizeof(uint16_t) * 3 * router_epad(E) * static_cast<size_t>(d);
-  const size_t b = sizeof(float) * static_cast<size_t>(E) * d;
-  return ((a + 255) & ~size_t(255)) + ((b + 255) & ~size_t(255)) + 2 * ((sizeof(int32_t) * T + 255) & ~size_t(255));
+  return ((a + 255) & ~size_t(255)) + ((sizeof(int32_t) * T + 255) & ~size_t(255));
 }
 
 cudaError_t launch_router_tc(const uint16_t* x, const float* w_r, void* scratch, float* part, int32_t* flagged_count,
@@ -711,11 +733,8 @@ cudaError_t launch_router_tc(const uint16_t* x, const float* w_r, void* scratch,
     return q;
   };
   uint16_t* w_split = reinterpret_cast<uint16_t*>(take(sizeof(uint16_t) * 3 * E_pad * static_cast<size_t>(d)));
-  float* wt = reinterpret_cast<float*>(take(sizeof(float) * static_cast<size_t>(E) * d));
-  int32_t* flags = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * T));
   int32_t* flagged = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * T));
-  wr_split_kernel<<<dim3(d / 32, (E_pad + 31) / 32), 256, 0, stream>>>(w_r, d, E, E_pad, w_split, wt,
-                                                                         flagged_count);
+  wr_split_kernel<<<dim3(d / 32, (E_pad + 31) / 32), 256, 0, stream>>>(w_r, d, E, E_pad, w_split, flagged_count);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   CUtensorMap tmX, tmW;
@@ -738,17 +757,18 @@ cudaError_t launch_router_tc(const uint16_t* x, const float* w_r, void* scratch,
   if (err != cudaSuccess) return err;
   router_tc_kernel<<<dim3((T + kTcTokens - 1) / kTcTokens, splits), 192, smem, stream>>>(tmX, tmW, a);
   router_select_flag_kernel<<<(T + 7) / 8, 256, 0, stream>>>(part, splits, T, E, n_groups, topk_groups, top_k,
-                                                             routed_scale, topk_idx, topk_w, flags, flagged,
-                                                             flagged_count, status);
-  router_refine_kernel<<<(T + 7) / 8, 256, 0, stream>>>(x, wt, T, d, top_k, routed_scale, flags, topk_idx, topk_w,
-                                                        status);
-  const size_t xs_bytes = sizeof(float) * static_cast<size_t>(d) * kFlagTokens;  // d <= 5120 for this path
-  err = cudaFuncSetAttribute(router_flagged_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                             routed_scale, topk_idx, topk_w, flagged, flagged_count,
+                                                             status);
+  // the tensor-core partials were consumed by the selection: reuse `part` for the recompute
+  const size_t xs_bytes = sizeof(float4) * static_cast<size_t>(d / kFlagSplits) +
+                          sizeof(float) * static_cast<size_t>(kFlagRing) * kFlagRows * E;
+  err = cudaFuncSetAttribute(router_flagged_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(xs_bytes));
   if (err != cudaSuccess) return err;
-  router_flagged_kernel<<<num_sms, kFlagThreads, xs_bytes, stream>>>(x, w_r, d, E, n_groups, topk_groups, top_k,
-                                                                     routed_scale, flagged, flagged_count, topk_idx,
-                                                                     topk_w, status);
+  router_flagged_logits_kernel<<<num_sms, kFlagThreads, xs_bytes, stream>>>(x, w_r, d, E, flagged, flagged_count,
+                                                                            part, status);
+  router_flagged_select_kernel<<<num_sms, 256, 0, stream>>>(part, E, n_groups, topk_groups, top_k, routed_scale,
+                                                            flagged, flagged_count, topk_idx, topk_w, status);
   return cudaGetLastError();
 }
 
