@@ -84,10 +84,13 @@ PROFILE_CASES = {
     # ~1024 tokens per expert, like the skewed workload's compute-bound tiles
     "profile_dense": W.MoEConfig("profile_dense", T=2048, d=5120, E=16, n_groups=4, topk_groups=4, top_k=8,
                                  inter=2560),
+    # the NVFP4 prefill shape with 32 experts (0.7 GB of NVFP4 weights)
+    "profile_nvfp4": W.MoEConfig("profile_nvfp4", T=512, d=5120, E=32, n_groups=8, topk_groups=4, top_k=8,
+                                 inter=2560, wfmt="nvfp4"),
 }
 
 DEFAULT_STEPS = {"decode": 300, "prefill": 200, "skewed": 40, "nvfp4": 200, "profile_decode": 20,
-                 "profile_prefill": 20, "profile_dense": 20}
+                 "profile_prefill": 20, "profile_dense": 20, "profile_nvfp4": 20}
 
 
 def workload_cfg(name):
@@ -112,25 +115,28 @@ def load_peaks():
     return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
 
 
-def profiled_traffic(kernel, algorithmic_bytes):
-    """DRAM bytes of one launch of `kernel`, from the committed ncu capture of a smaller case
-    scaled by algorithmic bytes (weights of touched experts + activations); None when the
-    kernel's sources changed since the capture."""
+def profiled_traffic(workload, kernel, algorithmic_bytes):
+    """DRAM bytes of one launch of `kernel`, from the committed ncu capture of the small case that
+    stands for `workload`, scaled by algorithmic bytes (weights of touched experts + activations);
+    None when the kernel's sources changed since the capture."""
     import hashlib
     p = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(p):
         return None, "no capture"
-    rec = json.load(open(p)).get(kernel)
-    if not rec:
+    rec = json.load(open(p))
+    cap_name = rec.get("capture_for_workload", {}).get(workload)
+    cap = rec.get("captures", {}).get(cap_name) if cap_name else None
+    k = cap["kernels"].get(kernel) if cap else None
+    if not k:
         return None, "no capture"
     h = hashlib.sha256()
     for src in rec["sources"]:
         h.update(open(os.path.join(ROOT, src), "rb").read())
     if h.hexdigest() != rec["source_sha256"]:
         return None, "kernel changed since the capture"
-    measured = rec["dram_bytes_read"] + rec["dram_bytes_write"]
-    return int(round(measured * algorithmic_bytes / rec["algorithmic_bytes"])), (
-        f"ncu dram__bytes_read+write of {rec['capture']}, scaled by algorithmic bytes")
+    measured = k["dram_bytes_read"] + k["dram_bytes_write"]
+    return int(round(measured * algorithmic_bytes / k["algorithmic_bytes"])), (
+        f"ncu dram__bytes_read+write of {cap_name} ({cap['workload']}), scaled by algorithmic bytes")
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -353,8 +359,8 @@ def run_ours(args, rank, world, local_rank):
         achieved, peak, unit = g1["bytes"] / gemm1_s / 1e9, peaks["hbm_gbs"], "GB/s"
     else:
         achieved, peak, unit = g1["flops"] / gemm1_s / 1e12, peaks["bf16_tflops"], "TFLOP/s"
-    traffic, traffic_src = (profiled_traffic("expert_gemm_kernel<GLU>", g1["bytes"]) if cfg.wfmt == "bf16"
-                            else (None, "no capture of the NVFP4 kernel"))
+    kname = "expert_gemm_kernel<GLU>" if cfg.wfmt == "bf16" else "expert_gemm_kernel<GLU, NVFP4>"
+    traffic, traffic_src = profiled_traffic(cfg.name, kname, g1["bytes"])
     line = {
         "metric": METRIC, "value": round(tokens_per_s, 1), "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
@@ -364,7 +370,7 @@ def run_ours(args, rank, world, local_rank):
                    "top_k": cfg.top_k, "parallelism": f"replicas x{world}",
                    "l2": f"no flush: {touched} experts x {3 * cfg.d * cfg.inter * weight_bytes_per_param(cfg) / 1e6:.1f} MB "
                          f"of weights streamed per step exceed the 126 MB L2"},
-        "roofline": {"kernel": "expert_gemm_kernel<GLU> (GEMM1 + SwiGLU)", "bound": bound,
+        "roofline": {"kernel": f"{kname} (GEMM1 + SwiGLU)", "bound": bound,
                      "achieved": round(achieved, 1), "peak": peak, "unit": unit, "frac": round(achieved / peak, 4),
                      "peak_source": f"{peaks['source']} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops'})",
                      "traffic": traffic, "traffic_source": traffic_src, "algorithmic_bytes": g1["bytes"], "algorithmic_flops": g1["flops"],

@@ -25,10 +25,12 @@
 //   warp 1      TMEM allocator and single-thread tcgen05.mma issuer
 //   warps 2..9  epilogue, two warpgroups splitting the token columns:
 //               tcgen05.ld, SwiGLU in FP32 (GEMM1) or fp32 store (GEMM2)
-//   warps 10..13 (NVFP4 weights only) converters: e2m1 codes times their e4m3
+//   warps 10..17 (NVFP4 weights only) converters: e2m1 codes times their e4m3
 //               block scale, which is exact in bf16, written in the 128-byte
 //               swizzled operand layout the MMA reads; the fp32 tensor scale
-//               is applied to the accumulator in the epilogue.
+//               is applied to the accumulator in the epilogue. NVFP4 uses two
+//               rings: a deep one for what TMA brings (packed codes, token
+//               rows) and a 2-slot one for the decoded bf16 weight tiles.
 // Work items {expert, weight tile, first row, tokens} are built on the device
 // from the expert offsets (no host synchronisation) and taken round-robin.
 // Every mbarrier wait is bounded; on expiry the CTA latches MOE_DEV_TIMEOUT,
@@ -55,9 +57,10 @@ constexpr uint64_t kDrainNs = 1000000000ull;             // 1 s bound for draini
 constexpr uint64_t kWaitNs = 2000000000ull;              // 2 s bound of a pipeline wait
 constexpr int kSmemLimit = 232448;                       // 227 KB opt-in per block
 
-constexpr int kEpiThreads = 256;  // two epilogue warpgroups
-constexpr int kConvBase = 320;    // first converter thread (NVFP4)
-constexpr int threads_for(bool w4) { return w4 ? 448 : 320; }
+constexpr int kEpiThreads = 256;    // two epilogue warpgroups
+constexpr int kConvBase = 320;      // first converter thread (NVFP4)
+constexpr int kConvThreads = 256;   // two converter threads per weight row (NVFP4)
+constexpr int threads_for(bool w4) { return w4 ? kConvBase + kConvThreads : 320; }
 
 struct GemmArgs {
   const int4* items;
@@ -72,6 +75,8 @@ struct GemmArgs {
   uint32_t stage_bytes;
   uint32_t b_offset;  // token tile offset inside a stage
   uint32_t p_offset;  // packed weight tile offset inside a stage (NVFP4)
+  uint32_t conv_offset;  // decoded weight ring (NVFP4): conv_stages slots of two bf16 tiles
+  int conv_stages;
   uint16_t* h_out;    // GEMM1 output [R][Nw] bf16
   float* y_out;       // GEMM2 output [R][Nw] fp32
   const float* ts0;   // per-expert scale applied to accumulator 0 (NVFP4), or null
@@ -124,22 +129,23 @@ __device__ __forceinline__ uint32_t scale_pair(uint32_t byte) {
   return s;
 }
 
-// Decode row r of one packed 128 x 64 weight tile into the 128-byte swizzled
-// bf16 tile: 16-byte chunk c of row r lives at chunk (c ^ (r & 7)).
-// `sc` holds the row's four block scales of this K slice (byte j: elements
-// 16j..16j+15).
-__device__ __forceinline__ void decode_row(const uint8_t* packed_tile, uint8_t* bf16_tile, int r, uint32_t sc) {
-  const uint4 p0 = *reinterpret_cast<const uint4*>(packed_tile + r * 32);
-  const uint4 p1 = *reinterpret_cast<const uint4*>(packed_tile + r * 32 + 16);
-  const uint32_t w[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+// Decode half h (elements 32h..32h+31) of row r of one packed 128 x 64 weight
+// tile into the 128-byte swizzled bf16 tile: 16-byte chunk c of row r lives
+// at chunk (c ^ (r & 7)). `sc` holds the row's four block scales of this K
+// slice (byte j: elements 16j..16j+15).
+__device__ __forceinline__ void decode_half_row(const uint8_t* packed_tile, uint8_t* bf16_tile, int r, int h,
+                                                uint32_t sc) {
+  const uint4 p = *reinterpret_cast<const uint4*>(packed_tile + r * 32 + h * 16);
+  const uint32_t w[4] = {p.x, p.y, p.z, p.w};
   uint8_t* row = bf16_tile + r * 128;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
+  for (int jj = 0; jj < 2; ++jj) {
+    const int j = 2 * h + jj;
     const uint32_t s2 = scale_pair((sc >> (8 * j)) & 0xFFu);
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int c = 2 * j + h;
-      *reinterpret_cast<uint4*>(row + ((c ^ (r & 7)) << 4)) = decode8(w[c], s2);
+    for (int hh = 0; hh < 2; ++hh) {
+      const int c = 2 * j + hh;
+      *reinterpret_cast<uint4*>(row + ((c ^ (r & 7)) << 4)) = decode8(w[2 * jj + hh], s2);
     }
   }
 }
@@ -151,7 +157,8 @@ __global__ void __launch_bounds__(threads_for(kW4), 1)
                        const __grid_constant__ CUtensorMap tmB128, const GemmArgs p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
-  __shared__ __align__(8) uint64_t conv_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t conv_bar[kMaxStages];        // decoded slot ready (NVFP4)
+  __shared__ __align__(8) uint64_t conv_empty_bar[kMaxStages];  // decoded slot free (NVFP4)
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
   __shared__ __align__(8) uint64_t accf_bar[kMaxAcc];
   __shared__ __align__(8) uint64_t acce_bar[kMaxAcc];
@@ -166,8 +173,11 @@ __global__ void __launch_bounds__(threads_for(kW4), 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(&full_bar[s], 1);
-      mbar_init(&conv_bar[s], 128);
       mbar_init(&empty_bar[s], 1);
+    }
+    for (int c = 0; c < p.conv_stages; ++c) {
+      mbar_init(&conv_bar[c], kConvThreads);
+      mbar_init(&conv_empty_bar[c], 1);
     }
     for (int a = 0; a < p.acc_bufs; ++a) {
       mbar_init(&accf_bar[a], 1);
@@ -250,9 +260,8 @@ __global__ void __launch_bounds__(threads_for(kW4), 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      int stage = 0, acc = 0;
-      uint32_t phase = 0, acc_phase = 0;
-      uint64_t* ready = kW4 ? conv_bar : full_bar;
+      int stage = 0, acc = 0, cstage = 0;
+      uint32_t phase = 0, acc_phase = 0, cphase = 0;
       for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
         const int4 item = p.items[it];
         const int n_mma = (item.w + 15) & ~15;
@@ -266,14 +275,18 @@ __global__ void __launch_bounds__(threads_for(kW4), 1)
         const uint32_t d1 = d0 + static_cast<uint32_t>(p.n_max);
         bool ok = true;
         for (int kb = 0; kb < kblocks; ++kb) {
-          if (!mbar_wait_bounded(&ready[stage], phase, p.wait_spins, kWaitNs, abort)) {
+          // NVFP4: the decoded slot is ready only after its raw stage landed
+          if (!mbar_wait_bounded(kW4 ? &conv_bar[cstage] : &full_bar[stage], kW4 ? cphase : phase, p.wait_spins,
+                                 kWaitNs, abort)) {
             if (!*abort) fail(p, abort, 3);
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sa = smem_u32(smem + static_cast<size_t>(stage) * p.stage_bytes);
-          const uint32_t sb = sa + p.b_offset;
+          const uint32_t st_addr = smem_u32(smem + static_cast<size_t>(stage) * p.stage_bytes);
+          const uint32_t sa = kW4 ? smem_u32(smem + p.conv_offset + static_cast<size_t>(cstage) * 2 * kATileBytes)
+                                  : st_addr;
+          const uint32_t sb = st_addr + p.b_offset;
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
             const uint64_t bdesc = sdesc_kmajor_sw128(sb + k * 32);
@@ -282,6 +295,13 @@ __global__ void __launch_bounds__(threads_for(kW4), 1)
             mma_bf16_ss(d1, sdesc_kmajor_sw128(sa + kATileBytes + k * 32), bdesc, idesc, accum);
           }
           mma_commit(&empty_bar[stage]);
+          if (kW4) {
+            mma_commit(&conv_empty_bar[cstage]);
+            if (++cstage == p.conv_stages) {
+              cstage = 0;
+              cphase ^= 1u;
+            }
+          }
           if (++stage == p.stages) {
             stage = 0;
             phase ^= 1u;
@@ -361,14 +381,17 @@ __global__ void __launch_bounds__(threads_for(kW4), 1)
     }
   } else if (kW4) {
     // ------------------------------------------------------------ NVFP4 converters
-    // Thread r decodes weight row r of every K slice. Block scales (4 per
-    // slice per row) are read 16 bytes (four slices) at a time from global
-    // memory, one group ahead, so the load latency hides behind decoding.
-    const int r = threadIdx.x - kConvBase;
+    // Threads 2r and 2r+1 decode the two halves of weight row r of every K
+    // slice (adjacent lanes read adjacent 16 bytes: no bank conflicts). Block
+    // scales (4 per slice per row) are read 16 bytes (four slices) at a time
+    // from global memory, one group ahead, so the load latency hides behind
+    // decoding.
+    const int cr = threadIdx.x - kConvBase;
+    const int r = cr >> 1, half = cr & 1;
     const int sf_ld = p.K / 16;        // bytes of block scales per weight row
     const int64_t rows_total = static_cast<int64_t>(p.E) * p.Nw;
-    int stage = 0;
-    uint32_t phase = 0;
+    int stage = 0, cstage = 0;
+    uint32_t phase = 0, cphase = 0;
     auto load_group = [&](int it, int g, uint4& s0, uint4& s1) {
       s0 = make_uint4(0, 0, 0, 0);
       s1 = make_uint4(0, 0, 0, 0);
@@ -391,18 +414,24 @@ __global__ void __launch_bounds__(threads_for(kW4), 1)
           if (kb + 4 < kblocks) load_group(it, (kb >> 2) + 1, nxt0, nxt1);
           else load_group(it + gridDim.x, 0, nxt0, nxt1);
         }
-        if (!mbar_wait_bounded(&full_bar[stage], phase, p.wait_spins, kWaitNs, abort)) {
+        if (!mbar_wait_bounded(&full_bar[stage], phase, p.wait_spins, kWaitNs, abort) ||
+            !mbar_wait_bounded(&conv_empty_bar[cstage], cphase ^ 1u, p.wait_spins, kWaitNs, abort)) {
           if (!*abort) fail(p, abort, 5);
           ok = false;
           break;
         }
         uint8_t* st = smem + static_cast<size_t>(stage) * p.stage_bytes;
+        uint8_t* dst = smem + p.conv_offset + static_cast<size_t>(cstage) * 2 * kATileBytes;
         const int q = kb & 3;
-        decode_row(st + p.p_offset, st, r, q == 0 ? cur0.x : q == 1 ? cur0.y : q == 2 ? cur0.z : cur0.w);
-        decode_row(st + p.p_offset + kPTileBytes, st + kATileBytes, r,
-                   q == 0 ? cur1.x : q == 1 ? cur1.y : q == 2 ? cur1.z : cur1.w);
+        decode_half_row(st + p.p_offset, dst, r, half, q == 0 ? cur0.x : q == 1 ? cur0.y : q == 2 ? cur0.z : cur0.w);
+        decode_half_row(st + p.p_offset + kPTileBytes, dst + kATileBytes, r, half,
+                        q == 0 ? cur1.x : q == 1 ? cur1.y : q == 2 ? cur1.z : cur1.w);
         fence_async_shared();  // generic-proxy writes -> visible to tcgen05.mma
-        mbar_arrive(&conv_bar[stage]);
+        mbar_arrive(&conv_bar[cstage]);
+        if (++cstage == p.conv_stages) {
+          cstage = 0;
+          cphase ^= 1u;
+        }
         if (++stage == p.stages) {
           stage = 0;
           phase ^= 1u;
@@ -536,24 +565,39 @@ int encode_packed_2d(CUtensorMap* map, const void* base, uint64_t inner_bytes, u
 }
 
 struct StageShape {
-  int stages, acc_bufs, acc_cols;
-  uint32_t stage_bytes, b_offset, p_offset;
+  int stages, acc_bufs, acc_cols, conv_stages;
+  uint32_t stage_bytes, b_offset, p_offset, conv_offset;
   size_t smem;
 };
+
+constexpr int kConvStages = 2;  // decoded NVFP4 weight slots
 
 StageShape stage_shape(bool glu, bool w4, int n_max) {
   StageShape s;
   (void)glu;
-  const uint32_t nA = 2u;
-  s.b_offset = kATileBytes * nA;
-  s.p_offset = s.b_offset + static_cast<uint32_t>(n_max) * BK * 2;
-  s.stage_bytes = s.p_offset + (w4 ? kPTileBytes * nA : 0u);
-  s.stage_bytes = (s.stage_bytes + 1023u) & ~1023u;
   const int budget = kSmemLimit - 1024 - 512;  // alignment slack + static barriers
-  s.stages = std::min(kMaxStages, budget / static_cast<int>(s.stage_bytes));
+  const uint32_t b_bytes = static_cast<uint32_t>(n_max) * BK * 2;
+  if (w4) {
+    // ring stage: token rows, then the two packed weight tiles; decoded tiles in their own ring
+    s.b_offset = 0;
+    s.p_offset = b_bytes;
+    s.stage_bytes = (b_bytes + 2 * kPTileBytes + 1023u) & ~1023u;
+    s.conv_stages = kConvStages;
+    const int conv_bytes = kConvStages * 2 * static_cast<int>(kATileBytes);
+    s.stages = std::min(kMaxStages, (budget - conv_bytes) / static_cast<int>(s.stage_bytes));
+    s.conv_offset = static_cast<uint32_t>(s.stages) * s.stage_bytes;
+    s.smem = 1024 + static_cast<size_t>(s.conv_offset) + conv_bytes;
+  } else {
+    s.b_offset = 2 * kATileBytes;
+    s.p_offset = s.b_offset + b_bytes;
+    s.stage_bytes = (s.p_offset + 1023u) & ~1023u;
+    s.conv_stages = 0;
+    s.stages = std::min(kMaxStages, budget / static_cast<int>(s.stage_bytes));
+    s.conv_offset = 0;
+    s.smem = 1024 + static_cast<size_t>(s.stages) * s.stage_bytes;
+  }
   s.acc_cols = 2 * n_max;
   s.acc_bufs = std::min(kMaxAcc, static_cast<int>(kTmemCols) / s.acc_cols);
-  s.smem = 1024 + static_cast<size_t>(s.stages) * s.stage_bytes;
   return s;
 }
 
@@ -567,6 +611,8 @@ cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUte
   args.stage_bytes = s.stage_bytes;
   args.b_offset = s.b_offset;
   args.p_offset = s.p_offset;
+  args.conv_offset = s.conv_offset;
+  args.conv_stages = s.conv_stages;
   args.n_max = n_max;
   cudaError_t err = cudaFuncSetAttribute(expert_gemm_kernel<kGLU, kW4>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s.smem));
