@@ -46,7 +46,7 @@ Layout make_layout(const moe_dims_t& d) {
                               router_uses_tensor_cores(d.T, d.E, d.d)
                                   ? std::max(4, router_tc_splits(Tc, d.d, kMaxSmsForLayout))  // 4: fp32 recompute
                                   : 1);
-  const ExpertPlan pl = plan_experts(d.T, d.d, d.E, d.top_k, d.inter);
+  const ExpertPlan pl = plan_experts(d.T, d.d, d.E, d.top_k, d.inter, d.wfmt == MOE_W_NVFP4);
   const int64_t nw = bitmap_words(d.T);
   size_t sz[R_NUM];
   sz[R_HDR] = sizeof(WsHeader);
@@ -155,7 +155,7 @@ moe_status_t do_permute(const moe_dims_t* d, const uint16_t* x, const int32_t* i
 moe_status_t do_ffn(const moe_dims_t* d, const uint16_t* x_perm, const int32_t* offsets,
                     const moe_expert_weights_t* w, float* y, void* ws, const Layout& L, cudaStream_t s,
                     cudaEvent_t after_gemm1 = nullptr) {
-  const ExpertPlan pl = plan_experts(d->T, d->d, d->E, d->top_k, d->inter);
+  const ExpertPlan pl = plan_experts(d->T, d->d, d->E, d->top_k, d->inter, d->wfmt == MOE_W_NVFP4);
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
   ExpertBuffers b;
   b.x_perm = x_perm;

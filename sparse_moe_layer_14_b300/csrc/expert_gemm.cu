@@ -26,11 +26,12 @@
 //   warps 2..9  epilogue, two warpgroups splitting the token columns:
 //               tcgen05.ld, SwiGLU in FP32 (GEMM1) or fp32 store (GEMM2)
 //   warps 10..17 (NVFP4 weights only) converters: e2m1 codes times their e4m3
-//               block scale, which is exact in bf16, written in the 128-byte
-//               swizzled operand layout the MMA reads; the fp32 tensor scale
-//               is applied to the accumulator in the epilogue. NVFP4 uses two
-//               rings: a deep one for what TMA brings (packed codes, token
-//               rows) and a 2-slot one for the decoded bf16 weight tiles.
+//               block scale, which is exact in bf16, written to tensor memory,
+//               from where the MMA reads its A operand (so decoded weights
+//               cost no shared-memory bandwidth, which the token operand and
+//               the copies need); the fp32 tensor scale is applied to the
+//               accumulator in the epilogue. The TMA ring holds packed codes
+//               and token rows; decoded tiles cycle through 2-4 TMEM slots.
 // Work items {expert, weight tile, first row, tokens} are built on the device
 // from the expert offsets (no host synchronisation) and taken round-robin.
 // Every mbarrier wait is bounded; on expiry the CTA latches MOE_DEV_TIMEOUT,
@@ -49,6 +50,8 @@ constexpr int BK = 64;        // K elements per pipeline stage (128 bytes of bf1
 constexpr int TOK_BOX = 16;   // token rows per TMA box
 constexpr int kMaxStages = 8;
 constexpr int kMaxAcc = 4;
+constexpr int kMaxConv = 4;   // decoded NVFP4 weight slots in TMEM
+constexpr int kConvCols = 64;  // TMEM columns of one slot: two 128 x 64 bf16 tiles
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kATileBytes = BM * BK * 2;            // 16 KB bf16 weight tile
 constexpr uint32_t kPTileBytes = BM * BK / 2;            // 4 KB packed e2m1 weight tile
@@ -59,7 +62,7 @@ constexpr int kSmemLimit = 232448;                       // 227 KB opt-in per bl
 
 constexpr int kEpiThreads = 256;    // two epilogue warpgroups
 constexpr int kConvBase = 320;      // first converter thread (NVFP4)
-constexpr int kConvThreads = 256;   // two converter threads per weight row (NVFP4)
+constexpr int kConvThreads = 256;   // one converter thread per row of each weight tile (NVFP4)
 constexpr int threads_for(bool w4) { return w4 ? kConvBase + kConvThreads : 320; }
 
 struct GemmArgs {
@@ -75,7 +78,7 @@ struct GemmArgs {
   uint32_t stage_bytes;
   uint32_t b_offset;  // token tile offset inside a stage
   uint32_t p_offset;  // packed weight tile offset inside a stage (NVFP4)
-  uint32_t conv_offset;  // decoded weight ring (NVFP4): conv_stages slots of two bf16 tiles
+  uint32_t a_col;     // first TMEM column of the decoded weight slots (NVFP4)
   int conv_stages;
   uint16_t* h_out;    // GEMM1 output [R][Nw] bf16
   float* y_out;       // GEMM2 output [R][Nw] fp32
@@ -92,10 +95,6 @@ __device__ __forceinline__ void fail(const GemmArgs& p, volatile int* abort, int
   latch_status(p.status, MOE_DEV_TIMEOUT);
   if (p.timeout_where) atomicCAS(p.timeout_where, 0, where);
   *abort = 1;
-}
-
-__device__ __forceinline__ void fence_async_shared() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // 8 e2m1 codes (one 32-bit word, element 2j in the low nibble of byte j) times
@@ -129,23 +128,23 @@ __device__ __forceinline__ uint32_t scale_pair(uint32_t byte) {
   return s;
 }
 
-// Decode half h (elements 32h..32h+31) of row r of one packed 128 x 64 weight
-// tile into the 128-byte swizzled bf16 tile: 16-byte chunk c of row r lives
-// at chunk (c ^ (r & 7)). `sc` holds the row's four block scales of this K
-// slice (byte j: elements 16j..16j+15).
-__device__ __forceinline__ void decode_half_row(const uint8_t* packed_tile, uint8_t* bf16_tile, int r, int h,
-                                                uint32_t sc) {
-  const uint4 p = *reinterpret_cast<const uint4*>(packed_tile + r * 32 + h * 16);
-  const uint32_t w[4] = {p.x, p.y, p.z, p.w};
-  uint8_t* row = bf16_tile + r * 128;
+// Decode row r of one packed 128 x 64 weight tile (64 e2m1 codes in 32 bytes)
+// with its four e4m3 block scales `sc` (byte j: elements 16j..16j+15) into 32
+// bf16x2 words in element order: word c holds elements 2c (low half) and 2c+1.
+__device__ __forceinline__ void decode_row(const uint8_t* packed_tile, int r, uint32_t sc, uint32_t (&out)[32]) {
+  const uint4 p0 = *reinterpret_cast<const uint4*>(packed_tile + r * 32);
+  const uint4 p1 = *reinterpret_cast<const uint4*>(packed_tile + r * 32 + 16);
+  const uint32_t w[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
 #pragma unroll
-  for (int jj = 0; jj < 2; ++jj) {
-    const int j = 2 * h + jj;
+  for (int j = 0; j < 4; ++j) {
     const uint32_t s2 = scale_pair((sc >> (8 * j)) & 0xFFu);
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
-      const int c = 2 * j + hh;
-      *reinterpret_cast<uint4*>(row + ((c ^ (r & 7)) << 4)) = decode8(w[2 * jj + hh], s2);
+      const uint4 v = decode8(w[2 * j + hh], s2);
+      out[8 * j + 4 * hh + 0] = v.x;
+      out[8 * j + 4 * hh + 1] = v.y;
+      out[8 * j + 4 * hh + 2] = v.z;
+      out[8 * j + 4 * hh + 3] = v.w;
     }
   }
 }
@@ -284,15 +283,21 @@ __global__ void __launch_bounds__(threads_for(kW4), 1)
           }
           tc_fence_after();
           const uint32_t st_addr = smem_u32(smem + static_cast<size_t>(stage) * p.stage_bytes);
-          const uint32_t sa = kW4 ? smem_u32(smem + p.conv_offset + static_cast<size_t>(cstage) * 2 * kATileBytes)
-                                  : st_addr;
           const uint32_t sb = st_addr + p.b_offset;
+          // NVFP4: slot cstage holds tile 0 in columns [0, 32), tile 1 in [32, 64);
+          // 8 columns per 16-wide K step
+          const uint32_t ta = tmem_base + p.a_col + static_cast<uint32_t>(cstage * kConvCols);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
             const uint64_t bdesc = sdesc_kmajor_sw128(sb + k * 32);
             const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
-            mma_bf16_ss(d0, sdesc_kmajor_sw128(sa + k * 32), bdesc, idesc, accum);
-            mma_bf16_ss(d1, sdesc_kmajor_sw128(sa + kATileBytes + k * 32), bdesc, idesc, accum);
+            if (kW4) {
+              mma_bf16_ts(d0, ta + k * 8, bdesc, idesc, accum);
+              mma_bf16_ts(d1, ta + kConvCols / 2 + k * 8, bdesc, idesc, accum);
+            } else {
+              mma_bf16_ss(d0, sdesc_kmajor_sw128(st_addr + k * 32), bdesc, idesc, accum);
+              mma_bf16_ss(d1, sdesc_kmajor_sw128(st_addr + kATileBytes + k * 32), bdesc, idesc, accum);
+            }
           }
           mma_commit(&empty_bar[stage]);
           if (kW4) {
@@ -381,52 +386,56 @@ __global__ void __launch_bounds__(threads_for(kW4), 1)
     }
   } else if (kW4) {
     // ------------------------------------------------------------ NVFP4 converters
-    // Threads 2r and 2r+1 decode the two halves of weight row r of every K
-    // slice (adjacent lanes read adjacent 16 bytes: no bank conflicts). Block
-    // scales (4 per slice per row) are read 16 bytes (four slices) at a time
-    // from global memory, one group ahead, so the load latency hides behind
-    // decoding.
-    const int cr = threadIdx.x - kConvBase;
-    const int r = cr >> 1, half = cr & 1;
-    const int sf_ld = p.K / 16;        // bytes of block scales per weight row
+    // Warp 10 + 4t + j decodes weight tile t (gate/up, or the two down tiles)
+    // for the 32 rows of the TMEM lane quarter it may access (warp % 4); one
+    // thread per row. Block scales (4 per slice per row) are read 16 bytes
+    // (four slices) at a time from global memory, one group ahead, so the load
+    // latency hides behind decoding.
+    const int t = (warp - kConvBase / 32) >> 2;
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    const int sf_ld = p.K / 16;  // bytes of block scales per weight row
     const int64_t rows_total = static_cast<int64_t>(p.E) * p.Nw;
+    const uint8_t* sf = t ? p.sf1 : p.sf0;
+    const int row_off = t ? kRow1 : 0;
+    const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + p.a_col +
+                            static_cast<uint32_t>(t * (kConvCols / 2));
     int stage = 0, cstage = 0;
     uint32_t phase = 0, cphase = 0;
-    auto load_group = [&](int it, int g, uint4& s0, uint4& s1) {
-      s0 = make_uint4(0, 0, 0, 0);
-      s1 = make_uint4(0, 0, 0, 0);
-      if (it >= n_items) return;
+    auto load_group = [&](int it, int g) {
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (it >= n_items) return v;
       const int4 item = p.items[it];
-      const int64_t row = static_cast<int64_t>(item.x) * p.Nw + item.y * kItemRows + r;
-      const int64_t row1 = row + kRow1;
+      const int64_t row = static_cast<int64_t>(item.x) * p.Nw + item.y * kItemRows + row_off + r;
       // padding rows past the last expert decode to zero
-      if (row < rows_total) s0 = __ldg(reinterpret_cast<const uint4*>(p.sf0 + row * sf_ld + g * 16));
-      if (row1 < rows_total) s1 = __ldg(reinterpret_cast<const uint4*>(p.sf1 + row1 * sf_ld + g * 16));
+      if (row < rows_total) v = __ldg(reinterpret_cast<const uint4*>(sf + row * sf_ld + g * 16));
+      return v;
     };
-    uint4 cur0, cur1, nxt0, nxt1;
-    load_group(blockIdx.x, 0, nxt0, nxt1);
+    uint4 cur = make_uint4(0, 0, 0, 0), nxt = load_group(blockIdx.x, 0);
     bool ok = true;
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
       for (int kb = 0; kb < kblocks; ++kb) {
         if ((kb & 3) == 0) {
-          cur0 = nxt0;
-          cur1 = nxt1;
-          if (kb + 4 < kblocks) load_group(it, (kb >> 2) + 1, nxt0, nxt1);
-          else load_group(it + gridDim.x, 0, nxt0, nxt1);
+          cur = nxt;
+          nxt = kb + 4 < kblocks ? load_group(it, (kb >> 2) + 1) : load_group(it + gridDim.x, 0);
         }
-        if (!mbar_wait_bounded(&full_bar[stage], phase, p.wait_spins, kWaitNs, abort) ||
-            !mbar_wait_bounded(&conv_empty_bar[cstage], cphase ^ 1u, p.wait_spins, kWaitNs, abort)) {
-          if (!*abort) fail(p, abort, 5);
+        // tcgen05.st is warp-collective: the whole warp proceeds or stops together
+        const bool ready = __all_sync(
+            0xffffffffu, mbar_wait_bounded(&full_bar[stage], phase, p.wait_spins, kWaitNs, abort) &&
+                             mbar_wait_bounded(&conv_empty_bar[cstage], cphase ^ 1u, p.wait_spins, kWaitNs, abort));
+        if (!ready) {
+          if (lane == 0 && !*abort) fail(p, abort, 5);
           ok = false;
           break;
         }
-        uint8_t* st = smem + static_cast<size_t>(stage) * p.stage_bytes;
-        uint8_t* dst = smem + p.conv_offset + static_cast<size_t>(cstage) * 2 * kATileBytes;
-        const int q = kb & 3;
-        decode_half_row(st + p.p_offset, dst, r, half, q == 0 ? cur0.x : q == 1 ? cur0.y : q == 2 ? cur0.z : cur0.w);
-        decode_half_row(st + p.p_offset + kPTileBytes, dst + kATileBytes, r, half,
-                        q == 0 ? cur1.x : q == 1 ? cur1.y : q == 2 ? cur1.z : cur1.w);
-        fence_async_shared();  // generic-proxy writes -> visible to tcgen05.mma
+        tc_fence_after();  // the MMAs that read this slot have completed
+        const uint8_t* packed = smem + static_cast<size_t>(stage) * p.stage_bytes + p.p_offset + t * kPTileBytes;
+        const int g = kb & 3;
+        uint32_t v[32];
+        decode_row(packed, r, g == 0 ? cur.x : g == 1 ? cur.y : g == 2 ? cur.z : cur.w, v);
+        tmem_st_32x32b_x32(t_lane + static_cast<uint32_t>(cstage * kConvCols), v);
+        tmem_st_wait();
+        tc_fence_before();
         mbar_arrive(&conv_bar[cstage]);
         if (++cstage == p.conv_stages) {
           cstage = 0;
@@ -566,38 +575,36 @@ int encode_packed_2d(CUtensorMap* map, const void* base, uint64_t inner_bytes, u
 
 struct StageShape {
   int stages, acc_bufs, acc_cols, conv_stages;
-  uint32_t stage_bytes, b_offset, p_offset, conv_offset;
+  uint32_t stage_bytes, b_offset, p_offset, a_col;
   size_t smem;
 };
-
-constexpr int kConvStages = 2;  // decoded NVFP4 weight slots
 
 StageShape stage_shape(bool glu, bool w4, int n_max) {
   StageShape s;
   (void)glu;
   const int budget = kSmemLimit - 1024 - 512;  // alignment slack + static barriers
   const uint32_t b_bytes = static_cast<uint32_t>(n_max) * BK * 2;
+  s.acc_cols = 2 * n_max;
   if (w4) {
-    // ring stage: token rows, then the two packed weight tiles; decoded tiles in their own ring
+    // ring stage: token rows, then the two packed weight tiles. TMEM: the
+    // accumulators, then 2-4 decoded slots (at least 3 where that leaves one
+    // accumulator buffer); n_max <= 192 keeps two slots.
     s.b_offset = 0;
     s.p_offset = b_bytes;
     s.stage_bytes = (b_bytes + 2 * kPTileBytes + 1023u) & ~1023u;
-    s.conv_stages = kConvStages;
-    const int conv_bytes = kConvStages * 2 * static_cast<int>(kATileBytes);
-    s.stages = std::min(kMaxStages, (budget - conv_bytes) / static_cast<int>(s.stage_bytes));
-    s.conv_offset = static_cast<uint32_t>(s.stages) * s.stage_bytes;
-    s.smem = 1024 + static_cast<size_t>(s.conv_offset) + conv_bytes;
+    s.acc_bufs = std::max(1, std::min(kMaxAcc, (static_cast<int>(kTmemCols) - 3 * kConvCols) / s.acc_cols));
+    s.a_col = static_cast<uint32_t>(s.acc_bufs * s.acc_cols);
+    s.conv_stages = std::min(kMaxConv, (static_cast<int>(kTmemCols) - static_cast<int>(s.a_col)) / kConvCols);
   } else {
     s.b_offset = 2 * kATileBytes;
     s.p_offset = s.b_offset + b_bytes;
     s.stage_bytes = (s.p_offset + 1023u) & ~1023u;
+    s.acc_bufs = std::min(kMaxAcc, static_cast<int>(kTmemCols) / s.acc_cols);
+    s.a_col = 0;
     s.conv_stages = 0;
-    s.stages = std::min(kMaxStages, budget / static_cast<int>(s.stage_bytes));
-    s.conv_offset = 0;
-    s.smem = 1024 + static_cast<size_t>(s.stages) * s.stage_bytes;
   }
-  s.acc_cols = 2 * n_max;
-  s.acc_bufs = std::min(kMaxAcc, static_cast<int>(kTmemCols) / s.acc_cols);
+  s.stages = std::min(kMaxStages, budget / static_cast<int>(s.stage_bytes));
+  s.smem = 1024 + static_cast<size_t>(s.stages) * s.stage_bytes;
   return s;
 }
 
@@ -605,13 +612,14 @@ template <bool kGLU, bool kW4>
 cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap (&b)[3], GemmArgs args,
                         int n_max, int grid, cudaStream_t stream) {
   const StageShape s = stage_shape(kGLU, kW4, n_max);
+  if (kW4 && s.conv_stages < 2) return cudaErrorInvalidValue;  // n_max above 192
   args.stages = s.stages;
   args.acc_bufs = s.acc_bufs;
   args.acc_cols = s.acc_cols;
   args.stage_bytes = s.stage_bytes;
   args.b_offset = s.b_offset;
   args.p_offset = s.p_offset;
-  args.conv_offset = s.conv_offset;
+  args.a_col = s.a_col;
   args.conv_stages = s.conv_stages;
   args.n_max = n_max;
   cudaError_t err = cudaFuncSetAttribute(expert_gemm_kernel<kGLU, kW4>,
@@ -623,16 +631,17 @@ cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUte
 
 }  // namespace
 
-ExpertPlan plan_experts(int T, int d, int E, int top_k, int inter) {
+ExpertPlan plan_experts(int T, int d, int E, int top_k, int inter, bool w4) {
   ExpertPlan p;
   // Token tile: a quarter above the mean tokens per expert, at least 64 and at
-  // most 256 (the MMA's largest N), never above the batch (an expert sees a
-  // token at most once). Smaller tiles leave shared memory for more pipeline
-  // stages; experts above the tile are split into near-equal tiles.
+  // most 256 (the MMA's largest N; 192 with NVFP4 weights, whose decoded tiles
+  // share tensor memory with the accumulators), never above the batch (an
+  // expert sees a token at most once). Smaller tiles leave shared memory for
+  // more pipeline stages; experts above the tile are split into near-equal tiles.
   const int64_t R = static_cast<int64_t>(T) * top_k;
   const int64_t mean = (R + E - 1) / std::max(E, 1);
   int64_t n = ((mean + mean / 4 + 15) / 16) * 16;
-  n = std::max<int64_t>(64, std::min<int64_t>(256, n));
+  n = std::max<int64_t>(64, std::min<int64_t>(w4 ? 192 : 256, n));
   const int tok = ((std::max(T, 1) + 15) / 16) * 16;
   p.n_max = static_cast<int>(std::min<int64_t>(n, tok));
   p.max_tiles = static_cast<int>(E + (R + p.n_max - 1) / p.n_max);

@@ -48,7 +48,7 @@ struct ExpertPlan {
   int wtiles2;      // 256-row weight tiles per expert in GEMM2 (ceil(d/256))
   int64_t max_items1, max_items2;
 };
-ExpertPlan plan_experts(int T, int d, int E, int top_k, int inter);
+ExpertPlan plan_experts(int T, int d, int E, int top_k, int inter, bool w4);
 
 struct ExpertBuffers {
   const uint16_t* x_perm;  // [R][d]
