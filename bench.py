@@ -249,7 +249,7 @@ def roofline_numbers(cfg, touched, peaks):
     bpp = weight_bytes_per_param(cfg)
     w_bytes_expert = 3 * d * I * bpp
     gemm1 = {"bytes": touched * 2 * I * d * bpp + R * d * 2 + R * I * 2, "flops": 2.0 * R * d * 2 * I}
-    gemm2 = {"bytes": touched * d * I * bpp + R * I * 2 + R * d * 4, "flops": 2.0 * R * I * d}
+    gemm2 = {"bytes": touched * d * I * bpp + R * I * 2 + R * d * 2, "flops": 2.0 * R * I * d}
     layer = {"bytes": touched * w_bytes_expert + d * E * 4 + cfg.T * d * 2 * 2,
              "flops": 2.0 * R * 3 * d * I + 2.0 * cfg.T * d * E}
     for x in (gemm1, gemm2, layer):

@@ -202,7 +202,7 @@ def moe_expert_ffn(dims: Dims, x_perm, offsets, weights: ExpertWeights, y_perm, 
     R = dims.T * dims.top_k
     _expect(x_perm, _BF16, (R, dims.d), "x_perm")
     _expect(offsets, (torch.int32,), (dims.E + 1,), "offsets")
-    _expect(y_perm, (torch.float32,), (R, dims.d), "y_perm")
+    _expect(y_perm, _BF16, (R, dims.d), "y_perm")
     _check_weights(dims, weights)
     _check("moe_expert_ffn", _lib().moe_expert_ffn(ctypes.byref(dims.c()), _ptr(x_perm), _ptr(offsets),
                                                    ctypes.byref(weights.c()), _ptr(y_perm), _ptr(ws), ws.numel(),
@@ -211,7 +211,7 @@ def moe_expert_ffn(dims: Dims, x_perm, offsets, weights: ExpertWeights, y_perm, 
 
 def moe_combine(dims: Dims, y_perm, inv_row, topk_w, out, ws=None, stream=None):
     R = dims.T * dims.top_k
-    _expect(y_perm, (torch.float32,), (R, dims.d), "y_perm")
+    _expect(y_perm, _BF16, (R, dims.d), "y_perm")
     _expect(inv_row, (torch.int32,), (R,), "inv_row")
     _expect(topk_w, (torch.float32,), (dims.T, dims.top_k), "topk_w")
     _expect(out, _BF16, (dims.T, dims.d), "out")

@@ -64,7 +64,7 @@ Layout make_layout(const moe_dims_t& d) {
   sz[R_ITEMS2] = sizeof(int4) * static_cast<size_t>(pl.max_items2);
   sz[R_XPERM] = sizeof(uint16_t) * R * d.d;
   sz[R_H] = sizeof(uint16_t) * R * d.inter;
-  sz[R_Y] = sizeof(float) * R * d.d;
+  sz[R_Y] = sizeof(uint16_t) * R * d.d;
   Layout L;
   size_t o = 0;
   for (int i = 0; i < R_NUM; ++i) {
@@ -153,7 +153,7 @@ moe_status_t do_permute(const moe_dims_t* d, const uint16_t* x, const int32_t* i
 }
 
 moe_status_t do_ffn(const moe_dims_t* d, const uint16_t* x_perm, const int32_t* offsets,
-                    const moe_expert_weights_t* w, float* y, void* ws, const Layout& L, cudaStream_t s,
+                    const moe_expert_weights_t* w, uint16_t* y, void* ws, const Layout& L, cudaStream_t s,
                     cudaEvent_t after_gemm1 = nullptr) {
   const ExpertPlan pl = plan_experts(d->T, d->d, d->E, d->top_k, d->inter, d->wfmt == MOE_W_NVFP4);
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
@@ -224,7 +224,7 @@ moe_status_t moe_permute(const moe_dims_t* dims, const moe_bf16_t* x, const int3
 }
 
 moe_status_t moe_expert_ffn(const moe_dims_t* dims, const moe_bf16_t* x_perm, const int32_t* offsets,
-                            const moe_expert_weights_t* weights, float* y_perm, void* ws, size_t ws_bytes,
+                            const moe_expert_weights_t* weights, moe_bf16_t* y_perm, void* ws, size_t ws_bytes,
                             void* stream) {
   moe_status_t st = check_dims(dims);
   if (st != MOE_OK) return st;
@@ -235,7 +235,7 @@ moe_status_t moe_expert_ffn(const moe_dims_t* dims, const moe_bf16_t* x_perm, co
   return do_ffn(dims, x_perm, offsets, weights, y_perm, ws, make_layout(*dims), static_cast<cudaStream_t>(stream));
 }
 
-moe_status_t moe_combine(const moe_dims_t* dims, const float* y_perm, const int32_t* inv_row, const float* topk_w,
+moe_status_t moe_combine(const moe_dims_t* dims, const moe_bf16_t* y_perm, const int32_t* inv_row, const float* topk_w,
                          moe_bf16_t* out, void* ws, size_t ws_bytes, void* stream) {
   moe_status_t st = check_dims(dims);
   if (st != MOE_OK) return st;
@@ -266,7 +266,7 @@ moe_status_t moe_forward(const moe_dims_t* dims, const moe_bf16_t* x, const floa
   int32_t* row_token = region<int32_t>(ws, L, R_ROWTOK);
   int32_t* inv_row = region<int32_t>(ws, L, R_INVROW);
   uint16_t* x_perm = region<uint16_t>(ws, L, R_XPERM);
-  float* y = region<float>(ws, L, R_Y);
+  uint16_t* y = region<uint16_t>(ws, L, R_Y);
   if (mark(0, s) != cudaSuccess) return MOE_ERR_CUDA;
   if ((st = do_route(dims, x, w_r, idx, w, ws, L, s)) != MOE_OK) return st;
   if (mark(1, s) != cudaSuccess) return MOE_ERR_CUDA;

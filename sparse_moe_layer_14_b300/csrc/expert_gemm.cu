@@ -5,7 +5,7 @@
 // stream": the SwiGLU product is computed in FP32).
 //
 //   GEMM1 + SwiGLU:  h[r][i] = bf16( silu(x_perm[r].Wg_e[i]) * (x_perm[r].Wu_e[i]) )
-//   GEMM2:           y[r][n] = h[r] . Wd_e[n]                                   (fp32)
+//   GEMM2:           y[r][n] = bf16( h[r] . Wd_e[n] )
 //
 // Every work item runs two 128-row weight tiles against the same token tile
 // (two MMAs per K step sharing the token operand): the gate and up tiles of
@@ -24,7 +24,7 @@
 //   warp 0      TMA producer: weight tile(s) + token rows per 64-wide K slice
 //   warp 1      TMEM allocator and single-thread tcgen05.mma issuer
 //   warps 2..9  epilogue, two warpgroups splitting the token columns:
-//               tcgen05.ld, SwiGLU in FP32 (GEMM1) or fp32 store (GEMM2)
+//               tcgen05.ld, SwiGLU in FP32 (GEMM1) or the bf16 output (GEMM2)
 //   warps 10..17 (NVFP4 weights only) converters: e2m1 codes times their e4m3
 //               block scale, which is exact in bf16, written to tensor memory,
 //               from where the MMA reads its A operand (so decoded weights
@@ -81,7 +81,7 @@ struct GemmArgs {
   uint32_t a_col;     // first TMEM column of the decoded weight slots (NVFP4)
   int conv_stages;
   uint16_t* h_out;    // GEMM1 output [R][Nw] bf16
-  float* y_out;       // GEMM2 output [R][Nw] fp32
+  uint16_t* y_out;    // GEMM2 output [R][Nw] bf16
   const float* ts0;   // per-expert scale applied to accumulator 0 (NVFP4), or null
   const float* ts1;
   const uint8_t* sf0;  // e4m3 block scales [E*Nw][K/16] of matrix 0 (NVFP4)
@@ -370,9 +370,9 @@ __global__ void __launch_bounds__(threads_for(kW4), 1)
           for (int j = 0; j < 16; ++j) {
             const int tok = c + j;
             if (tok < ntok) {
-              float* yrow = p.y_out + static_cast<size_t>(item.z + tok) * p.Nw;
-              if (valid0) yrow[col0] = __uint_as_float(g[j]) * s0;
-              if (valid1) yrow[col1] = __uint_as_float(u[j]) * s0;
+              uint16_t* yrow = p.y_out + static_cast<size_t>(item.z + tok) * p.Nw;
+              if (valid0) yrow[col0] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(g[j]) * s0));
+              if (valid1) yrow[col1] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(u[j]) * s0));
             }
           }
         }

@@ -54,7 +54,7 @@ struct ExpertBuffers {
   const uint16_t* x_perm;  // [R][d]
   const int32_t* offsets;  // [E+1]
   uint16_t* h;             // [R][inter]
-  float* y;                // [R][d]
+  uint16_t* y;             // [R][d] bf16
   int4* items1;            // GEMM1 work items {e, wtile, row0, ntok}
   int4* items2;
   int32_t* n_items;        // [2]
@@ -74,7 +74,7 @@ cudaError_t launch_expert_ffn(const ExpertPlan& plan, const ExpertBuffers& buf, 
                               cudaStream_t stream, int* cu_error, cudaEvent_t after_gemm1 = nullptr);
 
 // ---- combine (combine.cu) ----
-cudaError_t launch_combine(const float* y_perm, const int32_t* inv_row, const float* topk_w, uint16_t* out,
+cudaError_t launch_combine(const uint16_t* y_perm, const int32_t* inv_row, const float* topk_w, uint16_t* out,
                            int T, int d, int top_k, int32_t* status, cudaStream_t stream);
 
 }  // namespace beammoe
