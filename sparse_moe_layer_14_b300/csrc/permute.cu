@@ -10,7 +10,7 @@
 //   1. bitmap_kernel     set bit (e, t) for every slot            T*K threads
 //   2. column_scan_kernel per expert: popcount prefix over words   E blocks
 //   3. offsets_kernel    exclusive scan of the counts              1 block
-//   4. gather_kernel     rows, inverse rows, x -> x_perm copy      1 warp/token
+//   4. gather_kernel     rows, inverse rows, x -> x_perm copy      1 block/token, 1 warp/slot
 #include "common.cuh"
 #include "kernels.h"
 
@@ -87,32 +87,33 @@ __global__ void __launch_bounds__(1024) offsets_kernel(const int32_t* __restrict
   if (i == E - 1) offsets[E] = base + incl;
 }
 
-// One warp per token: rows of its K slots, then x[t] copied to each row.
-__global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict__ x,
-                                                     const int32_t* __restrict__ idx, int T, int d, int E, int K,
-                                                     int nw, const uint32_t* __restrict__ bitmap,
-                                                     const int32_t* __restrict__ word_prefix,
-                                                     const int32_t* __restrict__ offsets,
-                                                     int32_t* __restrict__ row_token, int32_t* __restrict__ inv_row,
-                                                     uint16_t* __restrict__ x_perm) {
-  const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (t >= T) return;
-  int my_row = -1;
-  if (lane < K) {
-    const int e = idx[static_cast<size_t>(t) * K + lane];
-    if (e >= 0 && e < E) {
-      const size_t wi = static_cast<size_t>(e) * nw + (t >> 5);
-      const uint32_t below = bitmap[wi] & ((1u << (t & 31)) - 1u);
-      my_row = offsets[e] + word_prefix[wi] + __popc(below);
-      row_token[my_row] = t;
-    }
-    inv_row[static_cast<size_t>(t) * K + lane] = my_row;
-  }
+// One block per token, one warp per slot (slots k, k + 8, ...): the slot's row,
+// then x[t] copied to it. A block per token keeps small batches spread over
+// the whole GPU.
+constexpr int kGatherWarps = 8;
+
+__global__ void __launch_bounds__(32 * kGatherWarps) gather_kernel(
+    const uint16_t* __restrict__ x, const int32_t* __restrict__ idx, int T, int d, int E, int K, int nw,
+    const uint32_t* __restrict__ bitmap, const int32_t* __restrict__ word_prefix,
+    const int32_t* __restrict__ offsets, int32_t* __restrict__ row_token, int32_t* __restrict__ inv_row,
+    uint16_t* __restrict__ x_perm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int t = blockIdx.x;
   const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * d);
   const int nvec = d / 8;
-  for (int k = 0; k < K; ++k) {
-    const int r = __shfl_sync(0xffffffffu, my_row, k);  // whole warp, outside the lane-strided loop
+  for (int k = warp; k < K; k += kGatherWarps) {
+    int my_row = -1;
+    if (lane == 0) {
+      const int e = idx[static_cast<size_t>(t) * K + k];
+      if (e >= 0 && e < E) {
+        const size_t wi = static_cast<size_t>(e) * nw + (t >> 5);
+        const uint32_t below = bitmap[wi] & ((1u << (t & 31)) - 1u);
+        my_row = offsets[e] + word_prefix[wi] + __popc(below);
+        row_token[my_row] = t;
+      }
+      inv_row[static_cast<size_t>(t) * K + k] = my_row;
+    }
+    const int r = __shfl_sync(0xffffffffu, my_row, 0);  // whole warp, outside the lane-strided loop
     if (r < 0) continue;
     uint4* dst = reinterpret_cast<uint4*>(x_perm + static_cast<size_t>(r) * d);
     for (int c = lane; c < nvec; c += 32) dst[c] = src[c];
@@ -135,8 +136,8 @@ cudaError_t launch_permute(const uint16_t* x, const int32_t* topk_idx, int T, in
                                                                                 status);
   column_scan_kernel<<<E, 256, 0, stream>>>(bitmap, nw, word_prefix, counts);
   offsets_kernel<<<1, 1024, 0, stream>>>(counts, E, offsets);
-  gather_kernel<<<(T + 7) / 8, 256, 0, stream>>>(x, topk_idx, T, d, E, top_k, nw, bitmap, word_prefix, offsets,
-                                                  row_token, inv_row, x_perm);
+  gather_kernel<<<T, 32 * kGatherWarps, 0, stream>>>(x, topk_idx, T, d, E, top_k, nw, bitmap, word_prefix, offsets,
+                                                      row_token, inv_row, x_perm);
   return cudaGetLastError();
 }
 

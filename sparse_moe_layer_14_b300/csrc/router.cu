@@ -8,7 +8,8 @@
 //  router_logits_kernel  FP32 SIMT GEMM, logits = x . W_r, with a split over
 //                        the hidden dimension so the whole GPU streams W_r.
 //  split_reduce_kernel   sums the split partials of each logit in a fixed
-//                        order, in place into split 0.
+//                        order (four interleaved chains, then pairwise), in
+//                        place into split 0.
 //  router_select_kernel  one warp per token: sigmoid, group top-2 sums, top
 //                        groups, top experts, normalisation.
 // Large batches (prefill):
@@ -110,13 +111,22 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const uint16_t* __re
   }
 }
 
-// part[0][t][e] = sum over s of part[s][t][e], s ascending.
+// part[0][t][e] = sum over s of part[s][t][e] in a fixed order: four chains
+// over s = 0,4,8,.. / 1,5,.. / 2,6,.. / 3,7,.. (independent loads in flight),
+// then (c0 + c1) + (c2 + c3).
 __global__ void __launch_bounds__(256) split_reduce_kernel(float* __restrict__ part, int splits, int64_t n) {
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= n) return;
-  float l = part[i];
-  for (int sp = 1; sp < splits; ++sp) l += part[static_cast<size_t>(sp) * n + i];
-  part[i] = l;
+  float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
+  int sp = 0;
+  for (; sp + 4 <= splits; sp += 4) {
+    c0 += part[static_cast<size_t>(sp) * n + i];
+    c1 += part[static_cast<size_t>(sp + 1) * n + i];
+    c2 += part[static_cast<size_t>(sp + 2) * n + i];
+    c3 += part[static_cast<size_t>(sp + 3) * n + i];
+  }
+  for (; sp < splits; ++sp) c0 += part[static_cast<size_t>(sp) * n + i];
+  part[i] = (c0 + c1) + (c2 + c3);
 }
 
 // (value, index) order of the selection: larger value first, ties to the
@@ -159,7 +169,33 @@ __device__ float2 warp_select(const float (&s)[kMaxPerLane], int lane, int t, in
 
   // group score: sum of the two largest scores of the group (lane g keeps group g's)
   float my_gs = kMasked;
-  for (int g = 0; g < G; ++g) {
+  if (gsz == 32) {
+    // element i of every lane is group i: all groups reduce side by side
+    float m1[kMaxPerLane], m2[kMaxPerLane];
+#pragma unroll
+    for (int i = 0; i < kMaxPerLane; ++i) {
+      m1[i] = s[i];
+      m2[i] = kMasked;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+#pragma unroll
+      for (int i = 0; i < kMaxPerLane; ++i) {
+        const float o1 = __shfl_xor_sync(0xffffffffu, m1[i], off);
+        const float o2 = __shfl_xor_sync(0xffffffffu, m2[i], off);
+        if (o1 > m1[i]) {
+          m2[i] = fmaxf(m1[i], o2);
+          m1[i] = o1;
+        } else {
+          m2[i] = fmaxf(m2[i], o1);
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kMaxPerLane; ++i)
+      if (lane == i && i < G) my_gs = m1[i] + m2[i];
+  }
+  for (int g = 0; g < G && gsz != 32; ++g) {
     float m1 = kMasked, m2 = kMasked;
 #pragma unroll
     for (int i = 0; i < kMaxPerLane; ++i) {
