@@ -344,19 +344,23 @@ __global__ void __launch_bounds__(threads_for(kW4), 1)
       const int ntok = item.w;
       const float s0 = p.ts0 ? p.ts0[item.x] : 1.0f;
       const float s1 = p.ts1 ? p.ts1[item.x] : s0;
-      for (int c = eg * 16; c < ntok; c += 32) {
-        uint32_t g[16], u[16];
-        tmem_ld_32x32b_x16(tb + c, g);
-        tmem_ld_32x32b_x16(tb + p.n_max + c, u);
-        tmem_ld_wait();
+      // 16-token chunks eg*16, eg*16 + 32, ...: the TMEM loads of the next chunk
+      // are in flight while this one is computed and stored, and the
+      // accumulator is handed back to the MMA as soon as the last chunk's loads
+      // have landed (its math and stores overlap the next item's MMAs).
+      auto load_chunk = [&](int c, uint32_t (&gg)[16], uint32_t (&uu)[16]) {
+        tmem_ld_32x32b_x16(tb + c, gg);
+        tmem_ld_32x32b_x16(tb + p.n_max + c, uu);
+      };
+      auto store_chunk = [&](int c, const uint32_t (&gg)[16], const uint32_t (&uu)[16]) {
         if (kGLU) {
           if (valid0) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const int tok = c + j;
               if (tok < ntok) {
-                const float gv = __uint_as_float(g[j]) * s0;
-                const float uv = __uint_as_float(u[j]) * s1;
+                const float gv = __uint_as_float(gg[j]) * s0;
+                const float uv = __uint_as_float(uu[j]) * s1;
                 // silu(g) = g / (1 + e^-g); h is rounded to bf16 right after, so the
                 // fast exponential and division (relative error ~1e-7) do not show
                 const float silu = __fdividef(gv, 1.0f + __expf(-gv));
@@ -371,14 +375,40 @@ __global__ void __launch_bounds__(threads_for(kW4), 1)
             const int tok = c + j;
             if (tok < ntok) {
               uint16_t* yrow = p.y_out + static_cast<size_t>(item.z + tok) * p.Nw;
-              if (valid0) yrow[col0] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(g[j]) * s0));
-              if (valid1) yrow[col1] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(u[j]) * s0));
+              if (valid0) yrow[col0] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(gg[j]) * s0));
+              if (valid1) yrow[col1] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(uu[j]) * s0));
             }
           }
         }
+      };
+      uint32_t ga[16], ua[16], gb[16], ub[16];
+      bool released = false;
+      auto next_or_release = [&](int cn, uint32_t (&gg)[16], uint32_t (&uu)[16]) {
+        if (cn < ntok) {
+          load_chunk(cn, gg, uu);
+        } else {
+          tc_fence_before();
+          mbar_arrive(&acce_bar[acc]);
+          released = true;
+        }
+      };
+      int c = eg * 16;
+      if (c < ntok) load_chunk(c, ga, ua);
+      while (c < ntok) {
+        tmem_ld_wait();
+        next_or_release(c + 32, gb, ub);
+        store_chunk(c, ga, ua);
+        c += 32;
+        if (c >= ntok) break;
+        tmem_ld_wait();
+        next_or_release(c + 32, ga, ua);
+        store_chunk(c, gb, ub);
+        c += 32;
       }
-      tc_fence_before();
-      mbar_arrive(&acce_bar[acc]);
+      if (!released) {
+        tc_fence_before();
+        mbar_arrive(&acce_bar[acc]);
+      }
       if (++acc == p.acc_bufs) {
         acc = 0;
         acc_phase ^= 1u;
