@@ -44,7 +44,7 @@ Layout make_layout(const moe_dims_t& d) {
   const int Tc = d.T > 0 ? d.T : 1;
   const int splits = std::max(router_splits(Tc, d.d, d.E, kMaxSmsForLayout),
                               router_uses_tensor_cores(d.T, d.E, d.d)
-                                  ? std::max(4, router_tc_splits(Tc, d.d, kMaxSmsForLayout))  // 4: fp32 recompute
+                                  ? std::max(kRouterFlagSplits, router_tc_splits(Tc, d.d, kMaxSmsForLayout))
                                   : 1);
   const ExpertPlan pl = plan_experts(d.T, d.d, d.E, d.top_k, d.inter, d.wfmt == MOE_W_NVFP4);
   const int64_t nw = bitmap_words(d.T);

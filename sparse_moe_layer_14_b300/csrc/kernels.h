@@ -25,6 +25,7 @@ cudaError_t launch_router_select(float* partial, int splits, int T, int E, int n
 // FFMA recompute of all logits of the flagged tokens.
 // `scratch` holds router_tc_scratch_bytes(T, d, E) bytes.
 constexpr int kRouterTcMinTokens = 1024;
+constexpr int kRouterFlagSplits = 8;  // hidden-dimension parts of the fp32 recompute: [8][flagged][E] in `part`
 int router_epad(int E);
 bool router_uses_tensor_cores(int T, int E, int d);
 size_t router_tc_scratch_bytes(int T, int d, int E);

@@ -568,17 +568,18 @@ __global__ void __launch_bounds__(256) router_select_flag_kernel(const float* __
 }
 
 // Flagged tokens: every logit as an fp32 FFMA dot product. Work items are
-// (group of up to kFlagTokens flagged tokens, quarter of the hidden
+// (group of up to kFlagTokens flagged tokens, eighth of the hidden
 // dimension), taken round-robin by the CTAs; an item streams its rows of W_r
 // through shared memory in chunks of kFlagRows rows by bulk-async copies (a
-// 4-deep ring), thread (q, e) of the 1024 adds rows q, q+4, ... of each chunk
-// for expert e, and the four sums are added in a fixed order into the
-// item's partial logits part[quarter][i][e].
+// 6-deep ring: the copy latency, not the FMAs, bounds an item), thread (q, e)
+// of the 1024 adds rows q, q+4, ... of each chunk for expert e, and the four
+// sums are added in a fixed order into the item's partial logits
+// part[eighth][i][e].
 constexpr int kFlagTokens = 4;
 constexpr int kFlagThreads = 1024;
 constexpr int kFlagRows = 32;    // W_r rows per chunk (32 x E fp32)
-constexpr int kFlagRing = 4;
-constexpr int kFlagSplits = 4;   // hidden-dimension quarters per token group
+constexpr int kFlagRing = 6;
+constexpr int kFlagSplits = kRouterFlagSplits;  // hidden-dimension parts per token group
 
 __global__ void __launch_bounds__(kFlagThreads) router_flagged_logits_kernel(
     const uint16_t* __restrict__ x, const float* __restrict__ wr, int d, int E,
@@ -681,7 +682,7 @@ __global__ void __launch_bounds__(kFlagThreads) router_flagged_logits_kernel(
   __syncthreads();
 }
 
-// One warp per flagged token: the quarters' partial logits summed in order,
+// One warp per flagged token: the parts' partial logits summed in order,
 // sigmoid and the full selection.
 __global__ void __launch_bounds__(256) router_flagged_select_kernel(const float* __restrict__ part, int E, int G,
                                                                    int Gk, int K, float scale,
@@ -737,9 +738,14 @@ int encode_router_map(CUtensorMap* map, const void* base, uint64_t inner, uint64
 
 int router_epad(int E) { return ((E + 15) / 16) * 16; }
 
-// The fp32 recompute works on hidden-dimension quarters of whole 32-row chunks.
+// The fp32 recompute works on hidden-dimension eighths of whole 32-row chunks,
+// and its x slice, W_r ring and partial sums must fit in shared memory.
 bool router_uses_tensor_cores(int T, int E, int d) {
-  return T >= kRouterTcMinTokens && router_epad(E) <= 256 && d % (kFlagSplits * kFlagRows) == 0;
+  const size_t smem = sizeof(float4) * static_cast<size_t>(d / kFlagSplits) +
+                      sizeof(float) * static_cast<size_t>(kFlagRing) * kFlagRows * E +
+                      sizeof(float) * 4 * kFlagTokens * 256 + 1024;
+  return T >= kRouterTcMinTokens && router_epad(E) <= 256 && d % (kFlagSplits * kFlagRows) == 0 &&
+         smem <= 232448;
 }
 
 // Split of the hidden dimension over CTAs: the largest that keeps all CTAs in
