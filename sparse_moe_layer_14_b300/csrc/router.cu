@@ -568,26 +568,29 @@ __global__ void __launch_bounds__(256) router_select_flag_kernel(const float* __
 }
 
 // Flagged tokens: every logit as an fp32 FFMA dot product. Work items are
-// (group of up to kFlagTokens flagged tokens, eighth of the hidden
-// dimension), taken round-robin by the CTAs; an item streams its rows of W_r
+// (group of up to kFlagTokens flagged tokens, one of `splits` parts of the
+// hidden dimension: 8, or 4 where d is not a multiple of 8 x 32), taken
+// round-robin by the CTAs; an item streams its rows of W_r
 // through shared memory in chunks of kFlagRows rows by bulk-async copies (a
 // 6-deep ring: the copy latency, not the FMAs, bounds an item), thread (q, e)
 // of the 1024 adds rows q, q+4, ... of each chunk for expert e, and the four
 // sums are added in a fixed order into the item's partial logits
-// part[eighth][i][e].
+// part[part][i][e].
 constexpr int kFlagTokens = 4;
 constexpr int kFlagThreads = 1024;
 constexpr int kFlagRows = 32;    // W_r rows per chunk (32 x E fp32)
 constexpr int kFlagRing = 6;
-constexpr int kFlagSplits = kRouterFlagSplits;  // hidden-dimension parts per token group
+constexpr int kFlagSplits = kRouterFlagSplits;  // hidden-dimension parts per token group (at most)
+
+int flag_splits(int d) { return d % (kFlagSplits * kFlagRows) == 0 ? kFlagSplits : kFlagSplits / 2; }
 
 __global__ void __launch_bounds__(kFlagThreads) router_flagged_logits_kernel(
     const uint16_t* __restrict__ x, const float* __restrict__ wr, int d, int E,
     const int32_t* __restrict__ flagged, const int32_t* __restrict__ flagged_count, float* __restrict__ part_out,
-    int32_t* status) {
+    int splits, int32_t* status) {
   extern __shared__ __align__(16) uint8_t fsm[];
-  float4* xs4 = reinterpret_cast<float4*>(fsm);                      // [d / kFlagSplits]: x of <= 4 tokens at k
-  float* wring = reinterpret_cast<float*>(fsm + sizeof(float4) * (d / kFlagSplits));  // [ring][rows][E]
+  float4* xs4 = reinterpret_cast<float4*>(fsm);                      // [d / splits]: x of <= 4 tokens at k
+  float* wring = reinterpret_cast<float*>(fsm + sizeof(float4) * (d / splits));  // [ring][rows][E]
   __shared__ float part[4][kFlagTokens][256];
   __shared__ __align__(8) uint64_t bar[kFlagRing];
   __shared__ int abort_flag;
@@ -597,7 +600,7 @@ __global__ void __launch_bounds__(kFlagThreads) router_flagged_logits_kernel(
   const int groups = (n + kFlagTokens - 1) / kFlagTokens;
   const int e = threadIdx.x & 255, q = threadIdx.x >> 8;
   const uint32_t chunk_bytes = static_cast<uint32_t>(kFlagRows) * E * sizeof(float);
-  const int kq = d / kFlagSplits;         // hidden elements of one item
+  const int kq = d / splits;              // hidden elements of one item
   const int nchunks = kq / kFlagRows;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kFlagRing; ++i) mbar_init(&bar[i], 1);
@@ -606,8 +609,8 @@ __global__ void __launch_bounds__(kFlagThreads) router_flagged_logits_kernel(
   }
   __syncthreads();
   uint32_t issued = 0, consumed = 0;  // chunk copies issued (thread 0) / waited
-  for (int item = blockIdx.x; item < groups * kFlagSplits; item += gridDim.x) {
-    const int i0 = (item / kFlagSplits) * kFlagTokens, z = item % kFlagSplits;
+  for (int item = blockIdx.x; item < groups * splits; item += gridDim.x) {
+    const int i0 = (item / splits) * kFlagTokens, z = item % splits;
     const int nt = min(kFlagTokens, n - i0);
     const int k0 = z * kq;
     const float* wsrc = wr + static_cast<size_t>(k0) * E;
@@ -684,7 +687,8 @@ __global__ void __launch_bounds__(kFlagThreads) router_flagged_logits_kernel(
 
 // One warp per flagged token: the parts' partial logits summed in order,
 // sigmoid and the full selection.
-__global__ void __launch_bounds__(256) router_flagged_select_kernel(const float* __restrict__ part, int E, int G,
+__global__ void __launch_bounds__(256) router_flagged_select_kernel(const float* __restrict__ part, int splits, int E,
+                                                                   int G,
                                                                    int Gk, int K, float scale,
                                                                    const int32_t* __restrict__ flagged,
                                                                    const int32_t* __restrict__ flagged_count,
@@ -700,7 +704,7 @@ __global__ void __launch_bounds__(256) router_flagged_select_kernel(const float*
       sv[j] = -1.0f;
       if (e < E) {
         float l = 0.f;
-        for (int z = 0; z < kFlagSplits; ++z) l += part[(static_cast<size_t>(z) * n + i) * E + e];
+        for (int z = 0; z < splits; ++z) l += part[(static_cast<size_t>(z) * n + i) * E + e];
         sv[j] = 1.0f / (1.0f + expf(-l));
       }
     }
@@ -738,13 +742,13 @@ int encode_router_map(CUtensorMap* map, const void* base, uint64_t inner, uint64
 
 int router_epad(int E) { return ((E + 15) / 16) * 16; }
 
-// The fp32 recompute works on hidden-dimension eighths of whole 32-row chunks,
+// The fp32 recompute works on hidden-dimension parts of whole 32-row chunks,
 // and its x slice, W_r ring and partial sums must fit in shared memory.
 bool router_uses_tensor_cores(int T, int E, int d) {
-  const size_t smem = sizeof(float4) * static_cast<size_t>(d / kFlagSplits) +
+  const size_t smem = sizeof(float4) * static_cast<size_t>(d / flag_splits(d)) +
                       sizeof(float) * static_cast<size_t>(kFlagRing) * kFlagRows * E +
                       sizeof(float) * 4 * kFlagTokens * 256 + 1024;
-  return T >= kRouterTcMinTokens && router_epad(E) <= 256 && d % (kFlagSplits * kFlagRows) == 0 &&
+  return T >= kRouterTcMinTokens && router_epad(E) <= 256 && d % (flag_splits(d) * kFlagRows) == 0 &&
          smem <= 232448;
 }
 
@@ -802,15 +806,17 @@ cudaError_t launch_router_tc(const uint16_t* x, const float* w_r, void* scratch,
                                                              routed_scale, topk_idx, topk_w, flagged, flagged_count,
                                                              status);
   // the tensor-core partials were consumed by the selection: reuse `part` for the recompute
-  const size_t xs_bytes = sizeof(float4) * static_cast<size_t>(d / kFlagSplits) +
+  const int fsplits = flag_splits(d);
+  const size_t xs_bytes = sizeof(float4) * static_cast<size_t>(d / fsplits) +
                           sizeof(float) * static_cast<size_t>(kFlagRing) * kFlagRows * E;
   err = cudaFuncSetAttribute(router_flagged_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(xs_bytes));
   if (err != cudaSuccess) return err;
   router_flagged_logits_kernel<<<num_sms, kFlagThreads, xs_bytes, stream>>>(x, w_r, d, E, flagged, flagged_count,
-                                                                            part, status);
-  router_flagged_select_kernel<<<num_sms, 256, 0, stream>>>(part, E, n_groups, topk_groups, top_k, routed_scale,
-                                                            flagged, flagged_count, topk_idx, topk_w, status);
+                                                                            part, fsplits, status);
+  router_flagged_select_kernel<<<num_sms, 256, 0, stream>>>(part, fsplits, E, n_groups, topk_groups, top_k,
+                                                            routed_scale, flagged, flagged_count, topk_idx, topk_w,
+                                                            status);
   return cudaGetLastError();
 }
 

@@ -251,6 +251,28 @@ def test_forward_nvfp4_full_parity(T, seed):
     check_output(host_bits(out), ref, TOL_NVFP4)
 
 
+# E = 40 (not a multiple of 16: padded to 48 on the tensor-core router), groups of 8 (the generic
+# group-score path), top-6 of 2 kept groups, intermediate 192 (a ragged 64-row second weight tile)
+ODD = W.MoEConfig("odd", T=1200, d=256, E=40, n_groups=5, topk_groups=2, top_k=6, inter=192)
+
+
+def test_forward_odd_shape_tensor_core_router():
+    """T = 1200 >= 1024 takes the tensor-core router (hidden split in 8 for the fp32 recompute)."""
+    cfg = ODD
+    x_h, wr_h = W.gen_x(cfg, 3), W.gen_wr(cfg, 3)
+    gi_route, gw_route = route_only(cfg, x_h, wr_h)
+    orc = O.route(cfg, x_h, wr_h)
+    compare_routing(cfg, gi_route, gw_route, orc)
+    dw = DeviceWeights(cfg, 3)
+    out, idx, counts, _ = run_forward(cfg, dev(x_h), dev(wr_h), dw.dev)
+    gi = idx.cpu().numpy()
+    excluded, ref_idx, ref_w = compare_routing_idx_only(cfg, gi, orc)
+    assert np.array_equal(counts.cpu().numpy(), np.bincount(gi.ravel(), minlength=cfg.E))
+    rows = np.arange(0, cfg.T, 7)
+    ref = O.forward_tokens(cfg, x_h, ref_idx, ref_w, rows, dw.host)
+    check_output(host_bits(out)[rows], ref, TOL_BF16)
+
+
 def test_forward_deterministic():
     cfg = TINY.with_tokens(200)
     inp = W.make_host_inputs(cfg, 9)
