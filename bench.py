@@ -89,12 +89,21 @@ PROFILE_CASES = {
                                  inter=2560, wfmt="nvfp4"),
 }
 
-DEFAULT_STEPS = {"decode": 300, "prefill": 200, "skewed": 40, "nvfp4": 200, "profile_decode": 20,
+# Dense SwiGLU MLP of the first decoder layers. The pages give no intermediate size for them;
+# 20480 = 8 x 2560 gives the dense FFN the per-token work of the 8 routed experts.
+DENSE_CASES = {
+    "dense_prefill": W.MoEConfig("dense_prefill", T=4096, d=5120, E=1, n_groups=1, topk_groups=1, top_k=1,
+                                 inter=20480),
+}
+
+DEFAULT_STEPS = {"dense_prefill": 100, "decode": 300, "prefill": 200, "skewed": 40, "nvfp4": 200, "profile_decode": 20,
                  "profile_prefill": 20, "profile_dense": 20, "profile_nvfp4": 20}
 
 
 def workload_cfg(name):
-    return W.CONFIGS[name] if name in W.CONFIGS else PROFILE_CASES[name]
+    if name in W.CONFIGS:
+        return W.CONFIGS[name]
+    return PROFILE_CASES[name] if name in PROFILE_CASES else DENSE_CASES[name]
 
 
 def describe(cfg):
@@ -423,6 +432,154 @@ def run_ours(args, rank, world, local_rank):
 
 # ----------------------------------------------------------------------------- oracle legs
 
+def run_dense(args, rank, world, local_rank):
+    """The dense SwiGLU MLP (moe_dense_mlp) on one batch, timed like the MoE forward."""
+    import torch
+    import sparse_moe_layer_14_b300 as bm
+
+    torch.cuda.set_device(local_rank)
+    cfg = workload_cfg(args.workload)
+    peaks = load_peaks()
+    want_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+    dims = bm.Dims.from_config(cfg)
+    weights, host_w = make_device_weights(cfg, args.seed, torch, keep_host=want_cpu)
+    x_h = W.gen_x(cfg, args.seed + 1000 * rank)
+    x = torch.from_numpy(x_h).view(torch.int16).view(torch.bfloat16).cuda()
+    out = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device="cuda")
+    ws = bm.allocate_dense_workspace(dims)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        bm.moe_dense_mlp(dims, x, weights, out, ws)
+    torch.cuda.synchronize()
+    K = args.steps
+    ev_sets = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    for evs in ev_sets:
+        for ev in evs:
+            ev.record(stream)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local_rank) if rank == 0 else None
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    start.record(stream)
+    for i in range(K):
+        bm.moe_set_stage_events(ev_sets[i])
+        bm.moe_dense_mlp(dims, x, weights, out, ws)
+    end.record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    bm.moe_set_stage_events(None)
+    if bm.moe_get_device_status(ws) != bm.MOE_DEV_OK:
+        raise RuntimeError("device status set during the timed region")
+    elapsed_ms = max_over_ranks(start.elapsed_time(end), world, "cuda")
+    g1_ms = float(np.mean([e[0].elapsed_time(e[3]) for e in ev_sets]))
+    g2_ms = float(np.mean([e[3].elapsed_time(e[4]) for e in ev_sets]))
+    clk = clocks.summary(wall0, wall1) if clocks else None
+    if clocks:
+        clocks.stop()
+
+    # end to end: pinned-host copies on a second stream, double-buffered (as for the MoE block)
+    x_pin = torch.from_numpy(x_h).view(torch.int16).pin_memory()
+    out_pin = [torch.empty((cfg.T, cfg.d), dtype=torch.int16).pin_memory() for _ in range(2)]
+    x_dev = [torch.empty_like(x) for _ in range(2)]
+    out_dev = [torch.empty_like(out) for _ in range(2)]
+    copy_stream = torch.cuda.Stream()
+
+    def e2e_run(n):
+        h2d = [torch.cuda.Event() for _ in range(2)]
+        fwd = [torch.cuda.Event() for _ in range(2)]
+        d2h = [torch.cuda.Event() for _ in range(2)]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(copy_stream):
+            t0.record(copy_stream)
+            x_dev[0].view(torch.int16).copy_(x_pin, non_blocking=True)
+            h2d[0].record(copy_stream)
+        for i in range(n):
+            b = i % 2
+            stream.wait_event(h2d[b])
+            if i >= 2:
+                stream.wait_event(d2h[b])
+            bm.moe_dense_mlp(dims, x_dev[b], weights, out_dev[b], ws)
+            fwd[b].record(stream)
+            with torch.cuda.stream(copy_stream):
+                if i + 1 < n:
+                    if i >= 1:
+                        copy_stream.wait_event(fwd[1 - b])
+                    x_dev[1 - b].view(torch.int16).copy_(x_pin, non_blocking=True)
+                    h2d[1 - b].record(copy_stream)
+                copy_stream.wait_event(fwd[b])
+                out_pin[b].copy_(out_dev[b].view(torch.int16), non_blocking=True)
+                d2h[b].record(copy_stream)
+        with torch.cuda.stream(copy_stream):
+            t1.record(copy_stream)
+        return t0, t1
+
+    e2e_run(max(2, args.warmup))
+    torch.cuda.synchronize()
+    e0, e1 = e2e_run(K)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, "cuda")
+    if rank != 0:
+        return None
+
+    d, I, T = cfg.d, cfg.inter, cfg.T
+    flops1, flops2 = 2.0 * T * d * 2 * I, 2.0 * T * I * d
+    bytes1 = 2 * I * d * 2 + T * d * 2 + T * I * 2
+    bytes2 = d * I * 2 + T * I * 2 + T * d * 2
+    ms_per_step = elapsed_ms / K
+
+    def roof(fl, by, ms):
+        t_f, t_b = fl / (peaks["bf16_tflops"] * 1e12), by / (peaks["hbm_gbs"] * 1e9)
+        bound = "tensor" if t_f >= t_b else "hbm"
+        ach = fl / (ms / 1e3) / 1e12 if bound == "tensor" else by / (ms / 1e3) / 1e9
+        pk = peaks["bf16_tflops"] if bound == "tensor" else peaks["hbm_gbs"]
+        return bound, ach, pk, max(t_f, t_b) * 1e3
+
+    b1, a1, p1, r1 = roof(flops1, bytes1, g1_ms)
+    _, _, _, r2 = roof(flops2, bytes2, g2_ms)
+    line = {
+        "metric": "dense SwiGLU MLP tokens/s (first decoder layers)", "value": round(world * T / (ms_per_step / 1e3), 1),
+        "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) activations, N(0,1/fan_in) weights)", "impl": "ours",
+        "config": {"workload": f"{cfg.name}: dense SwiGLU MLP, T={T} tokens, d={d}, intermediate {I} (a reading: "
+                               f"8 x 2560, the routed experts' per-token width), bf16 weights",
+                   "T": T, "d": d, "inter": I, "parallelism": f"replicas x{world}",
+                   "l2": f"no flush: {3 * d * I * 2 / 1e6:.0f} MB of weights and {T * I * 2 / 1e6:.0f} MB of h "
+                         f"per step exceed the 126 MB L2"},
+        "roofline": {"kernel": "expert_gemm_kernel<GLU> (GEMM1 + SwiGLU, one expert)", "bound": b1,
+                     "achieved": round(a1, 1), "peak": p1, "unit": "TFLOP/s" if b1 == "tensor" else "GB/s",
+                     "frac": round(a1 / p1, 4), "peak_source": f"{peaks['source']} "
+                     f"({'bf16_tflops' if b1 == 'tensor' else 'hbm_gbs'})", "traffic": None,
+                     "traffic_source": "no capture of this case", "algorithmic_bytes": bytes1,
+                     "algorithmic_flops": flops1, "avg_launch_ms": round(g1_ms, 4)},
+        "layer_roofline": {"roofline_ms": round(r1 + r2, 4), "frac": round((r1 + r2) / ms_per_step, 4),
+                           "algorithmic_flops": flops1 + flops2},
+        "stages_ms": {"offsets+schedule+gemm1": round(g1_ms, 4), "gemm2": round(g2_ms, 4)},
+        "gemm2_roofline": {"frac": round(r2 / g2_ms, 4)},
+        "e2e": {"value": round(world * T / (e2e_ms / K / 1e3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": T * d * 2, "d2h_bytes_per_step": T * d * 2, "ms_per_step": round(e2e_ms / K, 4),
+                "pipelining": "copies on a second stream, double-buffered: step i+1's input and step i-1's "
+                              "output move while step i computes"},
+        "gpu_launches": 4 * K,
+        "clocks": clk,
+    }
+    if want_cpu:
+        import oracle as O
+        n = 16
+        t0 = time.time()
+        O.ffn_rows(np.zeros(n, np.int32), x_h[:n], host_w, d, I, cfg.wfmt)
+        dt = time.time() - t0
+        line["cpu_baseline"] = {"value": round(n / dt, 3), "unit": "tokens/s", "cores": O.num_threads(),
+                                "kind": "oracle", "sample": f"first {n} of the {T} tokens (fp64 SwiGLU MLP rows)",
+                                "seconds": round(dt, 2)}
+    return line
+
+
 def cpu_sample_tokens(cfg):
     return min(cfg.T, 64)
 
@@ -480,7 +637,8 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="decode", choices=sorted(list(W.CONFIGS) + list(PROFILE_CASES)))
+    ap.add_argument("--workload", default="decode",
+                    choices=sorted(list(W.CONFIGS) + list(PROFILE_CASES) + list(DENSE_CASES)))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -503,7 +661,7 @@ def main():
         import torch
         torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group("nccl")
-    line = run_ours(args, rank, world, local_rank)
+    line = (run_dense if args.workload in DENSE_CASES else run_ours)(args, rank, world, local_rank)
     if line is not None:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -184,6 +184,24 @@ moe_status_t moe_permute_noalloc(const moe_dims_t* dims, const moe_bf16_t* x, co
                                  int32_t* counts, int32_t* offsets, int32_t* row_token, int32_t* inv_row,
                                  moe_bf16_t* x_perm, int32_t* device_status, void* stream);
 
+/* Dense SwiGLU MLP of the first decoder layers (release article, section
+ * "Architecture": the first 3 of the 52 layers use a dense SwiGLU MLP instead
+ * of the Mixture-of-Experts block). For every token t:
+ *   h = bf16( silu(x[t] . Wg) * (x[t] . Wu) )   (FP32 math, as for the experts)
+ *   out[t] = bf16( h . Wd )                       (FP32 accumulate)
+ * on the expert GEMM kernels with a single expert and no routing. Uses
+ * dims->T, d, inter and wfmt; E, n_groups, topk_groups, top_k and
+ * routed_scale are ignored. `w` holds one MLP in the expert layouts with E = 1
+ * (gate, up [inter][d], down [d][inter]; NVFP4 as for the experts). x [T][d]
+ * and out [T][d] bf16, 16-byte aligned; d a multiple of 64 up to 16384, inter
+ * a multiple of 64 up to 65536 (NVFP4: both multiples of 256). The workspace
+ * (moe_dense_workspace_bytes bytes, 256-byte aligned, header zeroed by
+ * moe_workspace_init) holds the work items and h [T][inter]. Host-side errors
+ * return before any launch; device codes latch in the workspace header. */
+size_t moe_dense_workspace_bytes(const moe_dims_t* dims);
+moe_status_t moe_dense_mlp(const moe_dims_t* dims, const moe_bf16_t* x, const moe_expert_weights_t* w,
+                           moe_bf16_t* out, void* ws, size_t ws_bytes, void* stream);
+
 /* Read (and with clear != 0, reset) the device code latched in the workspace
  * header. Synchronises `stream`. *code receives a moe_device_code_t. */
 moe_status_t moe_get_device_status(void* ws, void* stream, int32_t clear, int32_t* code);
@@ -199,7 +217,9 @@ void moe_set_wait_bound(int64_t spins);
  * before its first launch and events[i] after stage i on its stream:
  * 1 router, 2 permutation, 3 work-item schedule + expert GEMM1 (SwiGLU),
  * 4 expert GEMM2, 5 combine. cudaEventElapsedTime between consecutive events
- * then gives each stage's device time. NULL (or n < 6) turns it off. The
+ * then gives each stage's device time (moe_dense_mlp records events[0] before
+ * its first launch, events[3] after GEMM1 and events[4] after GEMM2). NULL (or
+ * n < 6) turns it off. The
  * setting is process-wide; do not change it while moe_forward calls run on
  * other host threads. */
 moe_status_t moe_set_stage_events(void* const* events, int32_t n);

@@ -219,6 +219,35 @@ def moe_combine(dims: Dims, y_perm, inv_row, topk_w, out, ws=None, stream=None):
                                              _ptr(out), _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
 
 
+def _dense(dims: Dims) -> Dims:
+    return Dims(dims.T, dims.d, 1, 1, 1, 1, dims.inter, 1.0, dims.wfmt)
+
+
+def moe_dense_workspace_bytes(dims: Dims) -> int:
+    n = _lib().moe_dense_workspace_bytes(ctypes.byref(dims.c()))
+    if n == 0:
+        raise MoEError("moe_dense_workspace_bytes", N.MOE_ERR_INVALID_ARG)
+    return int(n)
+
+
+def allocate_dense_workspace(dims: Dims, device="cuda") -> torch.Tensor:
+    """A zero-headed workspace of moe_dense_workspace_bytes(dims) bytes."""
+    ws = torch.empty(moe_dense_workspace_bytes(dims), dtype=torch.uint8, device=device)
+    if ws.data_ptr() % 256:
+        raise RuntimeError("workspace is not 256-byte aligned")
+    moe_workspace_init(ws)
+    return ws
+
+
+def moe_dense_mlp(dims: Dims, x, weights: ExpertWeights, out, ws, stream=None):
+    """Dense SwiGLU MLP (one expert's layout, E = 1): out = bf16(bf16(silu(x Wg) * (x Wu)) Wd)."""
+    _expect(x, _BF16, (dims.T, dims.d), "x")
+    _expect(out, _BF16, (dims.T, dims.d), "out")
+    _check_weights(_dense(dims), weights)
+    _check("moe_dense_mlp", _lib().moe_dense_mlp(ctypes.byref(dims.c()), _ptr(x), ctypes.byref(weights.c()), _ptr(out),
+                                                 _ptr(ws), ws.numel(), _stream(stream)))
+
+
 def moe_forward(dims: Dims, x, w_r, weights: ExpertWeights, out, ws, topk_idx=None, counts=None, stream=None):
     _expect(x, _BF16, (dims.T, dims.d), "x")
     _expect(w_r, (torch.float32,), (dims.d, dims.E), "w_r")

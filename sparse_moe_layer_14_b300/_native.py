@@ -20,7 +20,7 @@ MOE_W_BF16, MOE_W_NVFP4 = 0, 1
 
 EXPORTS = ["moe_workspace_bytes", "moe_workspace_init", "moe_route", "moe_permute", "moe_expert_ffn",
            "moe_combine", "moe_forward", "moe_get_device_status", "moe_set_wait_bound", "moe_set_stage_events",
-           "moe_version", "moe_permute_noalloc"]
+           "moe_version", "moe_permute_noalloc", "moe_dense_workspace_bytes", "moe_dense_mlp"]
 
 
 class MoeDims(ctypes.Structure):
@@ -70,6 +70,10 @@ def load(path: str = LIB_PATH):
     L.moe_permute_noalloc.restype = st
     L.moe_set_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int32]
     L.moe_set_stage_events.restype = st
+    L.moe_dense_workspace_bytes.argtypes = [pd]
+    L.moe_dense_workspace_bytes.restype = sz
+    L.moe_dense_mlp.argtypes = [pd, vp, pw, vp, vp, sz, vp]
+    L.moe_dense_mlp.restype = st
     L.moe_version.argtypes = []
     L.moe_version.restype = ctypes.c_char_p
     if path == LIB_PATH:

@@ -152,6 +152,21 @@ moe_status_t do_permute(const moe_dims_t* d, const uint16_t* x, const int32_t* i
   return cuda_status(e);
 }
 
+ExpertWeightsDev weights_dev(int wfmt, const moe_expert_weights_t* w) {
+  ExpertWeightsDev wd;
+  wd.wfmt = wfmt;
+  wd.gate = w->gate;
+  wd.up = w->up;
+  wd.down = w->down;
+  wd.gate_sf = w->gate_sf;
+  wd.up_sf = w->up_sf;
+  wd.down_sf = w->down_sf;
+  wd.gate_ts = w->gate_ts;
+  wd.up_ts = w->up_ts;
+  wd.down_ts = w->down_ts;
+  return wd;
+}
+
 moe_status_t do_ffn(const moe_dims_t* d, const uint16_t* x_perm, const int32_t* offsets,
                     const moe_expert_weights_t* w, uint16_t* y, void* ws, const Layout& L, cudaStream_t s,
                     cudaEvent_t after_gemm1 = nullptr) {
@@ -167,17 +182,7 @@ moe_status_t do_ffn(const moe_dims_t* d, const uint16_t* x_perm, const int32_t* 
   b.n_items = hdr->n_items;
   b.status = &hdr->status;
   b.timeout_where = &hdr->timeout_where;
-  ExpertWeightsDev wd;
-  wd.wfmt = d->wfmt;
-  wd.gate = w->gate;
-  wd.up = w->up;
-  wd.down = w->down;
-  wd.gate_sf = w->gate_sf;
-  wd.up_sf = w->up_sf;
-  wd.down_sf = w->down_sf;
-  wd.gate_ts = w->gate_ts;
-  wd.up_ts = w->up_ts;
-  wd.down_ts = w->down_ts;
+  const ExpertWeightsDev wd = weights_dev(d->wfmt, w);
   int cu_err = 0;
   const cudaError_t e = launch_expert_ffn(pl, b, wd, d->T, d->d, d->E, d->top_k, d->inter, num_sms(), g_wait_spins,
                                           s, &cu_err, after_gemm1);
@@ -281,6 +286,52 @@ moe_status_t moe_forward(const moe_dims_t* dims, const moe_bf16_t* x, const floa
   return mark(5, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+// ---------------------------------------------------------------- dense SwiGLU MLP
+
+// One expert, every token: the expert GEMMs with offsets {0, T}.
+moe_dims_t dense_dims(const moe_dims_t& d) {
+  moe_dims_t e = d;
+  e.E = 1;
+  e.n_groups = 1;
+  e.topk_groups = 1;
+  e.top_k = 1;
+  e.routed_scale = 1.0f;
+  return e;
+}
+
+moe_status_t check_dense_dims(const moe_dims_t* d) {
+  if (!d) return MOE_ERR_INVALID_ARG;
+  if (d->T < 0 || d->d <= 0 || d->inter <= 0) return MOE_ERR_INVALID_ARG;
+  if (d->wfmt != MOE_W_BF16 && d->wfmt != MOE_W_NVFP4) return MOE_ERR_INVALID_ARG;
+  if (d->T > 4194304 || d->d % 64 || d->inter % 64 || d->d > 16384 || d->inter > 65536) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+struct DenseLayout {
+  size_t offs, items1, items2, h, total;
+};
+
+DenseLayout make_dense_layout(const moe_dims_t& d) {
+  const ExpertPlan pl = plan_experts(d.T, d.d, 1, 1, d.inter, d.wfmt == MOE_W_NVFP4);
+  DenseLayout L;
+  size_t o = align_up(sizeof(WsHeader));
+  L.offs = o;
+  o = align_up(o + 2 * sizeof(int32_t));
+  L.items1 = o;
+  o = align_up(o + sizeof(int4) * static_cast<size_t>(pl.max_items1));
+  L.items2 = o;
+  o = align_up(o + sizeof(int4) * static_cast<size_t>(pl.max_items2));
+  L.h = o;
+  o = align_up(o + sizeof(uint16_t) * static_cast<size_t>(d.T) * d.inter);
+  L.total = o;
+  return L;
+}
+
+__global__ void dense_offsets_kernel(int32_t* offsets, int T) {
+  offsets[0] = 0;
+  offsets[1] = T;
+}
+
 moe_status_t moe_get_device_status(void* ws, void* stream, int32_t clear, int32_t* code) {
   if (!ws || !code) return MOE_ERR_INVALID_ARG;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -309,6 +360,48 @@ moe_status_t moe_set_stage_events(void* const* events, int32_t n) {
 }
 
 void moe_set_wait_bound(int64_t spins) { g_wait_spins = spins > 0 ? spins : kDefaultSpins; }
+
+size_t moe_dense_workspace_bytes(const moe_dims_t* dims) {
+  if (check_dense_dims(dims) != MOE_OK) return 0;
+  return make_dense_layout(*dims).total;
+}
+
+moe_status_t moe_dense_mlp(const moe_dims_t* dims, const moe_bf16_t* x, const moe_expert_weights_t* w,
+                           moe_bf16_t* out, void* ws, size_t ws_bytes, void* stream) {
+  moe_status_t st = check_dense_dims(dims);
+  if (st != MOE_OK) return st;
+  if (dims->T == 0) return MOE_OK;
+  if (!aligned16(x) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+  const moe_dims_t d1 = dense_dims(*dims);
+  if ((st = check_weights(&d1, w)) != MOE_OK) return st;
+  const DenseLayout L = make_dense_layout(*dims);
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0 || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  int32_t* offs = reinterpret_cast<int32_t*>(base + L.offs);
+  if (mark(0, s) != cudaSuccess) return MOE_ERR_CUDA;
+  dense_offsets_kernel<<<1, 1, 0, s>>>(offs, dims->T);
+  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+  ExpertBuffers b;
+  b.x_perm = x;  // one expert: the permuted rows are the tokens in order
+  b.offsets = offs;
+  b.h = reinterpret_cast<uint16_t*>(base + L.h);
+  b.y = out;
+  b.items1 = reinterpret_cast<int4*>(base + L.items1);
+  b.items2 = reinterpret_cast<int4*>(base + L.items2);
+  b.n_items = hdr->n_items;
+  b.status = &hdr->status;
+  b.timeout_where = &hdr->timeout_where;
+  const ExpertWeightsDev wd = weights_dev(d1.wfmt, w);
+  const ExpertPlan pl = plan_experts(d1.T, d1.d, 1, 1, d1.inter, d1.wfmt == MOE_W_NVFP4);
+  int cu_error = 0;
+  const cudaError_t e = launch_expert_ffn(pl, b, wd, d1.T, d1.d, 1, 1, d1.inter, num_sms(), g_wait_spins, s,
+                                          &cu_error, g_stage_events_on ? g_stage_events[3] : nullptr);
+  if (e == cudaErrorNotSupported) return MOE_ERR_UNSUPPORTED;
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  return mark(4, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
 
 const char* moe_version(void) { return "beammoe 0.1 sm_103a (tcgen05 bf16 grouped SwiGLU)"; }
 
