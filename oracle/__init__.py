@@ -44,6 +44,8 @@ def load(path: str | None = None):
     L.oracle_router_scores.argtypes = [i32, i32, i32, vp, vp, vp, vp]
     L.oracle_select.argtypes = [i32, i32, i32, i32, i32, dbl, vp, vp, vp, vp, vp, vp]
     L.oracle_select.restype = i32
+    L.oracle_select_biased.argtypes = [i32, i32, i32, i32, i32, dbl, vp, vp, vp, vp, vp, vp, vp]
+    L.oracle_select_biased.restype = i32
     L.oracle_permute.argtypes = [i32, i32, i32, vp, vp, vp, vp, vp]
     L.oracle_ffn_rows.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     L.oracle_combine.argtypes = [i32, i32, i32, vp, vp, vp, vp]
@@ -85,9 +87,10 @@ def router_scores(x, w_r, L=None):
     return logits, scores
 
 
-def select(scores, n_groups, topk_groups, top_k, routed_scale=2.5, L=None):
+def select(scores, n_groups, topk_groups, top_k, routed_scale=2.5, L=None, bias=None):
     """Group-limited top-k: returns dict(idx [T,K] i32, w [T,K] f64, gscores [T,G] f32,
-    margin_group [T], margin_expert [T])."""
+    margin_group [T], margin_expert [T]). `bias` [E] f32: per-expert selection bias (it
+    steers the choice; the weights use the unbiased scores)."""
     L = L or lib()
     scores = np.ascontiguousarray(scores, np.float32)
     T, E = scores.shape
@@ -96,18 +99,24 @@ def select(scores, n_groups, topk_groups, top_k, routed_scale=2.5, L=None):
     gs = np.empty((T, n_groups), np.float32)
     mg = np.empty(T, np.float64)
     me = np.empty(T, np.float64)
-    rc = L.oracle_select(T, E, n_groups, topk_groups, top_k, routed_scale, _p(scores), _p(idx), _p(w),
-                         _p(gs), _p(mg), _p(me))
+    if bias is None:
+        rc = L.oracle_select(T, E, n_groups, topk_groups, top_k, routed_scale, _p(scores), _p(idx), _p(w),
+                             _p(gs), _p(mg), _p(me))
+    else:
+        bias = np.ascontiguousarray(bias, np.float32)
+        assert bias.shape == (E,)
+        rc = L.oracle_select_biased(T, E, n_groups, topk_groups, top_k, routed_scale, _p(scores), _p(bias),
+                                    _p(idx), _p(w), _p(gs), _p(mg), _p(me))
     if rc < 0:
         raise ValueError("invalid selection dims")
     return {"idx": idx, "w": w, "gscores": gs, "margin_group": mg, "margin_expert": me,
             "zero_sum_tokens": rc}
 
 
-def route(cfg, x, w_r, L=None):
-    """Router of the block: scores then group-limited selection."""
+def route(cfg, x, w_r, L=None, bias=None):
+    """Router of the block: scores then group-limited selection (optional selection bias [E])."""
     logits, scores = router_scores(x, w_r, L)
-    out = select(scores, cfg.n_groups, cfg.topk_groups, cfg.top_k, cfg.routed_scale, L)
+    out = select(scores, cfg.n_groups, cfg.topk_groups, cfg.top_k, cfg.routed_scale, L, bias=bias)
     out["logits"], out["scores"] = logits, scores
     return out
 

@@ -129,24 +129,29 @@ void oracle_router_scores(int T, int d, int E, const uint16_t* x, const float* w
 }
 
 /* Group-limited top-k selection for one token.
- *   group score  = sum of the two largest scores in the group (FP32 add)
+ *   selection score = s, or s + bias[e] (FP32 add) with a per-expert bias:
+ *                  the balancing bias of DeepSeek-V3's router, which the
+ *                  article's router follows; it steers the choice only
+ *   group score  = sum of the two largest selection scores in the group (FP32 add)
  *   kept groups  = the topk_groups best group scores
- *   chosen       = the top_k best scores among experts of kept groups
- *   weight       = routed_scale * s / (sum of chosen s)
- * Ties: lower index first. Slots are in descending score order.
+ *   chosen       = the top_k best selection scores among experts of kept groups
+ *   weight       = routed_scale * s / (sum of chosen s)   (unbiased scores)
+ * Ties: lower index first. Slots are in descending selection-score order.
  * margin_group  = (worst kept group score) - (best dropped group score)
- * margin_expert = (worst chosen score) - (best unchosen candidate score)
+ * margin_expert = (worst chosen selection score) - (best unchosen candidate's)
  * (+INFINITY when nothing was dropped). Returns 0, or 1 if the score sum is 0. */
-static int select_one(int E, int G, int Gk, int K, double scale, const float* s, int32_t* idx,
-                      double* w, float* gs, double* mg, double* me) {
+static int select_one(int E, int G, int Gk, int K, double scale, const float* s, const float* bias,
+                      int32_t* idx, double* w, float* gs, double* mg, double* me) {
   const int gsz = E / G;
+  float sel[1024];
+  for (int e = 0; e < E; ++e) sel[e] = bias ? s[e] + bias[e] : s[e];
   for (int g = 0; g < G; ++g) {
     int b1 = -1, b2 = -1;
     for (int e = g * gsz; e < (g + 1) * gsz; ++e) {
-      if (b1 < 0 || s[e] > s[b1]) { b2 = b1; b1 = e; }
-      else if (b2 < 0 || s[e] > s[b2]) { b2 = e; }
+      if (b1 < 0 || sel[e] > sel[b1]) { b2 = b1; b1 = e; }
+      else if (b2 < 0 || sel[e] > sel[b2]) { b2 = e; }
     }
-    gs[g] = (gsz >= 2) ? (s[b1] + s[b2]) : s[b1];
+    gs[g] = (gsz >= 2) ? (sel[b1] + sel[b2]) : sel[b1];
   }
   char kept[64] = {0};
   int last_kept = -1;
@@ -167,15 +172,15 @@ static int select_one(int E, int G, int Gk, int K, double scale, const float* s,
   for (int k = 0; k < K; ++k) {
     int best = -1;
     for (int e = 0; e < E; ++e)
-      if (kept[e / gsz] && !taken[e] && (best < 0 || s[e] > s[best])) best = e;
+      if (kept[e / gsz] && !taken[e] && (best < 0 || sel[e] > sel[best])) best = e;
     taken[best] = 1;
     idx[k] = best;
     sum += (double)s[best];
   }
   int best_left = -1;
   for (int e = 0; e < E; ++e)
-    if (kept[e / gsz] && !taken[e] && (best_left < 0 || s[e] > s[best_left])) best_left = e;
-  *me = (best_left < 0) ? INFINITY : (double)s[idx[K - 1]] - (double)s[best_left];
+    if (kept[e / gsz] && !taken[e] && (best_left < 0 || sel[e] > sel[best_left])) best_left = e;
+  *me = (best_left < 0) ? INFINITY : (double)sel[idx[K - 1]] - (double)sel[best_left];
   if (sum == 0.0) {
     for (int k = 0; k < K; ++k) w[k] = 0.0;
     return 1;
@@ -184,12 +189,13 @@ static int select_one(int E, int G, int Gk, int K, double scale, const float* s,
   return 0;
 }
 
-/* Selection for T tokens from their FP32 scores. Output arrays are [T][K]
- * (idx, w), [T][G] (gscores, nullable), [T] (margins, nullable). Returns the
- * number of tokens whose chosen scores summed to zero. */
-int oracle_select(int T, int E, int G, int Gk, int K, double scale, const float* scores,
-                  int32_t* idx, double* w, float* gscores, double* margin_group,
-                  double* margin_expert) {
+/* Selection for T tokens from their FP32 scores and an optional per-expert
+ * selection bias [E] (NULL: none). Output arrays are [T][K] (idx, w), [T][G]
+ * (gscores, nullable), [T] (margins, nullable). Returns the number of tokens
+ * whose chosen scores summed to zero. */
+int oracle_select_biased(int T, int E, int G, int Gk, int K, double scale, const float* scores,
+                         const float* bias, int32_t* idx, double* w, float* gscores, double* margin_group,
+                         double* margin_expert) {
   if (E <= 0 || G <= 0 || E % G || G > 64 || E > 1024 || Gk < 1 || Gk > G || K < 1 ||
       K > Gk * (E / G))
     return -1;
@@ -198,7 +204,7 @@ int oracle_select(int T, int E, int G, int Gk, int K, double scale, const float*
   for (int t = 0; t < T; ++t) {
     float gs[64];
     double mg, me;
-    bad += select_one(E, G, Gk, K, scale, scores + (int64_t)t * E, idx + (int64_t)t * K,
+    bad += select_one(E, G, Gk, K, scale, scores + (int64_t)t * E, bias, idx + (int64_t)t * K,
                       w + (int64_t)t * K, gs, &mg, &me);
     if (gscores)
       for (int g = 0; g < G; ++g) gscores[(int64_t)t * G + g] = gs[g];
@@ -206,6 +212,13 @@ int oracle_select(int T, int E, int G, int Gk, int K, double scale, const float*
     if (margin_expert) margin_expert[t] = me;
   }
   return bad;
+}
+
+int oracle_select(int T, int E, int G, int Gk, int K, double scale, const float* scores,
+                  int32_t* idx, double* w, float* gscores, double* margin_group,
+                  double* margin_expert) {
+  return oracle_select_biased(T, E, G, Gk, K, scale, scores, NULL, idx, w, gscores, margin_group,
+                              margin_expert);
 }
 
 /* ---------------- permutation (grouping of token slots by expert) ---------------- */

@@ -108,6 +108,38 @@ def check_select_bruteforce(L):
             assert np.allclose(r["w"][t], ws, rtol=1e-15, atol=0)
 
 
+def check_select_bias(L):
+    """Selection bias (the balancing bias of DeepSeek-V3's router, which the article's router
+    follows): the choice is the brute-force group-limited top-k of s + b (float32 add), slots in
+    descending s + b; the weights are 2.5 * s / sum(s) with the unbiased scores; a zero bias
+    changes nothing; a bias far above the score range puts that expert in every choice."""
+    for (E, G, Gk, K, seed) in [(16, 4, 2, 4, 11), (12, 3, 2, 3, 12), (16, 8, 3, 4, 13)]:
+        T = 40
+        s = W.uniform_f64(seed, W.TID_AUX, 0, T * E).astype(np.float32).reshape(T, E)
+        b = (0.3 * (W.uniform_f64(seed, W.TID_AUX + 1, 0, E) - 0.5)).astype(np.float32)
+        r = O.select(s, G, Gk, K, 2.5, L, bias=b)
+        for t in range(T):
+            sel = (s[t] + b).astype(np.float32)
+            chosen, gs = _brute_select(sel, G, Gk, K)
+            assert set(r["idx"][t].tolist()) == chosen, (E, G, Gk, K, t)
+            assert np.array_equal(r["gscores"][t], gs)
+            assert np.all(np.diff(sel[r["idx"][t]].astype(np.float64)) <= 0)
+            sv = s[t][r["idx"][t]].astype(np.float64)
+            assert np.allclose(r["w"][t], 2.5 * sv / sv.sum(), rtol=1e-15, atol=0)
+        r0 = O.select(s, G, Gk, K, 2.5, L, bias=np.zeros(E, np.float32))
+        rn = O.select(s, G, Gk, K, 2.5, L)
+        assert np.array_equal(r0["idx"], rn["idx"]) and np.array_equal(r0["w"], rn["w"])
+    E, G, Gk, K = 16, 4, 2, 4
+    s = W.uniform_f64(14, W.TID_AUX, 0, 30 * E).astype(np.float32).reshape(30, E)
+    b = np.zeros(E, np.float32)
+    b[5] = 4.0
+    r = O.select(s, G, Gk, K, 2.5, L, bias=b)
+    assert np.all(r["idx"][:, 0] == 5)
+    s64 = s.astype(np.float64)
+    assert np.allclose(r["w"][:, 0], 2.5 * s64[:, 5] / np.take_along_axis(s64, r["idx"].astype(np.int64), 1).sum(1),
+                       rtol=1e-12, atol=0)
+
+
 def check_select_invariants(L):
     """Chosen experts are distinct, lie in kept groups; weights are >= 0 and sum to 2.5;
     margins are non-negative."""
@@ -271,7 +303,8 @@ def check_nvfp4_ffn(L):
         assert np.max(np.abs(y[r] - yr)) <= 1e-3 * np.sqrt((yr ** 2).mean())
 
 
-CHECKS = [check_uniform_scores, check_router_logits, check_select_bruteforce, check_select_invariants,
+CHECKS = [check_uniform_scores, check_router_logits, check_select_bruteforce, check_select_bias,
+          check_select_invariants,
           check_single_expert_dense, check_identical_experts, check_permute, check_combine,
           check_forward_matches_stages, check_nvfp4_decode, check_nvfp4_ffn]
 
@@ -306,14 +339,17 @@ def test_printed_block_facts():
 
 MUTANTS = {
     "sigmoid_sign": ("1.0 / (1.0 + exp(-(double)l))", "1.0 / (1.0 + exp((double)l))"),
-    "group_top1_only": ("(s[b1] + s[b2])", "(s[b1] + s[b1])"),
-    "group_max_not_sum": ("(s[b1] + s[b2])", "(s[b1])"),
+    "group_top1_only": ("(sel[b1] + sel[b2])", "(sel[b1] + sel[b1])"),
+    "group_max_not_sum": ("(sel[b1] + sel[b2])", "(sel[b1])"),
     "silu_is_sigmoid": ("(double)gf / (1.0 + exp(-(double)gf))", "1.0 / (1.0 + exp(-(double)gf))"),
     "gate_up_swapped": ("g += xbuf[j] * wmat_at(gate", "g += xbuf[j] * wmat_at(up"),
     "no_normalisation": ("w[k] = scale * (double)s[idx[k]] / sum;", "w[k] = scale * (double)s[idx[k]];"),
     "no_scale": ("w[k] = scale * (double)s[idx[k]] / sum;", "w[k] = (double)s[idx[k]] / sum;"),
-    "tie_to_higher_index": ("if (kept[e / gsz] && !taken[e] && (best < 0 || s[e] > s[best])) best = e;",
-                            "if (kept[e / gsz] && !taken[e] && (best < 0 || s[e] >= s[best])) best = e;"),
+    "tie_to_higher_index": ("if (kept[e / gsz] && !taken[e] && (best < 0 || sel[e] > sel[best])) best = e;",
+                            "if (kept[e / gsz] && !taken[e] && (best < 0 || sel[e] >= sel[best])) best = e;"),
+    "bias_ignored": ("sel[e] = bias ? s[e] + bias[e] : s[e];", "sel[e] = s[e];"),
+    "bias_in_weights": ("w[k] = scale * (double)s[idx[k]] / sum;", "w[k] = scale * (double)sel[idx[k]] / sum;"),
+    "bias_in_weight_sum": ("sum += (double)s[best];", "sum += (double)sel[best];"),
     "no_group_limit": ("if (kept[e / gsz] && !taken[e] && (best < 0", "if (!taken[e] && (best < 0"),
     "h_not_rounded": ("hbuf[i] = bf16_value(hb);", "hbuf[i] = (double)(silu * uf);"),
     "down_transposed": ("acc += hbuf[i] * wmat_at(down, e, n, i);", "acc += hbuf[i] * wmat_at(down, e, i % d, n % I);"),
