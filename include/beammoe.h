@@ -184,6 +184,20 @@ moe_status_t moe_permute_noalloc(const moe_dims_t* dims, const moe_bf16_t* x, co
                                  int32_t* counts, int32_t* offsets, int32_t* row_token, int32_t* inv_row,
                                  moe_bf16_t* x_perm, int32_t* device_status, void* stream);
 
+/* moe_route and moe_forward with a per-expert selection bias (nullable
+ * sel_bias [E] fp32, 4-byte aligned): the auxiliary-loss-free balancing bias
+ * of DeepSeek-V3's router, which the article's router follows (release
+ * article, section "Mixture of Experts"; the pre-training notes mention
+ * expert-bias updates). Group scores (top-2 sums) and the expert choice use
+ * s + sel_bias (FP32 add); the combine weights use the unbiased s:
+ * w = routed_scale * s / sum of the chosen s. Slot order is descending
+ * s + sel_bias. sel_bias = NULL is moe_route / moe_forward. */
+moe_status_t moe_route_ex(const moe_dims_t* dims, const moe_bf16_t* x, const float* w_r, const float* sel_bias,
+                          int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes, void* stream);
+moe_status_t moe_forward_ex(const moe_dims_t* dims, const moe_bf16_t* x, const float* w_r, const float* sel_bias,
+                            const moe_expert_weights_t* weights, moe_bf16_t* out, int32_t* topk_idx,
+                            int32_t* counts, void* ws, size_t ws_bytes, void* stream);
+
 /* Dense SwiGLU MLP of the first decoder layers (release article, section
  * "Architecture": the first 3 of the 52 layers use a dense SwiGLU MLP instead
  * of the Mixture-of-Experts block). For every token t:

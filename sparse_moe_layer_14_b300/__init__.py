@@ -141,13 +141,15 @@ def allocate_workspace(dims: Dims, device="cuda") -> torch.Tensor:
     return ws
 
 
-def moe_route(dims: Dims, x, w_r, topk_idx, topk_w, ws, stream=None):
+def moe_route(dims: Dims, x, w_r, topk_idx, topk_w, ws, stream=None, sel_bias=None):
+    """sel_bias: optional [E] fp32 per-expert selection bias (choice only; weights unbiased)."""
     _expect(x, _BF16, (dims.T, dims.d), "x")
     _expect(w_r, (torch.float32,), (dims.d, dims.E), "w_r")
     _expect(topk_idx, (torch.int32,), (dims.T, dims.top_k), "topk_idx")
     _expect(topk_w, (torch.float32,), (dims.T, dims.top_k), "topk_w")
-    _check("moe_route", _lib().moe_route(ctypes.byref(dims.c()), _ptr(x), _ptr(w_r), _ptr(topk_idx), _ptr(topk_w),
-                                         _ptr(ws), ws.numel(), _stream(stream)))
+    _expect(sel_bias, (torch.float32,), (dims.E,), "sel_bias")
+    _check("moe_route", _lib().moe_route_ex(ctypes.byref(dims.c()), _ptr(x), _ptr(w_r), _ptr(sel_bias), _ptr(topk_idx),
+                                            _ptr(topk_w), _ptr(ws), ws.numel(), _stream(stream)))
 
 
 def moe_permute(dims: Dims, x, topk_idx, counts, offsets, row_token, inv_row, x_perm, ws, stream=None):
@@ -248,16 +250,24 @@ def moe_dense_mlp(dims: Dims, x, weights: ExpertWeights, out, ws, stream=None):
                                                  _ptr(ws), ws.numel(), _stream(stream)))
 
 
-def moe_forward(dims: Dims, x, w_r, weights: ExpertWeights, out, ws, topk_idx=None, counts=None, stream=None):
+def moe_forward(dims: Dims, x, w_r, weights: ExpertWeights, out, ws, topk_idx=None, counts=None, stream=None,
+                sel_bias=None):
+    """sel_bias: optional [E] fp32 per-expert selection bias (choice only; weights unbiased)."""
     _expect(x, _BF16, (dims.T, dims.d), "x")
     _expect(w_r, (torch.float32,), (dims.d, dims.E), "w_r")
     _expect(out, _BF16, (dims.T, dims.d), "out")
     _expect(topk_idx, (torch.int32,), (dims.T, dims.top_k), "topk_idx")
     _expect(counts, (torch.int32,), (dims.E,), "counts")
+    _expect(sel_bias, (torch.float32,), (dims.E,), "sel_bias")
     _check_weights(dims, weights)
-    _check("moe_forward", _lib().moe_forward(ctypes.byref(dims.c()), _ptr(x), _ptr(w_r), ctypes.byref(weights.c()),
-                                             _ptr(out), _ptr(topk_idx), _ptr(counts), _ptr(ws), ws.numel(),
-                                             _stream(stream)))
+    if sel_bias is None:
+        rc = _lib().moe_forward(ctypes.byref(dims.c()), _ptr(x), _ptr(w_r), ctypes.byref(weights.c()), _ptr(out),
+                                _ptr(topk_idx), _ptr(counts), _ptr(ws), ws.numel(), _stream(stream))
+    else:
+        rc = _lib().moe_forward_ex(ctypes.byref(dims.c()), _ptr(x), _ptr(w_r), _ptr(sel_bias),
+                                   ctypes.byref(weights.c()), _ptr(out), _ptr(topk_idx), _ptr(counts), _ptr(ws),
+                                   ws.numel(), _stream(stream))
+    _check("moe_forward", rc)
 
 
 def moe_get_device_status(ws, clear: bool = False, stream=None) -> int:

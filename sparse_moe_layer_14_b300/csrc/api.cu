@@ -127,19 +127,19 @@ moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE
 
 int32_t* status_word(void* ws) { return ws ? &reinterpret_cast<WsHeader*>(ws)->status : nullptr; }
 
-moe_status_t do_route(const moe_dims_t* d, const uint16_t* x, const float* w_r, int32_t* idx, float* w,
-                      void* ws, const Layout& L, cudaStream_t s) {
+moe_status_t do_route(const moe_dims_t* d, const uint16_t* x, const float* w_r, const float* sel_bias, int32_t* idx,
+                      float* w, void* ws, const Layout& L, cudaStream_t s) {
   if (router_uses_tensor_cores(d->T, d->E, d->d))
     return cuda_status(launch_router_tc(x, w_r, region<uint8_t>(ws, L, R_WSPLIT), region<float>(ws, L, R_PART),
                                         &reinterpret_cast<WsHeader*>(ws)->router_flagged, d->T, d->d, d->E, d->n_groups,
-                                        d->topk_groups, d->top_k, d->routed_scale, idx, w, status_word(ws),
-                                        num_sms(), s));
+                                        d->topk_groups, d->top_k, d->routed_scale, sel_bias, idx, w,
+                                        status_word(ws), num_sms(), s));
   const int splits = router_splits(d->T, d->d, d->E, num_sms());
   float* part = region<float>(ws, L, R_PART);
   cudaError_t e = launch_router_logits(x, w_r, part, d->T, d->d, d->E, splits, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  e = launch_router_select(part, splits, d->T, d->E, d->n_groups, d->topk_groups, d->top_k, d->routed_scale, idx, w,
-                           status_word(ws), s);
+  e = launch_router_select(part, splits, d->T, d->E, d->n_groups, d->topk_groups, d->top_k, d->routed_scale,
+                           sel_bias, idx, w, status_word(ws), s);
   return cuda_status(e);
 }
 
@@ -205,14 +205,21 @@ moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, void* stream) {
   return cuda_status(cudaMemsetAsync(ws, 0, sizeof(WsHeader), static_cast<cudaStream_t>(stream)));
 }
 
-moe_status_t moe_route(const moe_dims_t* dims, const moe_bf16_t* x, const float* w_r, int32_t* topk_idx,
-                       float* topk_w, void* ws, size_t ws_bytes, void* stream) {
+moe_status_t moe_route_ex(const moe_dims_t* dims, const moe_bf16_t* x, const float* w_r, const float* sel_bias,
+                          int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes, void* stream) {
   moe_status_t st = check_dims(dims);
   if (st != MOE_OK) return st;
   if (dims->T == 0) return MOE_OK;
   if (!aligned16(x) || !aligned16(w_r) || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
+  if (sel_bias && (reinterpret_cast<uintptr_t>(sel_bias) & 3u)) return MOE_ERR_INVALID_ARG;
   if ((st = check_ws(dims, ws, ws_bytes)) != MOE_OK) return st;
-  return do_route(dims, x, w_r, topk_idx, topk_w, ws, make_layout(*dims), static_cast<cudaStream_t>(stream));
+  return do_route(dims, x, w_r, sel_bias, topk_idx, topk_w, ws, make_layout(*dims),
+                  static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_route(const moe_dims_t* dims, const moe_bf16_t* x, const float* w_r, int32_t* topk_idx,
+                       float* topk_w, void* ws, size_t ws_bytes, void* stream) {
+  return moe_route_ex(dims, x, w_r, nullptr, topk_idx, topk_w, ws, ws_bytes, stream);
 }
 
 moe_status_t moe_permute(const moe_dims_t* dims, const moe_bf16_t* x, const int32_t* topk_idx, int32_t* counts,
@@ -255,11 +262,18 @@ moe_status_t moe_combine(const moe_dims_t* dims, const moe_bf16_t* y_perm, const
 moe_status_t moe_forward(const moe_dims_t* dims, const moe_bf16_t* x, const float* w_r,
                          const moe_expert_weights_t* weights, moe_bf16_t* out, int32_t* topk_idx, int32_t* counts,
                          void* ws, size_t ws_bytes, void* stream) {
+  return moe_forward_ex(dims, x, w_r, nullptr, weights, out, topk_idx, counts, ws, ws_bytes, stream);
+}
+
+moe_status_t moe_forward_ex(const moe_dims_t* dims, const moe_bf16_t* x, const float* w_r, const float* sel_bias,
+                            const moe_expert_weights_t* weights, moe_bf16_t* out, int32_t* topk_idx, int32_t* counts,
+                            void* ws, size_t ws_bytes, void* stream) {
   moe_status_t st = check_dims(dims);
   if (st != MOE_OK) return st;
   if (dims->T == 0) return MOE_OK;
   if (!aligned16(x) || !aligned16(w_r) || !out || (reinterpret_cast<uintptr_t>(out) & 7u))
     return MOE_ERR_INVALID_ARG;
+  if (sel_bias && (reinterpret_cast<uintptr_t>(sel_bias) & 3u)) return MOE_ERR_INVALID_ARG;
   if ((st = check_weights(dims, weights)) != MOE_OK) return st;
   if ((st = check_ws(dims, ws, ws_bytes)) != MOE_OK) return st;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -273,7 +287,7 @@ moe_status_t moe_forward(const moe_dims_t* dims, const moe_bf16_t* x, const floa
   uint16_t* x_perm = region<uint16_t>(ws, L, R_XPERM);
   uint16_t* y = region<uint16_t>(ws, L, R_Y);
   if (mark(0, s) != cudaSuccess) return MOE_ERR_CUDA;
-  if ((st = do_route(dims, x, w_r, idx, w, ws, L, s)) != MOE_OK) return st;
+  if ((st = do_route(dims, x, w_r, sel_bias, idx, w, ws, L, s)) != MOE_OK) return st;
   if (mark(1, s) != cudaSuccess) return MOE_ERR_CUDA;
   if ((st = do_permute(dims, x, idx, cnt, offs, row_token, inv_row, x_perm, ws, L, s)) != MOE_OK) return st;
   if (mark(2, s) != cudaSuccess) return MOE_ERR_CUDA;

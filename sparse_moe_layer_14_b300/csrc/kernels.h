@@ -14,10 +14,11 @@ int router_splits(int T, int d, int E, int num_sms);
 cudaError_t launch_router_logits(const uint16_t* x, const float* w_r, float* partial, int T, int d, int E,
                                  int splits, cudaStream_t stream);
 // sums the split partials (in place into split 0), then sigmoid scores,
-// group-limited top-k and normalised weights.
+// group-limited top-k (on scores + sel_bias when sel_bias [E] is given) and
+// normalised weights (unbiased scores).
 cudaError_t launch_router_select(float* partial, int splits, int T, int E, int n_groups, int topk_groups,
-                                 int top_k, float routed_scale, int32_t* topk_idx, float* topk_w,
-                                 int32_t* status, cudaStream_t stream);
+                                 int top_k, float routed_scale, const float* sel_bias, int32_t* topk_idx,
+                                 float* topk_w, int32_t* status, cudaStream_t stream);
 
 // Tensor-core router for large batches (T >= kRouterTcMinTokens): W_r split
 // into three bf16 terms, partial logits on the tensor cores, a warp-per-token
@@ -32,7 +33,8 @@ size_t router_tc_scratch_bytes(int T, int d, int E);
 int router_tc_splits(int T, int d, int num_sms);  // partial-logit buffers: [splits][T][E] fp32 in `part`
 cudaError_t launch_router_tc(const uint16_t* x, const float* w_r, void* scratch, float* part, int32_t* flagged_count,
                              int T, int d, int E, int n_groups, int topk_groups, int top_k, float routed_scale,
-                             int32_t* topk_idx, float* topk_w, int32_t* status, int num_sms, cudaStream_t stream);
+                             const float* sel_bias, int32_t* topk_idx, float* topk_w, int32_t* status, int num_sms,
+                             cudaStream_t stream);
 
 // ---- permutation (permute.cu) ----
 int bitmap_words(int T);

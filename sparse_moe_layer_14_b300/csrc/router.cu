@@ -150,16 +150,25 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
 constexpr int kMaxPerLane = 8;  // E <= 256
 
 // Group-limited selection of one token by one warp. Lane l holds the scores
-// of experts l, l+32, l+64, ... in s[]; writes the token's K expert ids (slot
-// order: descending score, ties to the lower id) and weights. Returns, in
-// every lane, the decision margins: x = worst kept group score - best dropped
-// one; y = the smaller of (worst chosen score - best unchosen candidate) and
-// the gaps between consecutive slots.
-__device__ float2 warp_select(const float (&s)[kMaxPerLane], int lane, int t, int E, int G, int Gk, int K,
-                              float scale, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
-                              int32_t* status) {
+// of experts l, l+32, l+64, ... in s[]; `bias` ([E] fp32, nullable) is the
+// per-expert selection bias of DeepSeek-V3-style balancing: groups and
+// experts are chosen on s + bias, the weights use s. Writes the token's K
+// expert ids (slot order: descending selection score, ties to the lower id)
+// and weights. Returns, in every lane, the decision margins (on selection
+// scores): x = worst kept group score - best dropped one; y = the smaller of
+// (worst chosen score - best unchosen candidate) and the gaps between
+// consecutive slots.
+__device__ float2 warp_select(const float (&s_in)[kMaxPerLane], const float* __restrict__ bias, int lane, int t,
+                              int E, int G, int Gk, int K, float scale, int32_t* __restrict__ topk_idx,
+                              float* __restrict__ topk_w, int32_t* status) {
   const int gsz = E / G;
   constexpr float kMasked = -1.0f;  // below every sigmoid score
+  float s[kMaxPerLane];             // selection scores
+#pragma unroll
+  for (int i = 0; i < kMaxPerLane; ++i) {
+    const int e = lane + 32 * i;
+    s[i] = (bias && e < E) ? s_in[i] + bias[e] : s_in[i];
+  }
   int grp[kMaxPerLane];             // group of each of this lane's experts (E = none)
 #pragma unroll
   for (int i = 0; i < kMaxPerLane; ++i) {
@@ -242,9 +251,10 @@ __device__ float2 warp_select(const float (&s)[kMaxPerLane], int lane, int t, in
 
   // choose the K best experts of the kept groups (ties to the lower index)
   uint32_t taken = 0;  // bit i: this lane's element i is chosen
-  float my_s = 0.f;
+  float my_s = 0.f;    // slot `lane`: its selection score ...
+  float my_w = 0.f;    // ... and its unbiased score (the weight's)
   int my_e = 0;
-  float sum = 0.f;
+  float sum = 0.f;     // of unbiased scores
   for (int k = 0; k < K; ++k) {
     float v = -2.0f;
     int idx = 0x7fffffff;
@@ -257,16 +267,22 @@ __device__ float2 warp_select(const float (&s)[kMaxPerLane], int lane, int t, in
       }
     }
     warp_argmax(v, idx);
+    float u = 0.f;  // the chosen expert's unbiased score, from the lane that holds it
     if (idx >= E || idx < 0) {  // only possible with NaN scores
       latch_status(status, MOE_DEV_BAD_EXPERT);
       idx = 0;
       v = 0.f;
-    } else if ((idx & 31) == lane) {
-      taken |= 1u << (idx >> 5);
+    } else {
+      if ((idx & 31) == lane) taken |= 1u << (idx >> 5);
+#pragma unroll
+      for (int i = 0; i < kMaxPerLane; ++i)
+        if (i == (idx >> 5)) u = s_in[i];
+      u = __shfl_sync(0xffffffffu, u, idx & 31);
     }
-    sum += v;
+    sum += u;
     if (lane == k) {
       my_s = v;
+      my_w = u;
       my_e = idx;
     }
   }
@@ -294,7 +310,7 @@ __device__ float2 warp_select(const float (&s)[kMaxPerLane], int lane, int t, in
   if (lane < K) {
     float w = 0.f;
     if (sum > 0.f) {
-      w = scale * my_s / sum;
+      w = scale * my_w / sum;
     } else if (lane == 0) {
       latch_status(status, MOE_DEV_ZERO_SUM);
     }
@@ -306,6 +322,7 @@ __device__ float2 warp_select(const float (&s)[kMaxPerLane], int lane, int t, in
 
 __global__ void __launch_bounds__(256) router_select_kernel(const float* __restrict__ logits, int T,
                                                             int E, int G, int Gk, int K, float scale,
+                                                            const float* __restrict__ bias,
                                                             int32_t* __restrict__ topk_idx,
                                                             float* __restrict__ topk_w, int32_t* status) {
   const int lane = threadIdx.x & 31;
@@ -317,7 +334,7 @@ __global__ void __launch_bounds__(256) router_select_kernel(const float* __restr
     const int e = lane + 32 * i;
     s[i] = (e < E) ? 1.0f / (1.0f + expf(-logits[static_cast<size_t>(t) * E + e])) : -1.0f;
   }
-  warp_select(s, lane, t, E, G, Gk, K, scale, topk_idx, topk_w, status);
+  warp_select(s, bias, lane, t, E, G, Gk, K, scale, topk_idx, topk_w, status);
 }
 
 // ---------------------------------------------------------------- tensor-core path
@@ -525,6 +542,7 @@ __global__ void __launch_bounds__(192, 1) router_tc_kernel(const __grid_constant
 // relative).
 __global__ void __launch_bounds__(256) router_select_flag_kernel(const float* __restrict__ part, int splits, int T,
                                                                  int E, int G, int Gk, int K, float scale,
+                                                                 const float* __restrict__ bias,
                                                                  int32_t* __restrict__ topk_idx,
                                                                  float* __restrict__ topk_w,
                                                                  int32_t* __restrict__ flagged,
@@ -557,7 +575,7 @@ __global__ void __launch_bounds__(256) router_select_flag_kernel(const float* __
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, off));
-  const float2 margin = warp_select(s, lane, t, E, G, Gk, K, scale, topk_idx, topk_w, status);
+  const float2 margin = warp_select(s, bias, lane, t, E, G, Gk, K, scale, topk_idx, topk_w, status);
   // Score error bound of the tensor-core logits: measured at most 4.7e-6 on
   // Beam-shape inputs (|logit| <= 6, over a million scores); e_s keeps a factor
   // of at least 2.5. A group score sums two scores and a group margin compares
@@ -690,6 +708,7 @@ __global__ void __launch_bounds__(kFlagThreads) router_flagged_logits_kernel(
 __global__ void __launch_bounds__(256) router_flagged_select_kernel(const float* __restrict__ part, int splits, int E,
                                                                    int G,
                                                                    int Gk, int K, float scale,
+                                                                   const float* __restrict__ bias,
                                                                    const int32_t* __restrict__ flagged,
                                                                    const int32_t* __restrict__ flagged_count,
                                                                    int32_t* __restrict__ topk_idx,
@@ -708,7 +727,7 @@ __global__ void __launch_bounds__(256) router_flagged_select_kernel(const float*
         sv[j] = 1.0f / (1.0f + expf(-l));
       }
     }
-    warp_select(sv, lane, flagged[i], E, G, Gk, K, scale, topk_idx, topk_w, status);
+    warp_select(sv, bias, lane, flagged[i], E, G, Gk, K, scale, topk_idx, topk_w, status);
   }
 }
 
@@ -770,7 +789,8 @@ size_t router_tc_scratch_bytes(int T, int d, int E) {
 
 cudaError_t launch_router_tc(const uint16_t* x, const float* w_r, void* scratch, float* part, int32_t* flagged_count,
                              int T, int d, int E, int n_groups, int topk_groups, int top_k, float routed_scale,
-                             int32_t* topk_idx, float* topk_w, int32_t* status, int num_sms, cudaStream_t stream) {
+                             const float* sel_bias, int32_t* topk_idx, float* topk_w, int32_t* status, int num_sms,
+                             cudaStream_t stream) {
   const int E_pad = router_epad(E);
   uint8_t* p = static_cast<uint8_t*>(scratch);
   auto take = [&p](size_t bytes) {
@@ -803,8 +823,8 @@ cudaError_t launch_router_tc(const uint16_t* x, const float* w_r, void* scratch,
   if (err != cudaSuccess) return err;
   router_tc_kernel<<<dim3((T + kTcTokens - 1) / kTcTokens, splits), 192, smem, stream>>>(tmX, tmW, a);
   router_select_flag_kernel<<<(T + 7) / 8, 256, 0, stream>>>(part, splits, T, E, n_groups, topk_groups, top_k,
-                                                             routed_scale, topk_idx, topk_w, flagged, flagged_count,
-                                                             status);
+                                                             routed_scale, sel_bias, topk_idx, topk_w, flagged,
+                                                             flagged_count, status);
   // the tensor-core partials were consumed by the selection: reuse `part` for the recompute
   const int fsplits = flag_splits(d);
   const size_t xs_bytes = sizeof(float4) * static_cast<size_t>(d / fsplits) +
@@ -815,8 +835,8 @@ cudaError_t launch_router_tc(const uint16_t* x, const float* w_r, void* scratch,
   router_flagged_logits_kernel<<<num_sms, kFlagThreads, xs_bytes, stream>>>(x, w_r, d, E, flagged, flagged_count,
                                                                             part, fsplits, status);
   router_flagged_select_kernel<<<num_sms, 256, 0, stream>>>(part, fsplits, E, n_groups, topk_groups, top_k,
-                                                            routed_scale, flagged, flagged_count, topk_idx, topk_w,
-                                                            status);
+                                                            routed_scale, sel_bias, flagged, flagged_count, topk_idx,
+                                                            topk_w, status);
   return cudaGetLastError();
 }
 
@@ -843,14 +863,14 @@ cudaError_t launch_router_logits(const uint16_t* x, const float* w_r, float* par
 }
 
 cudaError_t launch_router_select(float* partial, int splits, int T, int E, int n_groups, int topk_groups,
-                                 int top_k, float routed_scale, int32_t* topk_idx, float* topk_w,
-                                 int32_t* status, cudaStream_t stream) {
+                                 int top_k, float routed_scale, const float* sel_bias, int32_t* topk_idx,
+                                 float* topk_w, int32_t* status, cudaStream_t stream) {
   if (splits > 1) {
     const int64_t n = static_cast<int64_t>(T) * E;
     split_reduce_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(partial, splits, n);
   }
   router_select_kernel<<<(T + 7) / 8, 256, 0, stream>>>(partial, T, E, n_groups, topk_groups, top_k, routed_scale,
-                                                         topk_idx, topk_w, status);
+                                                         sel_bias, topk_idx, topk_w, status);
   return cudaGetLastError();
 }
 

@@ -73,13 +73,15 @@ class DeviceWeights:
             self.dev = bm.ExpertWeights(**tens)
 
 
-def compare_routing(cfg, gpu_idx: np.ndarray, gpu_w: np.ndarray, orc: dict, all_tokens=True):
+def compare_routing(cfg, gpu_idx: np.ndarray, gpu_w: np.ndarray, orc: dict, all_tokens=True, bias=None):
     """Check GPU routing against the oracle; returns (excluded token list, ref_idx, ref_w)
-    where ref_* is the routing to use for the reference output."""
+    where ref_* is the routing to use for the reference output. With a selection bias
+    [E], slot order and tie validity are judged on s + bias (float32), weights on s."""
     T, K = gpu_idx.shape
     G, Gk = cfg.n_groups, cfg.topk_groups
     gsz = cfg.E // G
     s = orc["scores"].astype(np.float64)
+    sel = s if bias is None else (orc["scores"] + np.asarray(bias, np.float32)).astype(np.float32).astype(np.float64)
     near = (orc["margin_group"] < TIE_EPS) | (orc["margin_expert"] < TIE_EPS)
     excluded = np.nonzero(near)[0]
     ok = ~near
@@ -88,7 +90,7 @@ def compare_routing(cfg, gpu_idx: np.ndarray, gpu_w: np.ndarray, orc: dict, all_
     os_sorted = np.sort(orc["idx"][ok], axis=1)
     bad = np.nonzero(np.any(gs_sorted != os_sorted, axis=1))[0]
     assert bad.size == 0, f"routing differs on {bad.size} decided tokens, e.g. {np.nonzero(ok)[0][bad[:5]]}"
-    sv = np.take_along_axis(s, gpu_idx.astype(np.int64), axis=1)
+    sv = np.take_along_axis(sel, gpu_idx.astype(np.int64), axis=1)
     assert np.all(np.diff(sv[ok], axis=1) <= TIE_EPS), "slots not in descending score order"
     # per-expert counts over decided tokens (bit-exact)
     cg = np.bincount(gpu_idx[ok].ravel(), minlength=cfg.E)
@@ -106,7 +108,7 @@ def compare_routing(cfg, gpu_idx: np.ndarray, gpu_w: np.ndarray, orc: dict, all_
     for t in excluded:
         chosen = gpu_idx[t]
         assert len(set(chosen.tolist())) == K
-        assert any(_valid_under_ties(s[t], orc["gscores"][t].astype(np.float64), chosen, gsz, Gk, K, kept)
+        assert any(_valid_under_ties(sel[t], orc["gscores"][t].astype(np.float64), chosen, gsz, Gk, K, kept)
                    for kept in _tied_kept_sets(orc["gscores"][t].astype(np.float64), Gk)), \
             f"token {t}: GPU choice is not one of the tied optima"
         ref_idx[t] = chosen

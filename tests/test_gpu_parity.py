@@ -60,6 +60,51 @@ def test_route_parity(name, T, seed):
     assert excluded.size <= max(2, T // 200)
 
 
+@pytest.mark.parametrize("name,T,seed", [("tiny", 64, 21), ("decode", 64, 22), ("decode", 1100, 23),
+                                         ("prefill", 2048, 24)])
+def test_route_parity_selection_bias(name, T, seed):
+    """Per-expert selection bias (DeepSeek-V3-style balancing): choice on s + b, weights on s;
+    SIMT router (T < 1024) and tensor-core router with its fp32 recompute (T >= 1024)."""
+    cfg = W.CONFIGS[name].with_tokens(T)
+    x_h, wr_h = W.gen_x(cfg, seed), W.gen_wr(cfg, seed)
+    bias = (0.1 * (W.uniform_f64(seed, W.TID_AUX + 7, 0, cfg.E) - 0.5)).astype(np.float32)
+    dims = bm.Dims.from_config(cfg)
+    ws = bm.allocate_workspace(dims)
+    idx = torch.empty((T, cfg.top_k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, cfg.top_k), dtype=torch.float32, device="cuda")
+    bm.moe_route(dims, dev(x_h), dev(wr_h), idx, w, ws, sel_bias=dev(bias))
+    torch.cuda.synchronize()
+    assert bm.moe_get_device_status(ws) == bm.MOE_DEV_OK
+    gi, gw = idx.cpu().numpy(), w.cpu().numpy()
+    orc = O.route(cfg, x_h, wr_h, bias=bias)
+    excluded, _, _ = compare_routing(cfg, gi, gw, orc, bias=bias)
+    assert excluded.size <= max(2, T // 200)
+    # the bias changes the choice of some tokens, so the biased path is the one tested
+    assert np.any(np.sort(orc["idx"], 1) != np.sort(O.route(cfg, x_h, wr_h)["idx"], 1))
+
+
+def test_forward_selection_bias():
+    cfg = TINY.with_tokens(96)
+    inp = W.make_host_inputs(cfg, 25)
+    bias = (0.2 * (W.uniform_f64(25, W.TID_AUX + 7, 0, cfg.E) - 0.5)).astype(np.float32)
+    dw = DeviceWeights(cfg, 25)
+    dims = bm.Dims.from_config(cfg)
+    ws = bm.allocate_workspace(dims)
+    out = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device="cuda")
+    idx = torch.empty((cfg.T, cfg.top_k), dtype=torch.int32, device="cuda")
+    bm.moe_forward(dims, dev(inp["x"]), dev(inp["w_r"]), dw.dev, out, ws, topk_idx=idx, sel_bias=dev(bias))
+    torch.cuda.synchronize()
+    assert bm.moe_get_device_status(ws) == bm.MOE_DEV_OK
+    orc = O.route(cfg, inp["x"], inp["w_r"], bias=bias)
+    gi = idx.cpu().numpy()
+    s = orc["scores"].astype(np.float64)
+    sv = np.take_along_axis(s, gi.astype(np.int64), 1)
+    w_like = (cfg.routed_scale * sv / sv.sum(1, keepdims=True)).astype(np.float32)  # unbiased weights
+    _, ref_idx, ref_w = compare_routing(cfg, gi, w_like, orc, bias=bias)
+    ref = O.forward_tokens(cfg, inp["x"], ref_idx, ref_w, np.arange(cfg.T), dw.host)
+    check_output(host_bits(out), ref, TOL_BF16)
+
+
 def test_route_uniform_scores():
     """W_r = 0: every score is 0.5, lowest-index groups/experts win, w = 2.5/8 = 0.3125."""
     cfg = W.CONFIGS["decode"].with_tokens(40)
