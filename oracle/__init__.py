@@ -52,6 +52,7 @@ def load(path: str | None = None):
     L.oracle_forward_tokens.argtypes = [i32, i32, i32, i32, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp,
                                         vp, vp, vp, vp]
     L.oracle_num_threads.restype = i32
+    L.oracle_residual_update.argtypes = [i32, i32, vp, vp, vp, dbl, i32, vp]
     return L
 
 
@@ -164,6 +165,18 @@ def combine(y_rows, inv_row, w, L=None):
     out = np.empty((T, d), np.float64)
     L.oracle_combine(T, K, d, _p(y_rows), _p(np.ascontiguousarray(inv_row, np.int32)), _p(w), _p(out))
     return out
+
+
+def residual_update(out, h_old, gamma, eps, step, L=None):
+    """Post-norm and depth-scaled residual addition: h_new [T, d] f64 from the sublayer output
+    out [T, d] f64, the stream h_old [T, d] bf16 bits, the norm gain gamma [d] bf16 bits."""
+    L = L or lib()
+    out = np.ascontiguousarray(out, np.float64)
+    T, d = out.shape
+    h_new = np.empty((T, d), np.float64)
+    L.oracle_residual_update(T, d, _p(out), _p(np.ascontiguousarray(h_old, np.uint16)),
+                             _p(np.ascontiguousarray(gamma, np.uint16)), float(eps), int(step), _p(h_new))
+    return h_new
 
 
 def forward_tokens(cfg, x, idx, w, tokens, weights, L=None):

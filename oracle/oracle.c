@@ -358,6 +358,33 @@ void oracle_forward_tokens(int d, int I, int K, int wfmt, const uint16_t* x, con
   free(y);
 }
 
+/* ---------------- residual update: article section "Residual stream" ---------------- */
+
+/* Post-norm and depth-scaled residual addition of one sublayer output, per
+ * token row t (the article: every sublayer is normalised before and after; at
+ * step k the sublayer output is added with weight 1/sqrt(k) and the existing
+ * stream kept with weight sqrt((k-1)/k); the norms are computed in FP32 --
+ * here in double, the exact value):
+ *   r       = sqrt(mean_c(out[t][c]^2) + eps)
+ *   normed  = out[t][c] / r * gamma[c]                    (RMSNorm)
+ *   h_new   = sqrt((k-1)/k) * h_old[t][c] + (1/sqrt(k)) * normed
+ * out [T][d] double (the sublayer output), h_old [T][d] bf16 bits, gamma [d]
+ * bf16 bits, h_new [T][d] double. k >= 1 (k = 1 keeps nothing of h_old). */
+void oracle_residual_update(int T, int d, const double* out, const uint16_t* h_old, const uint16_t* gamma,
+                            double eps, int k, double* h_new) {
+  const double keep = sqrt((double)(k - 1) / (double)k), add = 1.0 / sqrt((double)k);
+#pragma omp parallel for schedule(static)
+  for (int t = 0; t < T; ++t) {
+    const double* o = out + (int64_t)t * d;
+    double ss = 0.0;
+    for (int c = 0; c < d; ++c) ss += o[c] * o[c];
+    const double r = sqrt(ss / d + eps);
+    for (int c = 0; c < d; ++c)
+      h_new[(int64_t)t * d + c] =
+          keep * bf16_value(h_old[(int64_t)t * d + c]) + add * (o[c] / r * bf16_value(gamma[c]));
+  }
+}
+
 int oracle_num_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();

@@ -303,10 +303,59 @@ def check_nvfp4_ffn(L):
         assert np.max(np.abs(y[r] - yr)) <= 1e-3 * np.sqrt((yr ** 2).mean())
 
 
+def _bf16_const(v, n):
+    return _bf16_bits(np.full(n, v, np.float32))
+
+
+def check_residual_step1_normalises(L):
+    """At step k = 1 nothing of the old stream is kept and the sublayer output is RMS-normalised:
+    each row's mean square is gamma^2 * ms / (ms + eps), which is gamma^2 for eps = 0, whatever
+    the output's own scale."""
+    T, d = 12, 96
+    out = W.normal_f32(31, W.TID_AUX, 0, T * d, 3.0).reshape(T, d).astype(np.float64)
+    h_old = W.normal_bf16(31, W.TID_AUX + 1, 0, T * d, 1.0).reshape(T, d)
+    for g, eps in ((1.0, 0.0), (2.0, 0.0), (1.0, 1e-2)):
+        hn = O.residual_update(out, h_old, _bf16_const(g, d), eps, 1, L)
+        ms = (out ** 2).mean(1)
+        assert np.allclose((hn ** 2).mean(1), g * g * ms / (ms + eps), rtol=1e-12, atol=0)
+    hn1 = O.residual_update(out, h_old, _bf16_const(1.0, d), 0.0, 1, L)
+    hn7 = O.residual_update(7.0 * out, h_old, _bf16_const(1.0, d), 0.0, 1, L)
+    assert np.allclose(hn1, hn7, rtol=1e-12, atol=1e-15)
+
+
+def check_residual_equal_weights(L):
+    """The article's claim: counting the input embedding as step 1 and adding 104 sublayer
+    outputs, every output and the embedding carry the same weight in the final stream. With
+    orthogonal unit-RMS vectors v_1..v_105 (scaled one-hot rows), the final stream's component
+    along each is 1/sqrt(105) (the stream is kept in bf16 between steps: rounding drifts the
+    coefficients by up to ~3 %; a wrong weight rule is off by tens of percent)."""
+    N, d = 105, 128
+    v = np.sqrt(d) * np.eye(d)[:N]               # v_j: unit RMS, mutually orthogonal
+    h = _bf16_bits(v[0].astype(np.float32))[None]  # step 1: the embedding
+    for k in range(2, N + 1):
+        hn = O.residual_update(v[k - 1][None], h, _bf16_const(1.0, d), 0.0, k, L)
+        h = _bf16_bits(hn.astype(np.float32))
+    coef = _f(h[0])[:N] / np.sqrt(d)
+    assert np.allclose(coef, 1 / np.sqrt(N), rtol=4e-2, atol=0), (coef.min(), coef.max())
+    assert np.all(_f(h[0])[N:] == 0)
+
+
+def check_residual_constant_scale(L):
+    """The weights' squares sum to one, so a unit-RMS stream plus an independent unit-RMS
+    output stays at unit RMS on average, at every step."""
+    T, d = 400, 256
+    for k in (2, 5, 52):
+        h_old = W.normal_bf16(40 + k, W.TID_AUX, 0, T * d, 1.0).reshape(T, d)
+        out = W.normal_f32(40 + k, W.TID_AUX + 1, 0, T * d, 0.3).reshape(T, d).astype(np.float64)
+        hn = O.residual_update(out, h_old, _bf16_const(1.0, d), 0.0, k, L)
+        assert abs((hn ** 2).mean() - 1.0) < 0.02, (k, (hn ** 2).mean())
+
+
 CHECKS = [check_uniform_scores, check_router_logits, check_select_bruteforce, check_select_bias,
           check_select_invariants,
           check_single_expert_dense, check_identical_experts, check_permute, check_combine,
-          check_forward_matches_stages, check_nvfp4_decode, check_nvfp4_ffn]
+          check_forward_matches_stages, check_nvfp4_decode, check_nvfp4_ffn, check_residual_step1_normalises,
+          check_residual_equal_weights, check_residual_constant_scale]
 
 
 @pytest.mark.parametrize("check", CHECKS, ids=lambda c: c.__name__)
@@ -350,6 +399,10 @@ MUTANTS = {
     "bias_ignored": ("sel[e] = bias ? s[e] + bias[e] : s[e];", "sel[e] = s[e];"),
     "bias_in_weights": ("w[k] = scale * (double)s[idx[k]] / sum;", "w[k] = scale * (double)sel[idx[k]] / sum;"),
     "bias_in_weight_sum": ("sum += (double)s[best];", "sum += (double)sel[best];"),
+    "residual_keep_linear": ("sqrt((double)(k - 1) / (double)k)", "((double)(k - 1) / (double)k)"),
+    "residual_keep_on_output": ("keep * bf16_value(h_old", "add * bf16_value(h_old"),
+    "rms_sum_not_mean": ("sqrt(ss / d + eps)", "sqrt(ss + eps)"),
+    "post_norm_no_gain": (" * bf16_value(gamma[c]))", ")"),
     "no_group_limit": ("if (kept[e / gsz] && !taken[e] && (best < 0", "if (!taken[e] && (best < 0"),
     "h_not_rounded": ("hbuf[i] = bf16_value(hb);", "hbuf[i] = (double)(silu * uf);"),
     "down_transposed": ("acc += hbuf[i] * wmat_at(down, e, n, i);", "acc += hbuf[i] * wmat_at(down, e, i % d, n % I);"),
