@@ -96,6 +96,8 @@ DENSE_CASES = {
                                  inter=20480),
 }
 
+RESIDUAL_STEP = 10  # the residual-addition index k used with --residual (weights sqrt(9/10), 1/sqrt(10))
+
 DEFAULT_STEPS = {"dense_prefill": 100, "decode": 300, "prefill": 200, "skewed": 40, "nvfp4": 200, "profile_decode": 20,
                  "profile_prefill": 20, "profile_dense": 20, "profile_nvfp4": 20}
 
@@ -291,8 +293,21 @@ def run_ours(args, rank, world, local_rank):
     stream = torch.cuda.current_stream()
     setup_s = time.time() - t_setup
 
+    gain = None
+    if args.residual:  # post-norm gain ~ 1 and a unit-RMS residual stream, updated in place each step
+        gain = (1.0 + 0.05 * torch.randn(cfg.d, generator=torch.Generator().manual_seed(args.seed))).to(
+            torch.bfloat16).cuda()
+        out.copy_(torch.randn((cfg.T, cfg.d), generator=torch.Generator().manual_seed(args.seed + 1)).to(
+            torch.bfloat16))
+
+    def forward(x_, out_, counts_=None):
+        if args.residual:
+            bm.moe_forward_residual(dims, x_, w_r, weights, gain, 1e-6, RESIDUAL_STEP, out_, ws, counts=counts_)
+        else:
+            bm.moe_forward(dims, x_, w_r, weights, out_, ws, counts=counts_)
+
     def step():
-        bm.moe_forward(dims, x, w_r, weights, out, ws, counts=counts)
+        forward(x, out, counts)
 
     for _ in range(args.warmup):
         step()
@@ -338,7 +353,7 @@ def run_ours(args, rank, world, local_rank):
     x_pin = torch.from_numpy(x_h).view(torch.int16).pin_memory()
     out_pin = [torch.empty((cfg.T, cfg.d), dtype=torch.int16).pin_memory() for _ in range(2)]
     x_dev = [torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
-    out_dev = [torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    out_dev = [out.clone() for _ in range(2)]  # (with --residual: the residual stream, updated in place)
     copy_stream = torch.cuda.Stream()
 
     def e2e_run(n):
@@ -355,7 +370,7 @@ def run_ours(args, rank, world, local_rank):
             stream.wait_event(h2d[b])
             if i >= 2:
                 stream.wait_event(d2h[b])  # out_dev[b] was read back
-            bm.moe_forward(dims, x_dev[b], w_r, weights, out_dev[b], ws)
+            forward(x_dev[b], out_dev[b])
             fwd[b].record(stream)
             with torch.cuda.stream(copy_stream):
                 if i + 1 < n:
@@ -401,6 +416,8 @@ def run_ours(args, rank, world, local_rank):
         "impl": "ours",
         "config": {"workload": describe(cfg), "T": cfg.T, "d": cfg.d, "E": cfg.E, "inter": cfg.inter,
                    "top_k": cfg.top_k, "parallelism": f"replicas x{world}",
+                   "last_stage": (f"combine fused with post-norm (RMSNorm) and residual update, step k={RESIDUAL_STEP}"
+                                  if args.residual else "combine to out"),
                    "l2": f"no flush: {touched} experts x {3 * cfg.d * cfg.inter * weight_bytes_per_param(cfg) / 1e6:.1f} MB "
                          f"of weights streamed per step exceed the 126 MB L2"},
         "roofline": {"kernel": f"{kname} (GEMM1 + SwiGLU)", "bound": bound,
@@ -643,6 +660,9 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-tokens", type=int, default=16, help="tokens per reference-arm step")
+    ap.add_argument("--residual", action="store_true",
+                    help="end the block with the fused post-norm and depth-scaled residual update "
+                         "(moe_forward_residual) instead of writing the output")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

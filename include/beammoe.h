@@ -198,6 +198,29 @@ moe_status_t moe_forward_ex(const moe_dims_t* dims, const moe_bf16_t* x, const f
                             const moe_expert_weights_t* weights, moe_bf16_t* out, int32_t* topk_idx,
                             int32_t* counts, void* ws, size_t ws_bytes, void* stream);
 
+/* Combine fused with the sublayer's post-norm and the depth-scaled residual
+ * addition (release article, section "Residual stream": every sublayer is
+ * normalised before and after; at step k the stream keeps weight
+ * sqrt((k-1)/k) and takes the sublayer output with weight 1/sqrt(k), the input
+ * embedding counting as step 1; the norms are computed in FP32). For every
+ * token t, with out[t] = sum_k topk_w[t][k] * y_perm[inv_row[t*top_k+k]] (FP32,
+ * slot order):
+ *   r = sqrt(mean_c(out[t][c]^2) + eps)
+ *   resid[t][c] = bf16( sqrt((step-1)/step) * resid[t][c]
+ *                       + (1/sqrt(step)) * out[t][c] / r * norm_gain[c] )
+ * in place. resid [T][d] bf16 and norm_gain [d] bf16 (the post-norm's RMSNorm
+ * weight) 16-byte aligned; step >= 1; eps >= 0 (the pages give none; 1e-6 is
+ * usual); d <= 8192 (larger d returns MOE_ERR_UNSUPPORTED). moe_forward_residual
+ * is moe_forward_ex with this as its
+ * last stage instead of writing out. */
+moe_status_t moe_combine_residual(const moe_dims_t* dims, const moe_bf16_t* y_perm, const int32_t* inv_row,
+                                  const float* topk_w, const moe_bf16_t* norm_gain, float eps, int32_t step,
+                                  moe_bf16_t* resid, void* ws, size_t ws_bytes, void* stream);
+moe_status_t moe_forward_residual(const moe_dims_t* dims, const moe_bf16_t* x, const float* w_r,
+                                  const float* sel_bias, const moe_expert_weights_t* weights,
+                                  const moe_bf16_t* norm_gain, float eps, int32_t step, moe_bf16_t* resid,
+                                  int32_t* topk_idx, int32_t* counts, void* ws, size_t ws_bytes, void* stream);
+
 /* Dense SwiGLU MLP of the first decoder layers (release article, section
  * "Architecture": the first 3 of the 52 layers use a dense SwiGLU MLP instead
  * of the Mixture-of-Experts block). For every token t:

@@ -221,6 +221,37 @@ def moe_combine(dims: Dims, y_perm, inv_row, topk_w, out, ws=None, stream=None):
                                              _ptr(out), _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
 
 
+def moe_combine_residual(dims: Dims, y_perm, inv_row, topk_w, norm_gain, eps: float, step: int, resid, ws=None,
+                         stream=None):
+    """Combine + post-norm (RMSNorm with gain norm_gain [d]) + depth-scaled residual update of
+    resid [T, d] in place: resid = sqrt((step-1)/step) resid + (1/sqrt(step)) RMSNorm(out)."""
+    R = dims.T * dims.top_k
+    _expect(y_perm, _BF16, (R, dims.d), "y_perm")
+    _expect(inv_row, (torch.int32,), (R,), "inv_row")
+    _expect(topk_w, (torch.float32,), (dims.T, dims.top_k), "topk_w")
+    _expect(norm_gain, _BF16, (dims.d,), "norm_gain")
+    _expect(resid, _BF16, (dims.T, dims.d), "resid")
+    _check("moe_combine_residual", _lib().moe_combine_residual(
+        ctypes.byref(dims.c()), _ptr(y_perm), _ptr(inv_row), _ptr(topk_w), _ptr(norm_gain), float(eps), int(step),
+        _ptr(resid), _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
+
+
+def moe_forward_residual(dims: Dims, x, w_r, weights: ExpertWeights, norm_gain, eps: float, step: int, resid, ws,
+                         topk_idx=None, counts=None, stream=None, sel_bias=None):
+    """moe_forward whose last stage is the post-norm and residual update of resid (in place)."""
+    _expect(x, _BF16, (dims.T, dims.d), "x")
+    _expect(w_r, (torch.float32,), (dims.d, dims.E), "w_r")
+    _expect(norm_gain, _BF16, (dims.d,), "norm_gain")
+    _expect(resid, _BF16, (dims.T, dims.d), "resid")
+    _expect(topk_idx, (torch.int32,), (dims.T, dims.top_k), "topk_idx")
+    _expect(counts, (torch.int32,), (dims.E,), "counts")
+    _expect(sel_bias, (torch.float32,), (dims.E,), "sel_bias")
+    _check_weights(dims, weights)
+    _check("moe_forward_residual", _lib().moe_forward_residual(
+        ctypes.byref(dims.c()), _ptr(x), _ptr(w_r), _ptr(sel_bias), ctypes.byref(weights.c()), _ptr(norm_gain),
+        float(eps), int(step), _ptr(resid), _ptr(topk_idx), _ptr(counts), _ptr(ws), ws.numel(), _stream(stream)))
+
+
 def _dense(dims: Dims) -> Dims:
     return Dims(dims.T, dims.d, 1, 1, 1, 1, dims.inter, 1.0, dims.wfmt)
 

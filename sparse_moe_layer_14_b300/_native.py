@@ -21,7 +21,7 @@ MOE_W_BF16, MOE_W_NVFP4 = 0, 1
 EXPORTS = ["moe_workspace_bytes", "moe_workspace_init", "moe_route", "moe_permute", "moe_expert_ffn",
            "moe_combine", "moe_forward", "moe_get_device_status", "moe_set_wait_bound", "moe_set_stage_events",
            "moe_version", "moe_permute_noalloc", "moe_dense_workspace_bytes", "moe_dense_mlp", "moe_route_ex",
-           "moe_forward_ex"]
+           "moe_forward_ex", "moe_combine_residual", "moe_forward_residual"]
 
 
 class MoeDims(ctypes.Structure):
@@ -66,6 +66,11 @@ def load(path: str = LIB_PATH):
     L.moe_route_ex.restype = st
     L.moe_forward_ex.argtypes = [pd, vp, vp, vp, pw, vp, vp, vp, vp, sz, vp]
     L.moe_forward_ex.restype = st
+    L.moe_combine_residual.argtypes = [pd, vp, vp, vp, vp, ctypes.c_float, ctypes.c_int32, vp, vp, sz, vp]
+    L.moe_combine_residual.restype = st
+    L.moe_forward_residual.argtypes = [pd, vp, vp, vp, pw, vp, ctypes.c_float, ctypes.c_int32, vp, vp, vp, vp, sz,
+                                       vp]
+    L.moe_forward_residual.restype = st
     L.moe_forward.restype = st
     L.moe_get_device_status.argtypes = [vp, vp, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]
     L.moe_get_device_status.restype = st

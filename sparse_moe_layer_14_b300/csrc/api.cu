@@ -265,14 +265,26 @@ moe_status_t moe_forward(const moe_dims_t* dims, const moe_bf16_t* x, const floa
   return moe_forward_ex(dims, x, w_r, nullptr, weights, out, topk_idx, counts, ws, ws_bytes, stream);
 }
 
-moe_status_t moe_forward_ex(const moe_dims_t* dims, const moe_bf16_t* x, const float* w_r, const float* sel_bias,
-                            const moe_expert_weights_t* weights, moe_bf16_t* out, int32_t* topk_idx, int32_t* counts,
-                            void* ws, size_t ws_bytes, void* stream) {
+// The fused forward; with res != nullptr the last stage is the combine fused
+// with the post-norm and residual update of res->resid (no `out`).
+struct ResidualArgs {
+  const uint16_t* gain;
+  float eps;
+  int step;
+  uint16_t* resid;
+};
+
+moe_status_t forward_impl(const moe_dims_t* dims, const moe_bf16_t* x, const float* w_r, const float* sel_bias,
+                          const moe_expert_weights_t* weights, moe_bf16_t* out, const ResidualArgs* res,
+                          int32_t* topk_idx, int32_t* counts, void* ws, size_t ws_bytes, void* stream) {
   moe_status_t st = check_dims(dims);
   if (st != MOE_OK) return st;
   if (dims->T == 0) return MOE_OK;
-  if (!aligned16(x) || !aligned16(w_r) || !out || (reinterpret_cast<uintptr_t>(out) & 7u))
+  if (!aligned16(x) || !aligned16(w_r)) return MOE_ERR_INVALID_ARG;
+  if (!res && (!out || (reinterpret_cast<uintptr_t>(out) & 7u))) return MOE_ERR_INVALID_ARG;
+  if (res && (!aligned16(res->resid) || !aligned16(res->gain) || res->step < 1 || !(res->eps >= 0.0f)))
     return MOE_ERR_INVALID_ARG;
+  if (res && dims->d > 8192) return MOE_ERR_UNSUPPORTED;  // one cluster of <= 8 blocks per row
   if (sel_bias && (reinterpret_cast<uintptr_t>(sel_bias) & 3u)) return MOE_ERR_INVALID_ARG;
   if ((st = check_weights(dims, weights)) != MOE_OK) return st;
   if ((st = check_ws(dims, ws, ws_bytes)) != MOE_OK) return st;
@@ -295,9 +307,40 @@ moe_status_t moe_forward_ex(const moe_dims_t* dims, const moe_bf16_t* x, const f
       MOE_OK)
     return st;
   if (mark(4, s) != cudaSuccess) return MOE_ERR_CUDA;
-  st = cuda_status(launch_combine(y, inv_row, w, out, dims->T, dims->d, dims->top_k, status_word(ws), s));
+  st = cuda_status(res ? launch_combine_residual(y, inv_row, w, res->gain, res->eps, res->step, res->resid, dims->T,
+                                                 dims->d, dims->top_k, status_word(ws), s)
+                       : launch_combine(y, inv_row, w, out, dims->T, dims->d, dims->top_k, status_word(ws), s));
   if (st != MOE_OK) return st;
   return mark(5, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status_t moe_forward_ex(const moe_dims_t* dims, const moe_bf16_t* x, const float* w_r, const float* sel_bias,
+                            const moe_expert_weights_t* weights, moe_bf16_t* out, int32_t* topk_idx, int32_t* counts,
+                            void* ws, size_t ws_bytes, void* stream) {
+  return forward_impl(dims, x, w_r, sel_bias, weights, out, nullptr, topk_idx, counts, ws, ws_bytes, stream);
+}
+
+moe_status_t moe_forward_residual(const moe_dims_t* dims, const moe_bf16_t* x, const float* w_r, const float* sel_bias,
+                                  const moe_expert_weights_t* weights, const moe_bf16_t* norm_gain, float eps,
+                                  int32_t step, moe_bf16_t* resid, int32_t* topk_idx, int32_t* counts, void* ws,
+                                  size_t ws_bytes, void* stream) {
+  const ResidualArgs res{norm_gain, eps, step, resid};
+  return forward_impl(dims, x, w_r, sel_bias, weights, nullptr, &res, topk_idx, counts, ws, ws_bytes, stream);
+}
+
+moe_status_t moe_combine_residual(const moe_dims_t* dims, const moe_bf16_t* y_perm, const int32_t* inv_row,
+                                  const float* topk_w, const moe_bf16_t* norm_gain, float eps, int32_t step,
+                                  moe_bf16_t* resid, void* ws, size_t ws_bytes, void* stream) {
+  moe_status_t st = check_dims(dims);
+  if (st != MOE_OK) return st;
+  if (dims->T == 0) return MOE_OK;
+  if (!aligned16(y_perm) || !inv_row || !topk_w || !aligned16(norm_gain) || !aligned16(resid) || step < 1 ||
+      !(eps >= 0.0f))
+    return MOE_ERR_INVALID_ARG;
+  if (dims->d > 8192) return MOE_ERR_UNSUPPORTED;
+  if (ws && ws_bytes < sizeof(WsHeader)) return MOE_ERR_WORKSPACE;
+  return cuda_status(launch_combine_residual(y_perm, inv_row, topk_w, norm_gain, eps, step, resid, dims->T, dims->d,
+                                             dims->top_k, status_word(ws), static_cast<cudaStream_t>(stream)));
 }
 
 // ---------------------------------------------------------------- dense SwiGLU MLP

@@ -77,6 +77,12 @@ cudaError_t launch_expert_ffn(const ExpertPlan& plan, const ExpertBuffers& buf, 
                               cudaStream_t stream, int* cu_error, cudaEvent_t after_gemm1 = nullptr);
 
 // ---- combine (combine.cu) ----
+// combine + post-norm (RMSNorm, gain [d]) + depth-scaled residual update of
+// resid [T][d] in place at step `step` (>= 1); d <= 8192 (one cluster of
+// <= 8 blocks per row).
+cudaError_t launch_combine_residual(const uint16_t* y_perm, const int32_t* inv_row, const float* topk_w,
+                                    const uint16_t* gain, float eps, int step, uint16_t* resid, int T, int d,
+                                    int top_k, int32_t* status, cudaStream_t stream);
 cudaError_t launch_combine(const uint16_t* y_perm, const int32_t* inv_row, const float* topk_w, uint16_t* out,
                            int T, int d, int top_k, int32_t* status, cudaStream_t stream);
 

@@ -394,3 +394,52 @@ def test_forward_full_size(name, beam_weights):
         c = counts.cpu().numpy()
         ratio = c[list(cfg.hot_experts)].mean() / (cfg.T * cfg.top_k / cfg.E)
         assert 3.5 < ratio < 4.5
+
+
+# ---------------------------------------------------------------------------------------- residual
+
+@pytest.mark.parametrize("T,K,d,step", [(33, 8, 5120, 2), (64, 4, 128, 1), (5, 8, 5120, 37), (1, 20, 192, 3)])
+def test_combine_residual_parity(T, K, d, step):
+    """Combine + RMSNorm post-norm + depth-scaled residual update (release article, section
+    "Residual stream"), against the oracle's exact combine and residual update."""
+    E = max(K, 16)
+    idx_h = W.random_topk(41, T, E, K)
+    _, _, _, inv_row_h = O.permute(idx_h, E)
+    y_h = W.normal_bf16(41, W.TID_AUX, 0, T * K * d, 1.0).reshape(T * K, d)
+    w_h = (2.5 * W.uniform_f64(41, W.TID_AUX + 1, 0, T * K)).astype(np.float32).reshape(T, K)
+    gain_h = W.normal_bf16(41, W.TID_AUX + 2, 0, d, 0.1)
+    gain_h = (W.bf16_to_f32(gain_h) + 1.0).astype(np.float32)
+    gain_bits = torch.from_numpy(gain_h).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    h_old = W.normal_bf16(41, W.TID_AUX + 3, 0, T * d, 1.0).reshape(T, d)
+    dims = bm.Dims(T, d, E, 1, 1, K, 64)
+    resid = dev(h_old)
+    bm.moe_combine_residual(dims, dev(y_h), dev(inv_row_h), dev(w_h), dev(gain_bits), 1e-6, step, resid)
+    torch.cuda.synchronize()
+    out = O.combine(W.bf16_to_f32(y_h), inv_row_h, w_h.astype(np.float64))
+    ref = O.residual_update(out, h_old, gain_bits, 1e-6, step)
+    check_output(host_bits(resid), ref, TOL_BF16)
+    # the only roundings: FP32 combine and norm, and the bf16 result (<= 2^-9 relative)
+    err = np.abs(bf16_to_f64(host_bits(resid)) - ref)
+    assert np.all(err <= 2.0 ** -8 * np.abs(ref) + 1e-5 * np.sqrt(np.mean(ref ** 2)))
+
+
+def test_forward_residual_parity():
+    cfg = TINY.with_tokens(80)
+    inp = W.make_host_inputs(cfg, 27)
+    dw = DeviceWeights(cfg, 27)
+    dims = bm.Dims.from_config(cfg)
+    ws = bm.allocate_workspace(dims)
+    h_old = W.normal_bf16(27, W.TID_AUX + 3, 0, cfg.T * cfg.d, 1.0).reshape(cfg.T, cfg.d)
+    gain_bits = W.normal_bf16(27, W.TID_AUX + 2, 0, cfg.d, 0.05)
+    gain_bits = torch.from_numpy(W.bf16_to_f32(gain_bits) + 1.0).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    resid = dev(h_old)
+    idx = torch.empty((cfg.T, cfg.top_k), dtype=torch.int32, device="cuda")
+    bm.moe_forward_residual(dims, dev(inp["x"]), dev(inp["w_r"]), dw.dev, dev(gain_bits), 1e-6, 7, resid, ws,
+                            topk_idx=idx)
+    torch.cuda.synchronize()
+    assert bm.moe_get_device_status(ws) == bm.MOE_DEV_OK
+    orc = O.route(cfg, inp["x"], inp["w_r"])
+    _, ref_idx, ref_w = compare_routing_idx_only(cfg, idx.cpu().numpy(), orc)
+    out = O.forward_tokens(cfg, inp["x"], ref_idx, ref_w, np.arange(cfg.T), dw.host)
+    ref = O.residual_update(out, h_old, gain_bits, 1e-6, 7)
+    check_output(host_bits(resid), ref, TOL_BF16)
