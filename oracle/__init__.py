@@ -20,7 +20,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
 
-WFMT = {"bf16": 0, "nvfp4": 1}
+WFMT = {"bf16": 0, "nvfp4": 1, "fp8": 2}
 
 
 def build(force: bool = False, src: str = _SRC, out: str = _LIB) -> str:
@@ -138,6 +138,9 @@ def permute(idx, E, L=None):
 def _wargs(weights, wfmt):
     if wfmt == "bf16":
         return [_p(weights["gate"]), _p(weights["up"]), _p(weights["down"]), None, None, None, None, None, None]
+    if wfmt == "fp8":  # e4m3 codes and fp32 128 x 128 block scales
+        return [_p(weights["gate"]), _p(weights["up"]), _p(weights["down"]),
+                _p(weights["gate_sf"]), _p(weights["up_sf"]), _p(weights["down_sf"]), None, None, None]
     return [_p(weights["gate"]), _p(weights["up"]), _p(weights["down"]),
             _p(weights["gate_sf"]), _p(weights["up_sf"]), _p(weights["down_sf"]),
             _p(weights["gate_ts"]), _p(weights["up_ts"]), _p(weights["down_ts"])]

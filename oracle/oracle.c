@@ -80,14 +80,14 @@ double oracle_e4m3_value(int code) {
 
 /* ---------------- weights ---------------- */
 
-enum { WFMT_BF16 = 0, WFMT_NVFP4 = 1 };
+enum { WFMT_BF16 = 0, WFMT_NVFP4 = 1, WFMT_FP8 = 2 };
 
 typedef struct {
   int fmt;
   const uint16_t* bf16;  /* [E][N][K] */
-  const uint8_t* packed; /* [E][N][K/2] */
-  const uint8_t* sf;     /* [E][N][K/16] */
-  const float* ts;       /* [E] */
+  const uint8_t* packed; /* NVFP4 [E][N][K/2]; FP8 [E][N][K] e4m3 codes */
+  const uint8_t* sf;     /* NVFP4 [E][N][K/16] e4m3; FP8: fp32 [E][N/128][K/128] */
+  const float* ts;       /* [E] (NVFP4) */
   int64_t N, K;
 } wmat;
 
@@ -95,6 +95,13 @@ typedef struct {
 static double wmat_at(const wmat* w, int e, int64_t n, int64_t k) {
   const int64_t row = (int64_t)e * w->N + n;
   if (w->fmt == WFMT_BF16) return bf16_value(w->bf16[row * w->K + k]);
+  if (w->fmt == WFMT_FP8) {
+    /* e4m3 code times the fp32 scale of its 128 x 128 block (DeepSeek-V3's FP8 layout) */
+    const float* bs = (const float*)w->sf;
+    const int64_t nbn = w->N / 128, nbk = w->K / 128;
+    return oracle_e4m3_value(w->packed[row * w->K + k]) *
+           (double)bs[((int64_t)e * nbn + n / 128) * nbk + k / 128];
+  }
   const uint8_t byte = w->packed[row * (w->K / 2) + k / 2];
   const int nib = (k & 1) ? (byte >> 4) : (byte & 15);
   return oracle_e2m1_value(nib) * oracle_e4m3_value(w->sf[row * (w->K / 16) + k / 16]) *

@@ -303,6 +303,39 @@ def check_nvfp4_ffn(L):
         assert np.max(np.abs(y[r] - yr)) <= 1e-3 * np.sqrt((yr ** 2).mean())
 
 
+def check_fp8_ffn(L):
+    """The FP8 expert MLP equals a dense float64 MLP on weights dequantised with torch's own
+    float8 e4m3 decoding times each 128 x 128 block's scale. Each block of the seeded weights is
+    scaled by its own factor first, so every block scale differs and a wrong block index shows."""
+    cfg = W.MoEConfig("q8", T=12, d=256, E=2, n_groups=1, topk_groups=1, top_k=1, inter=256, wfmt="fp8")
+    x = W.gen_x(cfg, 7)
+    q, deq = {}, {}
+    factor = np.array([[1.0, 2.0], [3.0, 5.0]], np.float32)
+    for which in ("gate", "up", "down"):
+        N, K = W.weight_shape(cfg, which)
+        codes = np.empty((2, N, K), np.uint8)
+        scales = np.empty((2, N // 128, K // 128), np.float32)
+        for e in range(2):
+            w = _f(W.gen_expert_bf16(cfg, 7, which, e, e + 1)[0]).astype(np.float32)
+            w *= np.repeat(np.repeat(factor * (e + 1), 128, 0), 128, 1)
+            codes[e], scales[e] = W.quantize_fp8(_bf16_bits(w))
+        assert np.unique(scales).size == scales.size
+        q[which], q[which + "_sf"] = codes, scales
+        vals = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+        deq[which] = vals * np.repeat(np.repeat(scales.astype(np.float64), 128, 1), 128, 2)
+    rows = np.array([0, 1] * 6, np.int32)
+    y, h = O.ffn_rows(rows, x, q, cfg.d, cfg.inter, "fp8", want_h=True, L=L)
+    xf = _f(x)
+    for r in range(12):
+        e = rows[r]
+        g = (xf[r] @ deq["gate"][e].T).astype(np.float32)
+        u = (xf[r] @ deq["up"][e].T).astype(np.float32)
+        silu = (g.astype(np.float64) * expit(g.astype(np.float64))).astype(np.float32)
+        hr = _f(_bf16_bits(silu * u))
+        yr = hr @ deq["down"][e].T
+        assert np.max(np.abs(y[r] - yr)) <= 1e-3 * np.sqrt((yr ** 2).mean())
+
+
 def _bf16_const(v, n):
     return _bf16_bits(np.full(n, v, np.float32))
 
@@ -354,7 +387,8 @@ def check_residual_constant_scale(L):
 CHECKS = [check_uniform_scores, check_router_logits, check_select_bruteforce, check_select_bias,
           check_select_invariants,
           check_single_expert_dense, check_identical_experts, check_permute, check_combine,
-          check_forward_matches_stages, check_nvfp4_decode, check_nvfp4_ffn, check_residual_step1_normalises,
+          check_forward_matches_stages, check_nvfp4_decode, check_nvfp4_ffn, check_fp8_ffn,
+          check_residual_step1_normalises,
           check_residual_equal_weights, check_residual_constant_scale]
 
 
@@ -403,6 +437,8 @@ MUTANTS = {
     "residual_keep_on_output": ("keep * bf16_value(h_old", "add * bf16_value(h_old"),
     "rms_sum_not_mean": ("sqrt(ss / d + eps)", "sqrt(ss + eps)"),
     "post_norm_no_gain": (" * bf16_value(gamma[c]))", ")"),
+    "fp8_block_transposed": ("bs[((int64_t)e * nbn + n / 128) * nbk + k / 128]",
+                             "bs[((int64_t)e * nbn + k / 128) * nbk + n / 128]"),
     "no_group_limit": ("if (kept[e / gsz] && !taken[e] && (best < 0", "if (!taken[e] && (best < 0"),
     "h_not_rounded": ("hbuf[i] = bf16_value(hb);", "hbuf[i] = (double)(silu * uf);"),
     "down_transposed": ("acc += hbuf[i] * wmat_at(down, e, n, i);", "acc += hbuf[i] * wmat_at(down, e, i % d, n % I);"),

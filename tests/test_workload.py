@@ -64,3 +64,20 @@ def test_skew_beta_reproduces_target(wl, olib):
         counts = np.bincount(r["idx"].ravel(), minlength=cfg.E)
         ratio = counts[list(cfg.hot_experts)].mean() / (1024 * cfg.top_k / cfg.E)
         assert 3.6 < ratio < 4.4, ratio
+
+
+def test_fp8_quantiser_round_trip():
+    """FP8 with 128 x 128 block scales: every block scale is amax/448 (fp32), and every weight,
+    decoded with torch's float8 e4m3 type, is within half an e4m3 step of the bf16 original
+    (3 mantissa bits: 2^-4 relative for normal codes, 2^-10 * scale below)."""
+    import torch
+    cfg = W.MoEConfig("q8", T=4, d=256, E=1, n_groups=1, topk_groups=1, top_k=1, inter=384, wfmt="fp8")
+    w = W.gen_expert_bf16(cfg, 3, "gate", 0, 1)[0]
+    codes, scales = W.quantize_fp8(w)
+    wf = W.bf16_to_f32(w).astype(np.float64)
+    amax = np.abs(wf).reshape(3, 128, 2, 128).max(axis=(1, 3))
+    assert np.array_equal(scales, (amax / 448.0).astype(np.float32))
+    s = np.repeat(np.repeat(scales.astype(np.float64), 128, 0), 128, 1)
+    deq = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy() * s
+    assert np.all(np.abs(deq - wf) <= np.maximum(np.abs(wf) * 2.0 ** -4, 2.0 ** -10 * s) * (1 + 1e-12))
+    assert np.all(np.abs(deq) <= np.abs(wf).max() * (1 + 2.0 ** -4))

@@ -50,7 +50,7 @@ class MoEConfig:
     top_k: int
     inter: int
     routed_scale: float = 2.5
-    wfmt: str = "bf16"  # "bf16" | "nvfp4"
+    wfmt: str = "bf16"  # "bf16" | "nvfp4" | "fp8"
     skew: bool = False
     hot_experts: tuple = field(default_factory=tuple)
 
@@ -108,6 +108,8 @@ def lib():
         L.gen_random_topk.argtypes = [u64, u64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                       dbl, vp]
         L.gen_quantize_nvfp4.argtypes = [vp, i64, i64, vp, vp]
+        L.gen_quantize_fp8.argtypes = [vp, i64, i64, vp, vp]
+        L.gen_quantize_fp8.restype = None
         L.gen_quantize_nvfp4.restype = ctypes.c_float
         _lib = L
     return _lib
@@ -244,12 +246,41 @@ def gen_expert_nvfp4(cfg: MoEConfig, seed: int, which: str, e0: int, e1: int):
     return packed, scales, ts
 
 
+def quantize_fp8(w: np.ndarray):
+    """FP8 encoding of one bf16 matrix w [N, K] (uint16 bits), 128 x 128 block scales.
+
+    Returns (codes [N, K] uint8 e4m3, scales [N/128, K/128] float32).
+    s = amax_block / 448; q = e4m3(w / s), round to nearest even, saturating.
+    """
+    N, K = w.shape
+    assert N % 128 == 0 and K % 128 == 0
+    w = np.ascontiguousarray(w)
+    codes = np.empty((N, K), np.uint8)
+    scales = np.empty((N // 128, K // 128), np.float32)
+    lib().gen_quantize_fp8(_ptr(w), N, K, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def gen_expert_fp8(cfg: MoEConfig, seed: int, which: str, e0: int, e1: int):
+    """FP8 encodings of experts [e0, e1): (codes [n,N,K], scales [n,N/128,K/128] f32)."""
+    N, K = weight_shape(cfg, which)
+    n = e1 - e0
+    codes = np.empty((n, N, K), np.uint8)
+    scales = np.empty((n, N // 128, K // 128), np.float32)
+    for i in range(n):
+        w = gen_expert_bf16(cfg, seed, which, e0 + i, e0 + i + 1)[0]
+        codes[i], scales[i] = quantize_fp8(w)
+    return codes, scales
+
+
 def make_host_inputs(cfg: MoEConfig, seed: int = 0):
     """All inputs of a (small) configuration as host numpy arrays."""
     out = {"x": gen_x(cfg, seed), "w_r": gen_wr(cfg, seed)}
     for which in ("gate", "up", "down"):
         if cfg.wfmt == "bf16":
             out[which] = gen_expert_bf16(cfg, seed, which, 0, cfg.E)
+        elif cfg.wfmt == "fp8":
+            out[which], out[which + "_sf"] = gen_expert_fp8(cfg, seed, which, 0, cfg.E)
         else:
             p, s, t = gen_expert_nvfp4(cfg, seed, which, 0, cfg.E)
             out[which], out[which + "_sf"], out[which + "_ts"] = p, s, t

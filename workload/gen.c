@@ -180,6 +180,36 @@ static inline double bf16_to_f64(uint16_t b) {
   return (double)f;
 }
 
+/* Quantise one [N][K] bf16 matrix to FP8 with 128 x 128 block scales (the
+ * layout of DeepSeek-V3's FP8 checkpoints; the article's router follows that
+ * model and names FP8 checkpoints for Hopper-class GPUs):
+ *   block scale  s = amax_block / 448   (fp32; 0 for an all-zero block)
+ *   value        q = e4m3(w / s)        (round to nearest even, saturating)
+ * codes[n][k]: e4m3 byte (bit 7 = sign). scales[n/128][k/128]: fp32.
+ * N and K must be multiples of 128. */
+void gen_quantize_fp8(const uint16_t* w, int64_t N, int64_t K, uint8_t* codes, float* scales) {
+  const int64_t nbn = N / 128, nbk = K / 128;
+#pragma omp parallel for collapse(2) schedule(static)
+  for (int64_t bn = 0; bn < nbn; ++bn)
+    for (int64_t bk = 0; bk < nbk; ++bk) {
+      double amax = 0.0;
+      for (int64_t n = bn * 128; n < bn * 128 + 128; ++n)
+        for (int64_t k = bk * 128; k < bk * 128 + 128; ++k) {
+          const double a = fabs(bf16_to_f64(w[n * K + k]));
+          if (a > amax) amax = a;
+        }
+      const float sc = (float)(amax / 448.0);
+      scales[bn * nbk + bk] = sc;
+      for (int64_t n = bn * 128; n < bn * 128 + 128; ++n)
+        for (int64_t k = bk * 128; k < bk * 128 + 128; ++k) {
+          const double v = bf16_to_f64(w[n * K + k]);
+          uint8_t code = 0;
+          if (sc > 0.0f) code = e4m3_code_rne(fabs(v) / (double)sc);
+          codes[n * K + k] = (uint8_t)(code | ((v < 0.0 && code != 0) ? 0x80 : 0));
+        }
+    }
+}
+
 /* Quantise one [N][K] bf16 matrix to NVFP4:
  *   tensor scale  s_t = amax / (6 * 448)
  *   block scale   s_b = e4m3(amax_block / (6 * s_t))       (16 values along K)
