@@ -87,6 +87,9 @@ PROFILE_CASES = {
     # the NVFP4 prefill shape with 32 experts (0.7 GB of NVFP4 weights)
     "profile_nvfp4": W.MoEConfig("profile_nvfp4", T=512, d=5120, E=32, n_groups=8, topk_groups=4, top_k=8,
                                  inter=2560, wfmt="nvfp4"),
+    # the FP8 prefill shape with 32 experts (1.3 GB of FP8 weights)
+    "profile_fp8": W.MoEConfig("profile_fp8", T=512, d=5120, E=32, n_groups=8, topk_groups=4, top_k=8,
+                               inter=2560, wfmt="fp8"),
 }
 
 # Dense SwiGLU MLP of the first decoder layers. The pages give no intermediate size for them;
@@ -98,8 +101,9 @@ DENSE_CASES = {
 
 RESIDUAL_STEP = 10  # the residual-addition index k used with --residual (weights sqrt(9/10), 1/sqrt(10))
 
-DEFAULT_STEPS = {"dense_prefill": 100, "decode": 300, "prefill": 200, "skewed": 40, "nvfp4": 200, "profile_decode": 20,
-                 "profile_prefill": 20, "profile_dense": 20, "profile_nvfp4": 20}
+DEFAULT_STEPS = {"dense_prefill": 100, "decode": 300, "prefill": 200, "skewed": 40, "nvfp4": 200, "fp8": 200,
+                 "profile_decode": 20, "profile_prefill": 20, "profile_dense": 20, "profile_nvfp4": 20,
+                 "profile_fp8": 20}
 
 
 def workload_cfg(name):
@@ -216,10 +220,18 @@ class ClockSampler:
 
 def make_device_weights(cfg, seed, torch, keep_host):
     """Seeded expert weights generated expert by expert on the host and copied to the device
-    (NVFP4: quantised from the same seeded bf16 draws)."""
+    (NVFP4, FP8: quantised from the same seeded bf16 draws)."""
     import sparse_moe_layer_14_b300 as bm
     host = {}
     tens = {}
+    if cfg.wfmt == "fp8":
+        for which in ("gate", "up", "down"):
+            codes, scales = W.gen_expert_fp8(cfg, seed, which, 0, cfg.E)
+            tens[which] = torch.from_numpy(codes).cuda()
+            tens[which + "_sf"] = torch.from_numpy(scales).cuda()
+            if keep_host:
+                host[which], host[which + "_sf"] = codes, scales
+        return bm.ExpertWeights(**tens), host
     if cfg.wfmt == "nvfp4":
         for which in ("gate", "up", "down"):
             p, s, ts = W.gen_expert_nvfp4(cfg, seed, which, 0, cfg.E)
@@ -249,8 +261,9 @@ def make_device_weights(cfg, seed, torch, keep_host):
 
 
 def weight_bytes_per_param(cfg):
-    """bf16: 2 B; NVFP4: 0.5 B of e2m1 code + 1/16 B of e4m3 block scale."""
-    return 2.0 if cfg.wfmt == "bf16" else 0.5 + 1.0 / 16
+    """bf16: 2 B; NVFP4: 0.5 B of e2m1 code + 1/16 B of e4m3 block scale; FP8: 1 B of e4m3
+    code + 4 B of fp32 scale per 128 x 128 block."""
+    return {"bf16": 2.0, "nvfp4": 0.5 + 1.0 / 16, "fp8": 1.0 + 4.0 / (128 * 128)}[cfg.wfmt]
 
 
 def roofline_numbers(cfg, touched, peaks):
@@ -407,12 +420,13 @@ def run_ours(args, rank, world, local_rank):
         achieved, peak, unit = g1["bytes"] / gemm1_s / 1e9, peaks["hbm_gbs"], "GB/s"
     else:
         achieved, peak, unit = g1["flops"] / gemm1_s / 1e12, peaks["bf16_tflops"], "TFLOP/s"
-    kname = "expert_gemm_kernel<GLU>" if cfg.wfmt == "bf16" else "expert_gemm_kernel<GLU, NVFP4>"
+    kname = {"bf16": "expert_gemm_kernel<GLU>", "nvfp4": "expert_gemm_kernel<GLU, NVFP4>",
+             "fp8": "expert_gemm_kernel<GLU, FP8>"}[cfg.wfmt]
     traffic, traffic_src = profiled_traffic(cfg.name, kname, g1["bytes"])
     line = {
         "metric": METRIC, "value": round(tokens_per_s, 1), "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16" if cfg.wfmt == "bf16" else "bf16 (NVFP4 weights decoded to bf16)", "data": "synthetic (seeded N(0,1) activations, N(0,1/fan_in) weights)",
+        "vs_baseline": None, "dtype": "bf16" if cfg.wfmt == "bf16" else f"bf16 ({cfg.wfmt.upper()} weights decoded to bf16)", "data": "synthetic (seeded N(0,1) activations, N(0,1/fan_in) weights)",
         "impl": "ours",
         "config": {"workload": describe(cfg), "T": cfg.T, "d": cfg.d, "E": cfg.E, "inter": cfg.inter,
                    "top_k": cfg.top_k, "parallelism": f"replicas x{world}",

@@ -33,6 +33,10 @@
  *    nibble bit 3 = sign), e4m3 block scales [E][N][K/16] (one per 16
  *    consecutive k), one fp32 tensor scale per expert and matrix; the weight
  *    is e2m1 * e4m3 * tensor_scale.
+ *  - FP8 weights (DeepSeek-V3's block-scaled layout): e4m3 codes [E][N][K]
+ *    (one byte per weight), fp32 scales [E][N/128][K/128] (one per 128 x 128
+ *    block of each expert's matrix); the weight is e4m3 * block scale. N and K
+ *    (d and inter) must be multiples of 128.
  *  - Routing order: slots of a token are in descending score order, ties to
  *    the lower expert index; within an expert, permuted rows are ordered by
  *    ascending token.
@@ -70,7 +74,7 @@ typedef enum {
   MOE_DEV_ZERO_SUM = 7     /* a token's chosen scores summed to 0: its weights are set to 0 */
 } moe_device_code_t;
 
-typedef enum { MOE_W_BF16 = 0, MOE_W_NVFP4 = 1 } moe_wfmt_t;
+typedef enum { MOE_W_BF16 = 0, MOE_W_NVFP4 = 1, MOE_W_FP8 = 2 } moe_wfmt_t;
 
 /* Block shape. Beam: d=5120, E=256, n_groups=8, topk_groups=4, top_k=8,
  * inter=2560, routed_scale=2.5 (release article, "Mixture of Experts").
@@ -90,16 +94,19 @@ typedef struct {
   int32_t wfmt; /* moe_wfmt_t */
 } moe_dims_t;
 
-/* Expert weights (device pointers). For MOE_W_BF16 only gate/up/down are read
- * (bf16, layouts above). For MOE_W_NVFP4 gate/up/down are the packed e2m1
- * codes and the *_sf / *_ts fields are required. */
+/* Expert weights (device pointers, 16-byte aligned). For MOE_W_BF16 only
+ * gate/up/down are read (bf16, layouts above). For MOE_W_NVFP4 gate/up/down
+ * are the packed e2m1 codes and the *_sf (e4m3 bytes) and *_ts fields are
+ * required. For MOE_W_FP8 gate/up/down are the e4m3 codes and *_sf point at
+ * the fp32 block scales (4-byte aligned); *_ts are ignored. The caller owns
+ * all of them; calls only read them. */
 typedef struct {
   const void* gate;
   const void* up;
   const void* down;
-  const uint8_t* gate_sf;
-  const uint8_t* up_sf;
-  const uint8_t* down_sf;
+  const void* gate_sf;
+  const void* up_sf;
+  const void* down_sf;
   const float* gate_ts;
   const float* up_ts;
   const float* down_ts;
@@ -141,7 +148,9 @@ moe_status_t moe_permute(const moe_dims_t* dims, const moe_bf16_t* x, const int3
  * offsets[E] <= T*top_k), y_perm [T*top_k][d] bf16 (the expert output in the
  * model's dtype, rounded once from the FP32 accumulator). The GEMMs run on tcgen05
  * tensor cores with bf16 operands (NVFP4 weights are decoded to exact bf16
- * values on chip; the tensor scale is applied to the FP32 accumulator). */
+ * values on chip, the tensor scale applied to the FP32 accumulator; FP8
+ * weights are decoded on chip as bf16(e4m3 * block scale), the product in
+ * FP32, rounded once). */
 moe_status_t moe_expert_ffn(const moe_dims_t* dims, const moe_bf16_t* x_perm,
                             const int32_t* offsets, const moe_expert_weights_t* weights,
                             moe_bf16_t* y_perm, void* ws, size_t ws_bytes, void* stream);
@@ -231,7 +240,7 @@ moe_status_t moe_forward_residual(const moe_dims_t* dims, const moe_bf16_t* x, c
  * routed_scale are ignored. `w` holds one MLP in the expert layouts with E = 1
  * (gate, up [inter][d], down [d][inter]; NVFP4 as for the experts). x [T][d]
  * and out [T][d] bf16, 16-byte aligned; d a multiple of 64 up to 16384, inter
- * a multiple of 64 up to 65536 (NVFP4: both multiples of 256). The workspace
+ * a multiple of 64 up to 65536 (NVFP4: both multiples of 256; FP8: of 128). The workspace
  * (moe_dense_workspace_bytes bytes, 256-byte aligned, header zeroed by
  * moe_workspace_init) holds the work items and h [T][inter]. Host-side errors
  * return before any launch; device codes latch in the workspace header. */

@@ -21,7 +21,7 @@ import torch
 
 from . import _native as N
 from ._native import (MOE_DEV_BAD_EXPERT, MOE_DEV_BAD_ROW, MOE_DEV_OK, MOE_DEV_TIMEOUT,  # noqa: F401
-                      MOE_DEV_ZERO_SUM, MOE_W_BF16, MOE_W_NVFP4, MoeDims, MoeExpertWeights)
+                      MOE_DEV_ZERO_SUM, MOE_W_BF16, MOE_W_FP8, MOE_W_NVFP4, MoeDims, MoeExpertWeights)
 
 __all__ = ["MoEError", "Dims", "ExpertWeights", "moe_workspace_bytes", "moe_workspace_init", "moe_route",
            "moe_permute", "moe_permute_noalloc", "moe_expert_ffn", "moe_combine", "moe_forward", "moe_get_device_status",
@@ -51,7 +51,7 @@ class Dims:
     @staticmethod
     def from_config(cfg, T: int | None = None) -> "Dims":
         return Dims(cfg.T if T is None else T, cfg.d, cfg.E, cfg.n_groups, cfg.topk_groups, cfg.top_k, cfg.inter,
-                    cfg.routed_scale, MOE_W_NVFP4 if cfg.wfmt == "nvfp4" else MOE_W_BF16)
+                    cfg.routed_scale, _WFMT[cfg.wfmt])
 
     def c(self) -> MoeDims:
         return MoeDims(self.T, self.d, self.E, self.n_groups, self.topk_groups, self.top_k, self.inter,
@@ -61,7 +61,8 @@ class Dims:
 @dataclass
 class ExpertWeights:
     """Expert weights on the device. bf16: gate/up [E, inter, d], down [E, d, inter] (bf16 or int16 bits).
-    NVFP4: gate/up/down packed uint8 [E, N, K/2], *_sf uint8 [E, N, K/16], *_ts float32 [E]."""
+    NVFP4: gate/up/down packed uint8 [E, N, K/2], *_sf uint8 [E, N, K/16], *_ts float32 [E].
+    FP8: gate/up/down e4m3 codes uint8 [E, N, K], *_sf float32 [E, N/128, K/128] (block scales)."""
 
     gate: torch.Tensor
     up: torch.Tensor
@@ -119,6 +120,7 @@ def _expect(t, dtypes, shape, name):
 
 
 _BF16 = (torch.bfloat16, torch.int16)
+_WFMT = {"bf16": MOE_W_BF16, "nvfp4": MOE_W_NVFP4, "fp8": MOE_W_FP8}
 
 
 def moe_workspace_bytes(dims: Dims) -> int:
@@ -191,6 +193,12 @@ def _check_weights(dims: Dims, w: ExpertWeights):
         _expect(w.gate, _BF16, (dims.E, dims.inter, dims.d), "gate")
         _expect(w.up, _BF16, (dims.E, dims.inter, dims.d), "up")
         _expect(w.down, _BF16, (dims.E, dims.d, dims.inter), "down")
+    elif dims.wfmt == MOE_W_FP8:
+        for name, n, k in (("gate", dims.inter, dims.d), ("up", dims.inter, dims.d), ("down", dims.d, dims.inter)):
+            _expect(getattr(w, name), (torch.uint8,), (dims.E, n, k), name)
+            _expect(getattr(w, name + "_sf"), (torch.float32,), (dims.E, n // 128, k // 128), name + "_sf")
+            if getattr(w, name + "_sf") is None:
+                raise ValueError(f"FP8 weights need {name}_sf")
     else:
         for name, n, k in (("gate", dims.inter, dims.d), ("up", dims.inter, dims.d), ("down", dims.d, dims.inter)):
             _expect(getattr(w, name), (torch.uint8,), (dims.E, n, k // 2), name)

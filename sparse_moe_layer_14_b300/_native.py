@@ -16,7 +16,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 # moe_device_code_t
 MOE_DEV_OK, MOE_DEV_BAD_EXPERT, MOE_DEV_BAD_ROW, MOE_DEV_TIMEOUT, MOE_DEV_ZERO_SUM = 0, 1, 2, 6, 7
 # moe_wfmt_t
-MOE_W_BF16, MOE_W_NVFP4 = 0, 1
+MOE_W_BF16, MOE_W_NVFP4, MOE_W_FP8 = 0, 1, 2
 
 EXPORTS = ["moe_workspace_bytes", "moe_workspace_init", "moe_route", "moe_permute", "moe_expert_ffn",
            "moe_combine", "moe_forward", "moe_get_device_status", "moe_set_wait_bound", "moe_set_stage_events",

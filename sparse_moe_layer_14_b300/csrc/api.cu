@@ -46,7 +46,7 @@ Layout make_layout(const moe_dims_t& d) {
                               router_uses_tensor_cores(d.T, d.E, d.d)
                                   ? std::max(kRouterFlagSplits, router_tc_splits(Tc, d.d, kMaxSmsForLayout))
                                   : 1);
-  const ExpertPlan pl = plan_experts(d.T, d.d, d.E, d.top_k, d.inter, d.wfmt == MOE_W_NVFP4);
+  const ExpertPlan pl = plan_experts(d.T, d.d, d.E, d.top_k, d.inter, d.wfmt != MOE_W_BF16);
   const int64_t nw = bitmap_words(d.T);
   size_t sz[R_NUM];
   sz[R_HDR] = sizeof(WsHeader);
@@ -87,7 +87,7 @@ moe_status_t check_dims(const moe_dims_t* d) {
     return MOE_ERR_INVALID_ARG;
   if (d->E % d->n_groups != 0 || d->topk_groups > d->n_groups || d->top_k > d->topk_groups * (d->E / d->n_groups))
     return MOE_ERR_INVALID_ARG;
-  if (d->wfmt != MOE_W_BF16 && d->wfmt != MOE_W_NVFP4) return MOE_ERR_INVALID_ARG;
+  if (d->wfmt != MOE_W_BF16 && d->wfmt != MOE_W_NVFP4 && d->wfmt != MOE_W_FP8) return MOE_ERR_INVALID_ARG;
   if (d->T > 4194304 || d->d % 64 || d->inter % 64 || d->d > 16384 || d->inter > 16384 || d->E > 256 ||
       d->n_groups > 32 || d->top_k > 32)
     return MOE_ERR_UNSUPPORTED;
@@ -108,6 +108,10 @@ moe_status_t check_weights(const moe_dims_t* d, const moe_expert_weights_t* w) {
     if (!aligned16(w->gate_sf) || !aligned16(w->up_sf) || !aligned16(w->down_sf) || !w->gate_ts || !w->up_ts ||
         !w->down_ts)
       return MOE_ERR_INVALID_ARG;
+  }
+  if (d->wfmt == MOE_W_FP8) {
+    const auto aligned4 = [](const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 3u) == 0; };
+    if (!aligned4(w->gate_sf) || !aligned4(w->up_sf) || !aligned4(w->down_sf)) return MOE_ERR_INVALID_ARG;
   }
   return MOE_OK;
 }
@@ -170,7 +174,7 @@ ExpertWeightsDev weights_dev(int wfmt, const moe_expert_weights_t* w) {
 moe_status_t do_ffn(const moe_dims_t* d, const uint16_t* x_perm, const int32_t* offsets,
                     const moe_expert_weights_t* w, uint16_t* y, void* ws, const Layout& L, cudaStream_t s,
                     cudaEvent_t after_gemm1 = nullptr) {
-  const ExpertPlan pl = plan_experts(d->T, d->d, d->E, d->top_k, d->inter, d->wfmt == MOE_W_NVFP4);
+  const ExpertPlan pl = plan_experts(d->T, d->d, d->E, d->top_k, d->inter, d->wfmt != MOE_W_BF16);
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
   ExpertBuffers b;
   b.x_perm = x_perm;
@@ -359,7 +363,7 @@ moe_dims_t dense_dims(const moe_dims_t& d) {
 moe_status_t check_dense_dims(const moe_dims_t* d) {
   if (!d) return MOE_ERR_INVALID_ARG;
   if (d->T < 0 || d->d <= 0 || d->inter <= 0) return MOE_ERR_INVALID_ARG;
-  if (d->wfmt != MOE_W_BF16 && d->wfmt != MOE_W_NVFP4) return MOE_ERR_INVALID_ARG;
+  if (d->wfmt != MOE_W_BF16 && d->wfmt != MOE_W_NVFP4 && d->wfmt != MOE_W_FP8) return MOE_ERR_INVALID_ARG;
   if (d->T > 4194304 || d->d % 64 || d->inter % 64 || d->d > 16384 || d->inter > 65536) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
@@ -369,7 +373,7 @@ struct DenseLayout {
 };
 
 DenseLayout make_dense_layout(const moe_dims_t& d) {
-  const ExpertPlan pl = plan_experts(d.T, d.d, 1, 1, d.inter, d.wfmt == MOE_W_NVFP4);
+  const ExpertPlan pl = plan_experts(d.T, d.d, 1, 1, d.inter, d.wfmt != MOE_W_BF16);
   DenseLayout L;
   size_t o = align_up(sizeof(WsHeader));
   L.offs = o;
@@ -451,7 +455,7 @@ moe_status_t moe_dense_mlp(const moe_dims_t* dims, const moe_bf16_t* x, const mo
   b.status = &hdr->status;
   b.timeout_where = &hdr->timeout_where;
   const ExpertWeightsDev wd = weights_dev(d1.wfmt, w);
-  const ExpertPlan pl = plan_experts(d1.T, d1.d, 1, 1, d1.inter, d1.wfmt == MOE_W_NVFP4);
+  const ExpertPlan pl = plan_experts(d1.T, d1.d, 1, 1, d1.inter, d1.wfmt != MOE_W_BF16);
   int cu_error = 0;
   const cudaError_t e = launch_expert_ffn(pl, b, wd, d1.T, d1.d, 1, 1, d1.inter, num_sms(), g_wait_spins, s,
                                           &cu_error, g_stage_events_on ? g_stage_events[3] : nullptr);

@@ -55,6 +55,10 @@ constexpr int kConvCols = 64;  // TMEM columns of one slot: two 128 x 64 bf16 ti
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kATileBytes = BM * BK * 2;            // 16 KB bf16 weight tile
 constexpr uint32_t kPTileBytes = BM * BK / 2;            // 4 KB packed e2m1 weight tile
+constexpr uint32_t kP8TileBytes = BM * BK;               // 8 KB e4m3 weight tile
+// Weight formats of the kernel (moe_wfmt_t values): bf16 straight from TMA into the
+// MMA; NVFP4 and FP8 through the converter warps into tensor memory.
+constexpr int kFmtBf16 = 0, kFmtNvfp4 = 1, kFmtFp8 = 2;
 constexpr uint32_t kTokBoxBytes = TOK_BOX * BK * 2;      // 2 KB
 constexpr uint64_t kDrainNs = 1000000000ull;             // 1 s bound for draining on abort
 constexpr uint64_t kWaitNs = 2000000000ull;              // 2 s bound of a pipeline wait
@@ -63,7 +67,7 @@ constexpr int kSmemLimit = 232448;                       // 227 KB opt-in per bl
 constexpr int kEpiThreads = 256;    // two epilogue warpgroups
 constexpr int kConvBase = 320;      // first converter thread (NVFP4)
 constexpr int kConvThreads = 256;   // one converter thread per row of each weight tile (NVFP4)
-constexpr int threads_for(bool w4) { return w4 ? kConvBase + kConvThreads : 320; }
+constexpr int threads_for(int fmt) { return fmt != kFmtBf16 ? kConvBase + kConvThreads : 320; }
 
 struct GemmArgs {
   const int4* items;
@@ -86,6 +90,8 @@ struct GemmArgs {
   const float* ts1;
   const uint8_t* sf0;  // e4m3 block scales [E*Nw][K/16] of matrix 0 (NVFP4)
   const uint8_t* sf1;
+  const float* fs0;    // fp32 block scales [E][Nw/128][K/128] of matrix 0 (FP8)
+  const float* fs1;
   int32_t* status;
   int32_t* timeout_where;
   long long wait_spins;
@@ -149,8 +155,34 @@ __device__ __forceinline__ void decode_row(const uint8_t* packed_tile, int r, ui
   }
 }
 
-template <bool kGLU, bool kW4>
-__global__ void __launch_bounds__(threads_for(kW4), 1)
+// Row r of one 128 x 64 FP8 weight tile (64 e4m3 codes, element k in byte k)
+// times the slice's fp32 block scale `s`, each product rounded once to bf16
+// (e4m3 -> f16 is exact; the product in fp32): 32 bf16x2 words in element
+// order, word c holding elements 2c (low half) and 2c+1.
+__device__ __forceinline__ uint32_t e4m3x2_scaled_bf16x2(uint32_t two, float s) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(static_cast<uint16_t>(two)));
+  const __half2 ph = *reinterpret_cast<const __half2*>(&h);
+  const __nv_bfloat162 b = __floats2bfloat162_rn(__low2float(ph) * s, __high2float(ph) * s);
+  return *reinterpret_cast<const uint32_t*>(&b);
+}
+
+__device__ __forceinline__ void decode_row_fp8(const uint8_t* packed_tile, int r, float s, uint32_t (&out)[32]) {
+  const uint4* row = reinterpret_cast<const uint4*>(packed_tile + r * 64);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 p = row[q];
+    const uint32_t w[4] = {p.x, p.y, p.z, p.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      out[8 * q + 2 * i] = e4m3x2_scaled_bf16x2(w[i] & 0xFFFFu, s);
+      out[8 * q + 2 * i + 1] = e4m3x2_scaled_bf16x2(w[i] >> 16, s);
+    }
+  }
+}
+
+template <bool kGLU, int kFmt>
+__global__ void __launch_bounds__(threads_for(kFmt), 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                        const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB64,
                        const __grid_constant__ CUtensorMap tmB128, const GemmArgs p) {
@@ -199,6 +231,9 @@ __global__ void __launch_bounds__(threads_for(kW4), 1)
   __syncthreads();
   tc_fence_after();
 
+  constexpr bool kConv = kFmt != kFmtBf16;    // weights decoded into tensor memory
+  constexpr bool kFp8 = kFmt == kFmtFp8;
+  constexpr uint32_t kPB = kFp8 ? kP8TileBytes : kPTileBytes;  // raw weight tile bytes (kConv)
   const uint32_t tmem_base = tmem_slot;
   const int n_items = *p.n_items;
   const int kblocks = p.K / BK;
@@ -217,7 +252,7 @@ __global__ void __launch_bounds__(threads_for(kW4), 1)
         const int4 item = p.items[it];
         const int a_row = item.x * p.Nw + item.y * kItemRows;
         const int nbox = (item.w + TOK_BOX - 1) / TOK_BOX;
-        const uint32_t bytes = (kW4 ? kPTileBytes : kATileBytes) * nA + static_cast<uint32_t>(nbox) * kTokBoxBytes;
+        const uint32_t bytes = (kConv ? kPB : kATileBytes) * nA + static_cast<uint32_t>(nbox) * kTokBoxBytes;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, p.wait_spins, kWaitNs, abort)) {
             if (!*abort) fail(p, abort, 1);
@@ -226,10 +261,11 @@ __global__ void __launch_bounds__(threads_for(kW4), 1)
           }
           uint8_t* st = smem + static_cast<size_t>(stage) * p.stage_bytes;
           mbar_arrive_expect_tx(&full_bar[stage], bytes);
-          if (kW4) {
-            // packed codes: 32 bytes (64 elements) per row
-            tma_load_2d(st + p.p_offset, &tmA0, kb * (BK / 2), a_row, &full_bar[stage]);
-            tma_load_2d(st + p.p_offset + kPTileBytes, &tmA1, kb * (BK / 2), a_row + kRow1, &full_bar[stage]);
+          if (kConv) {
+            // raw codes of one 64-element K slice: 32 bytes (e2m1) or 64 bytes (e4m3) per row
+            const int x0 = kb * static_cast<int>(kPB / BM);
+            tma_load_2d(st + p.p_offset, &tmA0, x0, a_row, &full_bar[stage]);
+            tma_load_2d(st + p.p_offset + kPB, &tmA1, x0, a_row + kRow1, &full_bar[stage]);
           } else {
             tma_load_2d(st, &tmA0, kb * BK, a_row, &full_bar[stage]);
             tma_load_2d(st + kATileBytes, &tmA1, kb * BK, a_row + kRow1, &full_bar[stage]);
@@ -274,8 +310,8 @@ __global__ void __launch_bounds__(threads_for(kW4), 1)
         const uint32_t d1 = d0 + static_cast<uint32_t>(p.n_max);
         bool ok = true;
         for (int kb = 0; kb < kblocks; ++kb) {
-          // NVFP4: the decoded slot is ready only after its raw stage landed
-          if (!mbar_wait_bounded(kW4 ? &conv_bar[cstage] : &full_bar[stage], kW4 ? cphase : phase, p.wait_spins,
+          // NVFP4 / FP8: the decoded slot is ready only after its raw stage landed
+          if (!mbar_wait_bounded(kConv ? &conv_bar[cstage] : &full_bar[stage], kConv ? cphase : phase, p.wait_spins,
                                  kWaitNs, abort)) {
             if (!*abort) fail(p, abort, 3);
             ok = false;
@@ -284,14 +320,14 @@ __global__ void __launch_bounds__(threads_for(kW4), 1)
           tc_fence_after();
           const uint32_t st_addr = smem_u32(smem + static_cast<size_t>(stage) * p.stage_bytes);
           const uint32_t sb = st_addr + p.b_offset;
-          // NVFP4: slot cstage holds tile 0 in columns [0, 32), tile 1 in [32, 64);
+          // NVFP4 / FP8: slot cstage holds tile 0 in columns [0, 32), tile 1 in [32, 64);
           // 8 columns per 16-wide K step
           const uint32_t ta = tmem_base + p.a_col + static_cast<uint32_t>(cstage * kConvCols);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
             const uint64_t bdesc = sdesc_kmajor_sw128(sb + k * 32);
             const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
-            if (kW4) {
+            if (kConv) {
               mma_bf16_ts(d0, ta + k * 8, bdesc, idesc, accum);
               mma_bf16_ts(d1, ta + kConvCols / 2 + k * 8, bdesc, idesc, accum);
             } else {
@@ -300,7 +336,7 @@ __global__ void __launch_bounds__(threads_for(kW4), 1)
             }
           }
           mma_commit(&empty_bar[stage]);
-          if (kW4) {
+          if (kConv) {
             mma_commit(&conv_empty_bar[cstage]);
             if (++cstage == p.conv_stages) {
               cstage = 0;
@@ -414,31 +450,46 @@ __global__ void __launch_bounds__(threads_for(kW4), 1)
         acc_phase ^= 1u;
       }
     }
-  } else if (kW4) {
-    // ------------------------------------------------------------ NVFP4 converters
+  } else if (kConv) {
+    // ------------------------------------------------------------ NVFP4 / FP8 converters
     // Warp 10 + 4t + j decodes weight tile t (gate/up, or the two down tiles)
     // for the 32 rows of the TMEM lane quarter it may access (warp % 4); one
-    // thread per row. Block scales (4 per slice per row) are read 16 bytes
-    // (four slices) at a time from global memory, one group ahead, so the load
-    // latency hides behind decoding.
+    // thread per row. Scales are read from global memory one group of four
+    // K slices ahead, so the load latency hides behind decoding:
+    //   NVFP4: 4 e4m3 block scales per slice per row, 16 bytes (four slices) a load;
+    //   FP8: one fp32 scale per 128 x 128 block, uniform over the tile (tiles
+    //   start on 128-row boundaries) and shared by two 64-wide slices.
     const int t = (warp - kConvBase / 32) >> 2;
     const int q = warp & 3;
     const int r = q * 32 + lane;
-    const int sf_ld = p.K / 16;  // bytes of block scales per weight row
-    const int64_t rows_total = static_cast<int64_t>(p.E) * p.Nw;
-    const uint8_t* sf = t ? p.sf1 : p.sf0;
     const int row_off = t ? kRow1 : 0;
     const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + p.a_col +
                             static_cast<uint32_t>(t * (kConvCols / 2));
     int stage = 0, cstage = 0;
     uint32_t phase = 0, cphase = 0;
+    // scale group g of item `it`: slices 4g .. 4g+3
     auto load_group = [&](int it, int g) {
       uint4 v = make_uint4(0, 0, 0, 0);
       if (it >= n_items) return v;
       const int4 item = p.items[it];
-      const int64_t row = static_cast<int64_t>(item.x) * p.Nw + item.y * kItemRows + row_off + r;
-      // padding rows past the last expert decode to zero
-      if (row < rows_total) v = __ldg(reinterpret_cast<const uint4*>(sf + row * sf_ld + g * 16));
+      if constexpr (kFp8) {
+        const int nbr = p.Nw / BM, kbr = p.K / BM;  // 128-blocks per expert: rows, K
+        const int br = (item.y * kItemRows + row_off) / BM;
+        // padding rows past the expert (ragged last down tile) get scale 0
+        if (br < nbr) {
+          const float* f = (t ? p.fs1 : p.fs0) + (static_cast<int64_t>(item.x) * nbr + br) * kbr;
+          const int k0 = 2 * g;  // 128-wide K blocks covered by slices 4g .. 4g+3
+          v.x = __float_as_uint(__ldg(f + k0));
+          if (k0 + 1 < kbr) v.y = __float_as_uint(__ldg(f + k0 + 1));
+        }
+      } else {
+        const int sf_ld = p.K / 16;  // bytes of block scales per weight row
+        const int64_t rows_total = static_cast<int64_t>(p.E) * p.Nw;
+        const int64_t row = static_cast<int64_t>(item.x) * p.Nw + item.y * kItemRows + row_off + r;
+        // padding rows past the last expert decode to zero
+        if (row < rows_total)
+          v = __ldg(reinterpret_cast<const uint4*>((t ? p.sf1 : p.sf0) + row * sf_ld + g * 16));
+      }
       return v;
     };
     uint4 cur = make_uint4(0, 0, 0, 0), nxt = load_group(blockIdx.x, 0);
@@ -459,10 +510,14 @@ __global__ void __launch_bounds__(threads_for(kW4), 1)
           break;
         }
         tc_fence_after();  // the MMAs that read this slot have completed
-        const uint8_t* packed = smem + static_cast<size_t>(stage) * p.stage_bytes + p.p_offset + t * kPTileBytes;
+        const uint8_t* packed = smem + static_cast<size_t>(stage) * p.stage_bytes + p.p_offset + t * kPB;
         const int g = kb & 3;
         uint32_t v[32];
-        decode_row(packed, r, g == 0 ? cur.x : g == 1 ? cur.y : g == 2 ? cur.z : cur.w, v);
+        if constexpr (kFp8) {
+          decode_row_fp8(packed, r, __uint_as_float(g < 2 ? cur.x : cur.y), v);
+        } else {
+          decode_row(packed, r, g == 0 ? cur.x : g == 1 ? cur.y : g == 2 ? cur.z : cur.w, v);
+        }
         tmem_st_32x32b_x32(t_lane + static_cast<uint32_t>(cstage * kConvCols), v);
         tmem_st_wait();
         tc_fence_before();
@@ -588,14 +643,15 @@ int encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t 
   return r == CUDA_SUCCESS ? 0 : static_cast<int>(r);
 }
 
-// 2-D byte tensor [outer][inner_bytes] of packed e2m1 codes, box [128][32 bytes]
-// (one 64-element K slice of 128 weight rows), no swizzle.
-int encode_packed_2d(CUtensorMap* map, const void* base, uint64_t inner_bytes, uint64_t outer) {
+// 2-D byte tensor [outer][inner_bytes] of weight codes, box [128][box_bytes]
+// (one 64-element K slice of 128 weight rows: 32 bytes of e2m1, 64 of e4m3),
+// no swizzle.
+int encode_packed_2d(CUtensorMap* map, const void* base, uint64_t inner_bytes, uint64_t outer, uint32_t box_bytes) {
   auto fn = encode_fn();
   if (!fn) return -1;
   cuuint64_t dims[2] = {inner_bytes, outer};
   cuuint64_t strides[1] = {inner_bytes};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(BK / 2), static_cast<cuuint32_t>(BM)};
+  cuuint32_t box[2] = {box_bytes, static_cast<cuuint32_t>(BM)};
   cuuint32_t estr[2] = {1, 1};
   const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -609,19 +665,20 @@ struct StageShape {
   size_t smem;
 };
 
-StageShape stage_shape(bool glu, bool w4, int n_max) {
+StageShape stage_shape(bool glu, int fmt, int n_max) {
   StageShape s;
   (void)glu;
   const int budget = kSmemLimit - 1024 - 512;  // alignment slack + static barriers
   const uint32_t b_bytes = static_cast<uint32_t>(n_max) * BK * 2;
   s.acc_cols = 2 * n_max;
-  if (w4) {
-    // ring stage: token rows, then the two packed weight tiles. TMEM: the
+  if (fmt != kFmtBf16) {
+    // ring stage: token rows, then the two raw weight tiles. TMEM: the
     // accumulators, then 2-4 decoded slots (at least 3 where that leaves one
     // accumulator buffer); n_max <= 192 keeps two slots.
+    const uint32_t pb = fmt == kFmtFp8 ? kP8TileBytes : kPTileBytes;
     s.b_offset = 0;
     s.p_offset = b_bytes;
-    s.stage_bytes = (b_bytes + 2 * kPTileBytes + 1023u) & ~1023u;
+    s.stage_bytes = (b_bytes + 2 * pb + 1023u) & ~1023u;
     s.acc_bufs = std::max(1, std::min(kMaxAcc, (static_cast<int>(kTmemCols) - 3 * kConvCols) / s.acc_cols));
     s.a_col = static_cast<uint32_t>(s.acc_bufs * s.acc_cols);
     s.conv_stages = std::min(kMaxConv, (static_cast<int>(kTmemCols) - static_cast<int>(s.a_col)) / kConvCols);
@@ -638,11 +695,11 @@ StageShape stage_shape(bool glu, bool w4, int n_max) {
   return s;
 }
 
-template <bool kGLU, bool kW4>
+template <bool kGLU, int kFmt>
 cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap (&b)[3], GemmArgs args,
                         int n_max, int grid, cudaStream_t stream) {
-  const StageShape s = stage_shape(kGLU, kW4, n_max);
-  if (kW4 && s.conv_stages < 2) return cudaErrorInvalidValue;  // n_max above 192
+  const StageShape s = stage_shape(kGLU, kFmt, n_max);
+  if (kFmt != kFmtBf16 && s.conv_stages < 2) return cudaErrorInvalidValue;  // n_max above 192
   args.stages = s.stages;
   args.acc_bufs = s.acc_bufs;
   args.acc_cols = s.acc_cols;
@@ -652,26 +709,26 @@ cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUte
   args.a_col = s.a_col;
   args.conv_stages = s.conv_stages;
   args.n_max = n_max;
-  cudaError_t err = cudaFuncSetAttribute(expert_gemm_kernel<kGLU, kW4>,
+  cudaError_t err = cudaFuncSetAttribute(expert_gemm_kernel<kGLU, kFmt>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s.smem));
   if (err != cudaSuccess) return err;
-  expert_gemm_kernel<kGLU, kW4><<<grid, threads_for(kW4), s.smem, stream>>>(a0, a1, b[0], b[1], b[2], args);
+  expert_gemm_kernel<kGLU, kFmt><<<grid, threads_for(kFmt), s.smem, stream>>>(a0, a1, b[0], b[1], b[2], args);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-ExpertPlan plan_experts(int T, int d, int E, int top_k, int inter, bool w4) {
+ExpertPlan plan_experts(int T, int d, int E, int top_k, int inter, bool decoded) {
   ExpertPlan p;
   // Token tile: a quarter above the mean tokens per expert, at least 64 and at
-  // most 256 (the MMA's largest N; 192 with NVFP4 weights, whose decoded tiles
+  // most 256 (the MMA's largest N; 192 with NVFP4 or FP8 weights, whose decoded tiles
   // share tensor memory with the accumulators), never above the batch (an
   // expert sees a token at most once). Smaller tiles leave shared memory for
   // more pipeline stages; experts above the tile are split into near-equal tiles.
   const int64_t R = static_cast<int64_t>(T) * top_k;
   const int64_t mean = (R + E - 1) / std::max(E, 1);
   int64_t n = ((mean + mean / 4 + 15) / 16) * 16;
-  n = std::max<int64_t>(64, std::min<int64_t>(w4 ? 192 : 256, n));
+  n = std::max<int64_t>(64, std::min<int64_t>(decoded ? 192 : 256, n));
   const int tok = ((std::max(T, 1) + 15) / 16) * 16;
   p.n_max = static_cast<int>(std::min<int64_t>(n, tok));
   p.max_tiles = static_cast<int>(E + (R + p.n_max - 1) / p.n_max);
@@ -687,8 +744,10 @@ cudaError_t launch_expert_ffn(const ExpertPlan& plan, const ExpertBuffers& buf, 
                               cudaStream_t stream, int* cu_error, cudaEvent_t after_gemm1) {
   *cu_error = 0;
   const int R = T * top_k;
-  const bool w4 = w.wfmt == MOE_W_NVFP4;
-  if (w4 && ((d % 256) || (inter % 256))) return cudaErrorNotSupported;
+  const int fmt = w.wfmt;
+  if (fmt != MOE_W_BF16 && fmt != MOE_W_NVFP4 && fmt != MOE_W_FP8) return cudaErrorInvalidValue;
+  if (fmt == MOE_W_NVFP4 && ((d % 256) || (inter % 256))) return cudaErrorNotSupported;
+  if (fmt == MOE_W_FP8 && ((d % 128) || (inter % 128))) return cudaErrorNotSupported;
   schedule_kernel<<<1, 256, 0, stream>>>(buf.offsets, E, R, plan.n_max, plan.wtiles1, plan.wtiles2, buf.items1,
                                          buf.items2, buf.n_items, buf.status);
   cudaError_t err = cudaGetLastError();
@@ -696,10 +755,14 @@ cudaError_t launch_expert_ffn(const ExpertPlan& plan, const ExpertBuffers& buf, 
 
   CUtensorMap tg, tu, td, tx[3], th[3];
   int rc = 0;
-  if (w4) {
-    rc |= encode_packed_2d(&tg, w.gate, d / 2, static_cast<uint64_t>(E) * inter);
-    rc |= encode_packed_2d(&tu, w.up, d / 2, static_cast<uint64_t>(E) * inter);
-    rc |= encode_packed_2d(&td, w.down, inter / 2, static_cast<uint64_t>(E) * d);
+  if (fmt == MOE_W_NVFP4) {
+    rc |= encode_packed_2d(&tg, w.gate, d / 2, static_cast<uint64_t>(E) * inter, BK / 2);
+    rc |= encode_packed_2d(&tu, w.up, d / 2, static_cast<uint64_t>(E) * inter, BK / 2);
+    rc |= encode_packed_2d(&td, w.down, inter / 2, static_cast<uint64_t>(E) * d, BK / 2);
+  } else if (fmt == MOE_W_FP8) {
+    rc |= encode_packed_2d(&tg, w.gate, d, static_cast<uint64_t>(E) * inter, BK);
+    rc |= encode_packed_2d(&tu, w.up, d, static_cast<uint64_t>(E) * inter, BK);
+    rc |= encode_packed_2d(&td, w.down, inter, static_cast<uint64_t>(E) * d, BK);
   } else {
     rc |= encode_bf16_2d(&tg, w.gate, d, static_cast<uint64_t>(E) * inter, BM);
     rc |= encode_bf16_2d(&tu, w.up, d, static_cast<uint64_t>(E) * inter, BM);
@@ -724,14 +787,18 @@ cudaError_t launch_expert_ffn(const ExpertPlan& plan, const ExpertBuffers& buf, 
   a1.status = buf.status;
   a1.timeout_where = buf.timeout_where;
   a1.wait_spins = wait_spins;
-  if (w4) {
+  if (fmt == MOE_W_NVFP4) {
     a1.ts0 = w.gate_ts;
     a1.ts1 = w.up_ts;
-    a1.sf0 = w.gate_sf;
-    a1.sf1 = w.up_sf;
-    err = launch_gemm<true, true>(tg, tu, tx, a1, plan.n_max, num_sms, stream);
+    a1.sf0 = static_cast<const uint8_t*>(w.gate_sf);
+    a1.sf1 = static_cast<const uint8_t*>(w.up_sf);
+    err = launch_gemm<true, kFmtNvfp4>(tg, tu, tx, a1, plan.n_max, num_sms, stream);
+  } else if (fmt == MOE_W_FP8) {
+    a1.fs0 = static_cast<const float*>(w.gate_sf);
+    a1.fs1 = static_cast<const float*>(w.up_sf);
+    err = launch_gemm<true, kFmtFp8>(tg, tu, tx, a1, plan.n_max, num_sms, stream);
   } else {
-    err = launch_gemm<true, false>(tg, tu, tx, a1, plan.n_max, num_sms, stream);
+    err = launch_gemm<true, kFmtBf16>(tg, tu, tx, a1, plan.n_max, num_sms, stream);
   }
   if (err != cudaSuccess) return err;
   if (after_gemm1 && (err = cudaEventRecord(after_gemm1, stream)) != cudaSuccess) return err;
@@ -745,13 +812,18 @@ cudaError_t launch_expert_ffn(const ExpertPlan& plan, const ExpertBuffers& buf, 
   a2.status = buf.status;
   a2.timeout_where = buf.timeout_where;
   a2.wait_spins = wait_spins;
-  if (w4) {
+  if (fmt == MOE_W_NVFP4) {
     a2.ts0 = w.down_ts;
-    a2.sf0 = w.down_sf;
-    a2.sf1 = w.down_sf;
-    return launch_gemm<false, true>(td, td, th, a2, plan.n_max, num_sms, stream);
+    a2.sf0 = static_cast<const uint8_t*>(w.down_sf);
+    a2.sf1 = a2.sf0;
+    return launch_gemm<false, kFmtNvfp4>(td, td, th, a2, plan.n_max, num_sms, stream);
   }
-  return launch_gemm<false, false>(td, td, th, a2, plan.n_max, num_sms, stream);
+  if (fmt == MOE_W_FP8) {
+    a2.fs0 = static_cast<const float*>(w.down_sf);
+    a2.fs1 = a2.fs0;
+    return launch_gemm<false, kFmtFp8>(td, td, th, a2, plan.n_max, num_sms, stream);
+  }
+  return launch_gemm<false, kFmtBf16>(td, td, th, a2, plan.n_max, num_sms, stream);
 }
 
 }  // namespace beammoe

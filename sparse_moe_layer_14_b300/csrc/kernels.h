@@ -51,7 +51,8 @@ struct ExpertPlan {
   int wtiles2;      // 256-row weight tiles per expert in GEMM2 (ceil(d/256))
   int64_t max_items1, max_items2;
 };
-ExpertPlan plan_experts(int T, int d, int E, int top_k, int inter, bool w4);
+// decoded: NVFP4 or FP8 weights (decoded into tensor memory; token tile <= 192)
+ExpertPlan plan_experts(int T, int d, int E, int top_k, int inter, bool decoded);
 
 struct ExpertBuffers {
   const uint16_t* x_perm;  // [R][d]
@@ -68,7 +69,7 @@ struct ExpertBuffers {
 struct ExpertWeightsDev {
   int wfmt;
   const void *gate, *up, *down;
-  const uint8_t *gate_sf, *up_sf, *down_sf;
+  const void *gate_sf, *up_sf, *down_sf;  // e4m3 bytes (NVFP4) or fp32 (FP8)
   const float *gate_ts, *up_ts, *down_ts;
 };
 

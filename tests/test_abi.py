@@ -88,6 +88,12 @@ def test_null_and_misaligned_pointers_rejected(lib):
     # NVFP4 needs scales
     d4 = _dims(wfmt=1)
     assert lib.moe_forward(ctypes.byref(d4), fake, fake, ctypes.byref(w), fake, None, None, fake, ws_bytes, None) == N.MOE_ERR_INVALID_ARG
+    # FP8 needs 4-byte aligned block scales
+    d8 = _dims(wfmt=N.MOE_W_FP8)
+    ws8 = lib.moe_workspace_bytes(ctypes.byref(d8))
+    assert lib.moe_forward(ctypes.byref(d8), fake, fake, ctypes.byref(w), fake, None, None, fake, ws8, None) == N.MOE_ERR_INVALID_ARG
+    w8 = N.MoeExpertWeights(fake, fake, fake, fake, ctypes.c_void_p((1 << 20) + 2), fake)
+    assert lib.moe_forward(ctypes.byref(d8), fake, fake, ctypes.byref(w8), fake, None, None, fake, ws8, None) == N.MOE_ERR_INVALID_ARG
     assert lib.moe_workspace_init(None, 4096, None) == N.MOE_ERR_WORKSPACE
     code = ctypes.c_int32()
     assert lib.moe_get_device_status(None, None, 0, ctypes.byref(code)) == N.MOE_ERR_INVALID_ARG

@@ -41,8 +41,9 @@ def test_dense_mlp_parity(T, d, inter, seed):
     assert np.sqrt(np.mean((W.bf16_to_f32(got).astype(np.float64) - ref) ** 2)) <= 2e-3 * np.sqrt(np.mean(ref ** 2))
 
 
-def test_dense_mlp_nvfp4_parity():
-    _run(_dense_cfg(100, 256, 512, "nvfp4"), 4)
+@pytest.mark.parametrize("wfmt", ["nvfp4", "fp8"])
+def test_dense_mlp_quantised_parity(wfmt):
+    _run(_dense_cfg(100, 256, 512, wfmt), 4)
 
 
 def test_dense_mlp_beam_width_sampled_rows():

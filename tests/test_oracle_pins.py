@@ -402,7 +402,7 @@ def test_printed_block_facts():
     arithmetic closes: 3*5120*2560 ~ 39M per expert, 49*256 experts ~ 98.4% of 501B,
     and the routed parameters plus the replicated rest fit the 23B active figure."""
     g = json.load(open(GOLDEN))
-    for name in ("decode", "prefill", "skewed", "nvfp4"):
+    for name in ("decode", "prefill", "skewed", "nvfp4", "fp8"):
         c = W.CONFIGS[name]
         assert (c.d, c.E, c.n_groups, c.E // c.n_groups, c.topk_groups, c.top_k, c.inter, c.routed_scale) == (
             g["hidden"], g["experts"], g["groups"], g["group_size"], g["groups_kept"], g["routed_per_token"],

@@ -75,6 +75,9 @@ CONFIGS = {
     # Beam shape prefill with NVFP4 expert weights
     "nvfp4": MoEConfig("nvfp4", T=4096, d=5120, E=256, n_groups=8, topk_groups=4, top_k=8, inter=2560,
                        wfmt="nvfp4"),
+    # Beam shape prefill with FP8 expert weights (128 x 128 block scales)
+    "fp8": MoEConfig("fp8", T=4096, d=5120, E=256, n_groups=8, topk_groups=4, top_k=8, inter=2560,
+                     wfmt="fp8"),
 }
 
 
