@@ -19,7 +19,8 @@
  *  - section "Key specifications": 8 experts routed per token.
  *
  * Readings where the article is silent (each one is listed in the design
- * notes): ties go to the lower group / expert index; the router has no bias;
+ * notes): ties go to the lower group / expert index; the router logits have no
+ * bias term (the optional selection bias of load balancing is separate);
  * the normalisation has no epsilon; h = silu(g) * u is formed in FP32 and
  * rounded to bf16 before the down projection (the down GEMM takes bf16 input);
  * the block output is returned unrounded (double).
@@ -33,6 +34,8 @@
  *   router:   [d][E] fp32 (logits = x . W_r)
  * NVFP4 weights: packed e2m1 [E][N][K/2] (low nibble = even k), e4m3 block
  * scales [E][N][K/16], one fp32 tensor scale per expert and matrix.
+ * FP8 weights: e4m3 codes [E][N][K], one fp32 scale per 128 x 128 block
+ * [E][N/128][K/128] (DeepSeek-V3's block-scaled layout).
  */
 #include <math.h>
 #include <stdint.h>

@@ -155,10 +155,8 @@ __device__ __forceinline__ void decode_row(const uint8_t* packed_tile, int r, ui
   }
 }
 
-// Row r of one 128 x 64 FP8 weight tile (64 e4m3 codes, element k in byte k)
-// times the slice's fp32 block scale `s`, each product rounded once to bf16
-// (e4m3 -> f16 is exact; the product in fp32): 32 bf16x2 words in element
-// order, word c holding elements 2c (low half) and 2c+1.
+// Two e4m3 codes (low byte = lower element) times the fp32 block scale `s`:
+// e4m3 -> f16 is exact, the product is rounded to fp32 and then to bf16.
 __device__ __forceinline__ uint32_t e4m3x2_scaled_bf16x2(uint32_t two, float s) {
   uint32_t h;
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(static_cast<uint16_t>(two)));
@@ -167,6 +165,9 @@ __device__ __forceinline__ uint32_t e4m3x2_scaled_bf16x2(uint32_t two, float s) 
   return *reinterpret_cast<const uint32_t*>(&b);
 }
 
+// Row r of one 128 x 64 FP8 weight tile (64 e4m3 codes, element k in byte k)
+// scaled and rounded as above: 32 bf16x2 words in element order, word c
+// holding elements 2c (low half) and 2c+1.
 __device__ __forceinline__ void decode_row_fp8(const uint8_t* packed_tile, int r, float s, uint32_t (&out)[32]) {
   const uint4* row = reinterpret_cast<const uint4*>(packed_tile + r * 64);
 #pragma unroll

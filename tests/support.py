@@ -22,7 +22,7 @@ TOL_NVFP4 = 5e-2  # ... NVFP4 and FP8 weights
 # Typical (RMS) error bar of the expert FFN relative to the RMS output. bf16 and
 # NVFP4 weights reach the tensor cores exactly, leaving fp32 summation order and
 # 1-ulp flips of the bf16 h and output (~1.1e-3 to 1.7e-3). FP8 weights are
-# dequantised on chip to bf16 (e4m3 x block scale rounded once, ulp 2^-7; the
+# dequantised on chip to bf16 (e4m3 x block scale rounded to fp32, then to bf16, ulp 2^-7; the
 # oracle keeps the exact product): a relative error of RMS ~2^-8 / sqrt(3) /
 # sqrt(2) ~ 1.6e-3 per weight, reaching y through gate, up and down. A CPU model
 # of exactly these roundings gives 3.9e-3 on the ragged-tile case, as the kernel

@@ -439,6 +439,8 @@ MUTANTS = {
     "post_norm_no_gain": (" * bf16_value(gamma[c]))", ")"),
     "fp8_block_transposed": ("bs[((int64_t)e * nbn + n / 128) * nbk + k / 128]",
                              "bs[((int64_t)e * nbn + k / 128) * nbk + n / 128]"),
+    "fp8_scale_dropped": ("(double)bs[((int64_t)e * nbn + n / 128) * nbk + k / 128]", "1.0"),
+    "fp8_scales_of_expert_0": ("bs[((int64_t)e * nbn + n / 128)", "bs[((int64_t)0 * nbn + n / 128)"),
     "no_group_limit": ("if (kept[e / gsz] && !taken[e] && (best < 0", "if (!taken[e] && (best < 0"),
     "h_not_rounded": ("hbuf[i] = bf16_value(hb);", "hbuf[i] = (double)(silu * uf);"),
     "down_transposed": ("acc += hbuf[i] * wmat_at(down, e, n, i);", "acc += hbuf[i] * wmat_at(down, e, i % d, n % I);"),
