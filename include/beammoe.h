@@ -81,7 +81,9 @@ typedef enum { MOE_W_BF16 = 0, MOE_W_NVFP4 = 1, MOE_W_FP8 = 2 } moe_wfmt_t;
  * Supported: T >= 0 (T == 0 is a no-op), d and inter multiples of 64 and at
  * most 16384, 1 <= E <= 256, n_groups divides E and n_groups <= 32,
  * 1 <= topk_groups <= n_groups, 1 <= top_k <= min(32, topk_groups*E/n_groups),
- * T <= 4194304. */
+ * T <= 4194304. Calls that run the expert GEMMs return MOE_ERR_UNSUPPORTED
+ * unless d and inter are multiples of 256 for MOE_W_NVFP4 and of 128 for
+ * MOE_W_FP8. */
 typedef struct {
   int32_t T;
   int32_t d;
