@@ -53,6 +53,7 @@ def load(path: str | None = None):
                                         vp, vp, vp, vp]
     L.oracle_num_threads.restype = i32
     L.oracle_residual_update.argtypes = [i32, i32, vp, vp, vp, dbl, i32, vp]
+    L.oracle_pre_norm.argtypes = [i32, i32, vp, vp, dbl, vp]
     return L
 
 
@@ -180,6 +181,17 @@ def residual_update(out, h_old, gamma, eps, step, L=None):
     L.oracle_residual_update(T, d, _p(out), _p(np.ascontiguousarray(h_old, np.uint16)),
                              _p(np.ascontiguousarray(gamma, np.uint16)), float(eps), int(step), _p(h_new))
     return h_new
+
+
+def pre_norm(h, gamma, eps, L=None):
+    """Pre-norm of the sublayer input: x [T, d] bf16 bits = bf16(RMSNorm(h) * gamma) from the
+    stream h [T, d] bf16 bits and the gain gamma [d] bf16 bits."""
+    L = L or lib()
+    h = np.ascontiguousarray(h, np.uint16)
+    T, d = h.shape
+    x = np.empty((T, d), np.uint16)
+    L.oracle_pre_norm(T, d, _p(h), _p(np.ascontiguousarray(gamma, np.uint16)), float(eps), _p(x))
+    return x
 
 
 def forward_tokens(cfg, x, idx, w, tokens, weights, L=None):

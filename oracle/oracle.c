@@ -395,6 +395,25 @@ void oracle_residual_update(int T, int d, const double* out, const uint16_t* h_o
   }
 }
 
+/* Pre-norm of the sublayer input, per token row t (the article: every sublayer
+ * is normalised before and after, the norms in FP32): the exact RMSNorm value
+ * is rounded to FP32, then to bf16, the dtype the block takes as x:
+ *   r       = sqrt(mean_c(h[t][c]^2) + eps)
+ *   x[t][c] = bf16( fp32( h[t][c] / r * gamma[c] ) )
+ * h [T][d] bf16 bits (the residual stream), gamma [d] bf16 bits, x [T][d] bf16
+ * bits. */
+void oracle_pre_norm(int T, int d, const uint16_t* h, const uint16_t* gamma, double eps, uint16_t* x) {
+#pragma omp parallel for schedule(static)
+  for (int t = 0; t < T; ++t) {
+    const uint16_t* row = h + (int64_t)t * d;
+    double ss = 0.0;
+    for (int c = 0; c < d; ++c) ss += bf16_value(row[c]) * bf16_value(row[c]);
+    const double r = sqrt(ss / d + eps);
+    for (int c = 0; c < d; ++c)
+      x[(int64_t)t * d + c] = bf16_round((float)(bf16_value(row[c]) / r * bf16_value(gamma[c])));
+  }
+}
+
 int oracle_num_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();

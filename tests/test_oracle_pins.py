@@ -384,12 +384,41 @@ def check_residual_constant_scale(L):
         assert abs((hn ** 2).mean() - 1.0) < 0.02, (k, (hn ** 2).mean())
 
 
+def check_pre_norm_closed_forms(L):
+    """RMSNorm before the sublayer, in closed forms that hold exactly for bf16 inputs with
+    eps = 0: a constant row maps to sign * gain; a one-hot row a * e_j maps to
+    sign(a) * sqrt(d) * gain_j at j and 0 elsewhere (sqrt(64) = 8); scaling a row by a power
+    of two changes nothing; a positive eps shrinks the mean square to ms / (ms + eps)."""
+    d = 64
+    gain = _bf16_bits(np.linspace(0.5, 1.5, d).astype(np.float32))
+    g = _f(gain)
+    for c in (3.0, -0.375, 1e-3):
+        x = O.pre_norm(_bf16_const(c, d)[None], gain, 0.0, L)
+        assert np.array_equal(_f(x[0]), np.sign(c) * g)
+    for j, a in ((0, 2.5), (17, -0.75), (63, 40.0)):
+        h = np.zeros(d, np.float32)
+        h[j] = a
+        x = _f(O.pre_norm(_bf16_bits(h)[None], gain, 0.0, L)[0])
+        want = np.zeros(d)
+        want[j] = _f(_bf16_bits(np.array([np.sign(a) * 8.0 * g[j]], np.float32)))[0]
+        assert np.array_equal(x, want), (j, x[j], want[j])
+    h = W.normal_bf16(51, W.TID_AUX, 0, 16 * d, 1.0).reshape(16, d)
+    x1 = O.pre_norm(h, gain, 0.0, L)
+    x8 = O.pre_norm(_bf16_bits(_f(h) * 8.0), gain, 0.0, L)
+    assert np.array_equal(x1, x8)
+    ones = _bf16_const(1.0, d)
+    ms = (_f(h).astype(np.float64) ** 2).mean(1)
+    for eps in (0.0, 0.5):
+        xr = _f(O.pre_norm(h, ones, eps, L)).astype(np.float64)
+        assert np.allclose((xr ** 2).mean(1), ms / (ms + eps), rtol=5e-3, atol=0)
+
+
 CHECKS = [check_uniform_scores, check_router_logits, check_select_bruteforce, check_select_bias,
           check_select_invariants,
           check_single_expert_dense, check_identical_experts, check_permute, check_combine,
           check_forward_matches_stages, check_nvfp4_decode, check_nvfp4_ffn, check_fp8_ffn,
           check_residual_step1_normalises,
-          check_residual_equal_weights, check_residual_constant_scale]
+          check_residual_equal_weights, check_residual_constant_scale, check_pre_norm_closed_forms]
 
 
 @pytest.mark.parametrize("check", CHECKS, ids=lambda c: c.__name__)
@@ -439,6 +468,14 @@ MUTANTS = {
     "post_norm_no_gain": (" * bf16_value(gamma[c]))", ")"),
     "fp8_block_transposed": ("bs[((int64_t)e * nbn + n / 128) * nbk + k / 128]",
                              "bs[((int64_t)e * nbn + k / 128) * nbk + n / 128]"),
+    "pre_norm_no_gain": ("bf16_round((float)(bf16_value(row[c]) / r * bf16_value(gamma[c])))",
+                         "bf16_round((float)(bf16_value(row[c]) / r))"),
+    "pre_norm_abs_not_square": ("ss += bf16_value(row[c]) * bf16_value(row[c]);",
+                                "ss += fabs(bf16_value(row[c]));"),
+    "pre_norm_eps_outside_sqrt": ("const double r = sqrt(ss / d + eps);\n    for (int c = 0; c < d; ++c)\n      x[",
+                                  "const double r = sqrt(ss / d) + eps;\n    for (int c = 0; c < d; ++c)\n      x["),
+    "pre_norm_sum_not_mean": ("const double r = sqrt(ss / d + eps);\n    for (int c = 0; c < d; ++c)\n      x[",
+                              "const double r = sqrt(ss + eps);\n    for (int c = 0; c < d; ++c)\n      x["),
     "fp8_scale_dropped": ("(double)bs[((int64_t)e * nbn + n / 128) * nbk + k / 128]", "1.0"),
     "fp8_scales_of_expert_0": ("bs[((int64_t)e * nbn + n / 128)", "bs[((int64_t)0 * nbn + n / 128)"),
     "no_group_limit": ("if (kept[e / gsz] && !taken[e] && (best < 0", "if (!taken[e] && (best < 0"),
