@@ -24,8 +24,12 @@ from ._native import (MOE_DEV_BAD_EXPERT, MOE_DEV_BAD_ROW, MOE_DEV_OK, MOE_DEV_T
                       MOE_DEV_ZERO_SUM, MOE_W_BF16, MOE_W_FP8, MOE_W_NVFP4, MoeDims, MoeExpertWeights)
 
 __all__ = ["MoEError", "Dims", "ExpertWeights", "moe_workspace_bytes", "moe_workspace_init", "moe_route",
-           "moe_permute", "moe_permute_noalloc", "moe_expert_ffn", "moe_combine", "moe_forward", "moe_get_device_status",
-           "moe_set_wait_bound", "moe_set_stage_events", "moe_version", "allocate_workspace", "library_path"]
+           "moe_permute", "moe_permute_noalloc", "moe_expert_ffn", "moe_combine", "moe_combine_residual",
+           "moe_forward", "moe_forward_residual", "moe_dense_workspace_bytes", "moe_dense_mlp",
+           "moe_get_device_status", "moe_set_wait_bound", "moe_set_stage_events", "moe_version",
+           "allocate_workspace", "allocate_dense_workspace", "library_path",
+           "MOE_DEV_OK", "MOE_DEV_BAD_EXPERT", "MOE_DEV_BAD_ROW", "MOE_DEV_TIMEOUT", "MOE_DEV_ZERO_SUM",
+           "MOE_W_BF16", "MOE_W_NVFP4", "MOE_W_FP8"]
 
 
 class MoEError(RuntimeError):

@@ -120,3 +120,14 @@ def test_product_never_imports_the_oracle():
                 src = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+(oracle|workload)\b", src, re.M), f
                 assert "liboracle" not in src and "oracle.c" not in src, f
+
+
+def test_binding_exports_every_public_call():
+    """Every name in the package's __all__ exists, and every C entry point the header declares
+    that takes block arguments has a Python wrapper of the same name."""
+    for name in bm.__all__:
+        assert hasattr(bm, name), name
+    wrapped = {n for n in declared_functions() if hasattr(bm, n)}
+    for required in ("moe_route", "moe_permute", "moe_expert_ffn", "moe_combine", "moe_forward",
+                     "moe_forward_residual", "moe_combine_residual", "moe_dense_mlp", "moe_permute_noalloc"):
+        assert required in wrapped, required
