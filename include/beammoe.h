@@ -232,6 +232,28 @@ moe_status_t moe_forward_residual(const moe_dims_t* dims, const moe_bf16_t* x, c
                                   const moe_bf16_t* norm_gain, float eps, int32_t step, moe_bf16_t* resid,
                                   int32_t* topk_idx, int32_t* counts, void* ws, size_t ws_bytes, void* stream);
 
+/* Pre-norm of a sublayer input (release article, section "Residual stream":
+ * every sublayer is normalised before and after, the norms in FP32). For every
+ * token t:
+ *   x[t][c] = bf16( h[t][c] * gain[c] / sqrt(mean_c(h[t][c]^2) + eps) )   (FP32)
+ * h, x [T][d] and gain [d] bf16, 16-byte aligned; x must not overlap h;
+ * eps >= 0. Uses dims->T and dims->d (a multiple of 64, at most 16384); the
+ * other fields are ignored. One kernel, no workspace. */
+moe_status_t moe_pre_norm(const moe_dims_t* dims, const moe_bf16_t* h, const moe_bf16_t* gain, float eps,
+                          moe_bf16_t* x, void* stream);
+
+/* The MoE sublayer as a decoder layer runs it (release article, section
+ * "Residual stream"): x = the pre-norm of resid with pre_gain (as
+ * moe_pre_norm, into the caller's x [T][d], which must not overlap resid);
+ * the block forward on x with the optional selection bias (as moe_forward_ex);
+ * then the post-norm with post_gain and the depth-scaled update of resid in
+ * place at step `step` (as moe_forward_residual). One eps for both norms;
+ * d <= 8192. All arguments are checked before the first launch. */
+moe_status_t moe_sublayer(const moe_dims_t* dims, moe_bf16_t* resid, const moe_bf16_t* pre_gain,
+                          const moe_bf16_t* post_gain, float eps, int32_t step, const float* w_r,
+                          const float* sel_bias, const moe_expert_weights_t* weights, moe_bf16_t* x,
+                          int32_t* topk_idx, int32_t* counts, void* ws, size_t ws_bytes, void* stream);
+
 /* Dense SwiGLU MLP of the first decoder layers (release article, section
  * "Architecture": the first 3 of the 52 layers use a dense SwiGLU MLP instead
  * of the Mixture-of-Experts block). For every token t:

@@ -25,7 +25,8 @@ from ._native import (MOE_DEV_BAD_EXPERT, MOE_DEV_BAD_ROW, MOE_DEV_OK, MOE_DEV_T
 
 __all__ = ["MoEError", "Dims", "ExpertWeights", "moe_workspace_bytes", "moe_workspace_init", "moe_route",
            "moe_permute", "moe_permute_noalloc", "moe_expert_ffn", "moe_combine", "moe_combine_residual",
-           "moe_forward", "moe_forward_residual", "moe_dense_workspace_bytes", "moe_dense_mlp",
+           "moe_forward", "moe_forward_residual", "moe_pre_norm", "moe_sublayer", "moe_dense_workspace_bytes",
+           "moe_dense_mlp",
            "moe_get_device_status", "moe_set_wait_bound", "moe_set_stage_events", "moe_version",
            "allocate_workspace", "allocate_dense_workspace", "library_path",
            "MOE_DEV_OK", "MOE_DEV_BAD_EXPERT", "MOE_DEV_BAD_ROW", "MOE_DEV_TIMEOUT", "MOE_DEV_ZERO_SUM",
@@ -262,6 +263,34 @@ def moe_forward_residual(dims: Dims, x, w_r, weights: ExpertWeights, norm_gain, 
     _check("moe_forward_residual", _lib().moe_forward_residual(
         ctypes.byref(dims.c()), _ptr(x), _ptr(w_r), _ptr(sel_bias), ctypes.byref(weights.c()), _ptr(norm_gain),
         float(eps), int(step), _ptr(resid), _ptr(topk_idx), _ptr(counts), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_pre_norm(dims: Dims, h, gain, eps: float, x, stream=None):
+    """x = bf16(RMSNorm(h) * gain) per token row, FP32 (x must not overlap h)."""
+    _expect(h, _BF16, (dims.T, dims.d), "h")
+    _expect(gain, _BF16, (dims.d,), "gain")
+    _expect(x, _BF16, (dims.T, dims.d), "x")
+    _check("moe_pre_norm", _lib().moe_pre_norm(ctypes.byref(dims.c()), _ptr(h), _ptr(gain), float(eps), _ptr(x),
+                                               _stream(stream)))
+
+
+def moe_sublayer(dims: Dims, resid, pre_gain, post_gain, eps: float, step: int, w_r, weights: ExpertWeights, x, ws,
+                 topk_idx=None, counts=None, stream=None, sel_bias=None):
+    """The MoE sublayer: x = pre-norm(resid) (into x), the block forward on x, then the post-norm and
+    depth-scaled update of resid in place."""
+    _expect(resid, _BF16, (dims.T, dims.d), "resid")
+    _expect(pre_gain, _BF16, (dims.d,), "pre_gain")
+    _expect(post_gain, _BF16, (dims.d,), "post_gain")
+    _expect(w_r, (torch.float32,), (dims.d, dims.E), "w_r")
+    _expect(x, _BF16, (dims.T, dims.d), "x")
+    _expect(topk_idx, (torch.int32,), (dims.T, dims.top_k), "topk_idx")
+    _expect(counts, (torch.int32,), (dims.E,), "counts")
+    _expect(sel_bias, (torch.float32,), (dims.E,), "sel_bias")
+    _check_weights(dims, weights)
+    _check("moe_sublayer", _lib().moe_sublayer(
+        ctypes.byref(dims.c()), _ptr(resid), _ptr(pre_gain), _ptr(post_gain), float(eps), int(step), _ptr(w_r),
+        _ptr(sel_bias), ctypes.byref(weights.c()), _ptr(x), _ptr(topk_idx), _ptr(counts), _ptr(ws), ws.numel(),
+        _stream(stream)))
 
 
 def _dense(dims: Dims) -> Dims:

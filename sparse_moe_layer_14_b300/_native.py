@@ -21,7 +21,7 @@ MOE_W_BF16, MOE_W_NVFP4, MOE_W_FP8 = 0, 1, 2
 EXPORTS = ["moe_workspace_bytes", "moe_workspace_init", "moe_route", "moe_permute", "moe_expert_ffn",
            "moe_combine", "moe_forward", "moe_get_device_status", "moe_set_wait_bound", "moe_set_stage_events",
            "moe_version", "moe_permute_noalloc", "moe_dense_workspace_bytes", "moe_dense_mlp", "moe_route_ex",
-           "moe_forward_ex", "moe_combine_residual", "moe_forward_residual"]
+           "moe_forward_ex", "moe_combine_residual", "moe_forward_residual", "moe_pre_norm", "moe_sublayer"]
 
 
 class MoeDims(ctypes.Structure):
@@ -71,6 +71,10 @@ def load(path: str = LIB_PATH):
     L.moe_forward_residual.argtypes = [pd, vp, vp, vp, pw, vp, ctypes.c_float, ctypes.c_int32, vp, vp, vp, vp, sz,
                                        vp]
     L.moe_forward_residual.restype = st
+    L.moe_pre_norm.argtypes = [pd, vp, vp, ctypes.c_float, vp, vp]
+    L.moe_pre_norm.restype = st
+    L.moe_sublayer.argtypes = [pd, vp, vp, vp, ctypes.c_float, ctypes.c_int32, vp, vp, pw, vp, vp, vp, vp, sz, vp]
+    L.moe_sublayer.restype = st
     L.moe_forward.restype = st
     L.moe_get_device_status.argtypes = [vp, vp, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]
     L.moe_get_device_status.restype = st

@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libbeammoe.so")
-SOURCES = ["router.cu", "permute.cu", "expert_gemm.cu", "combine.cu", "api.cu", "noalloc.cu"]
+SOURCES = ["router.cu", "permute.cu", "expert_gemm.cu", "combine.cu", "norm.cu", "api.cu", "noalloc.cu"]
 HEADERS = ["common.cuh", "kernels.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -347,6 +347,49 @@ moe_status_t moe_combine_residual(const moe_dims_t* dims, const moe_bf16_t* y_pe
                                              dims->top_k, status_word(ws), static_cast<cudaStream_t>(stream)));
 }
 
+// ---------------------------------------------------------------- pre-norm and the sublayer
+
+namespace {
+
+moe_status_t check_norm_args(const moe_dims_t* d, const void* h, const void* gain, float eps, const void* x) {
+  if (!d || d->T < 0 || d->d <= 0) return MOE_ERR_INVALID_ARG;
+  if (d->T > 4194304 || d->d % 64 || d->d > 16384) return MOE_ERR_UNSUPPORTED;
+  if (d->T == 0) return MOE_OK;
+  if (!aligned16(h) || !aligned16(gain) || !aligned16(x) || !(eps >= 0.0f)) return MOE_ERR_INVALID_ARG;
+  const uintptr_t hb = reinterpret_cast<uintptr_t>(h), xb = reinterpret_cast<uintptr_t>(x);
+  const uintptr_t n = static_cast<uintptr_t>(d->T) * static_cast<uintptr_t>(d->d) * 2u;
+  if (hb < xb + n && xb < hb + n) return MOE_ERR_INVALID_ARG;  // x overlaps h
+  return MOE_OK;
+}
+
+}  // namespace
+
+moe_status_t moe_pre_norm(const moe_dims_t* dims, const moe_bf16_t* h, const moe_bf16_t* gain, float eps,
+                          moe_bf16_t* x, void* stream) {
+  const moe_status_t st = check_norm_args(dims, h, gain, eps, x);
+  if (st != MOE_OK || dims->T == 0) return st;
+  return cuda_status(launch_pre_norm(h, gain, eps, x, dims->T, dims->d, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_sublayer(const moe_dims_t* dims, moe_bf16_t* resid, const moe_bf16_t* pre_gain,
+                          const moe_bf16_t* post_gain, float eps, int32_t step, const float* w_r,
+                          const float* sel_bias, const moe_expert_weights_t* weights, moe_bf16_t* x,
+                          int32_t* topk_idx, int32_t* counts, void* ws, size_t ws_bytes, void* stream) {
+  moe_status_t st = check_dims(dims);
+  if (st != MOE_OK) return st;
+  if ((st = check_norm_args(dims, resid, pre_gain, eps, x)) != MOE_OK || dims->T == 0) return st;
+  // everything forward_impl checks, before the pre-norm is enqueued
+  if (!aligned16(w_r) || !aligned16(post_gain) || step < 1) return MOE_ERR_INVALID_ARG;
+  if (dims->d > 8192) return MOE_ERR_UNSUPPORTED;
+  if (sel_bias && (reinterpret_cast<uintptr_t>(sel_bias) & 3u)) return MOE_ERR_INVALID_ARG;
+  if ((st = check_weights(dims, weights)) != MOE_OK) return st;
+  if ((st = check_ws(dims, ws, ws_bytes)) != MOE_OK) return st;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((st = cuda_status(launch_pre_norm(resid, pre_gain, eps, x, dims->T, dims->d, s))) != MOE_OK) return st;
+  const ResidualArgs res{post_gain, eps, step, resid};
+  return forward_impl(dims, x, w_r, sel_bias, weights, nullptr, &res, topk_idx, counts, ws, ws_bytes, stream);
+}
+
 // ---------------------------------------------------------------- dense SwiGLU MLP
 
 // One expert, every token: the expert GEMMs with offsets {0, T}.

@@ -77,6 +77,11 @@ cudaError_t launch_expert_ffn(const ExpertPlan& plan, const ExpertBuffers& buf, 
                               int d, int E, int top_k, int inter, int num_sms, long long wait_spins,
                               cudaStream_t stream, int* cu_error, cudaEvent_t after_gemm1 = nullptr);
 
+// ---- pre-norm (norm.cu) ----
+// x [T][d] = bf16(RMSNorm(h) * gain), FP32; d a multiple of 64; x must not overlap h.
+cudaError_t launch_pre_norm(const uint16_t* h, const uint16_t* gain, float eps, uint16_t* x, int T, int d,
+                            cudaStream_t stream);
+
 // ---- combine (combine.cu) ----
 // combine + post-norm (RMSNorm, gain [d]) + depth-scaled residual update of
 // resid [T][d] in place at step `step` (>= 1); d <= 8192 (one cluster of

@@ -129,5 +129,28 @@ def test_binding_exports_every_public_call():
         assert hasattr(bm, name), name
     wrapped = {n for n in declared_functions() if hasattr(bm, n)}
     for required in ("moe_route", "moe_permute", "moe_expert_ffn", "moe_combine", "moe_forward",
-                     "moe_forward_residual", "moe_combine_residual", "moe_dense_mlp", "moe_permute_noalloc"):
+                     "moe_forward_residual", "moe_combine_residual", "moe_dense_mlp", "moe_permute_noalloc",
+                     "moe_pre_norm", "moe_sublayer"):
         assert required in wrapped, required
+
+
+def test_pre_norm_and_sublayer_host_checks(lib):
+    """Host-side validation of moe_pre_norm / moe_sublayer: nothing is launched."""
+    fake = ctypes.c_void_p(1 << 20)
+    d = _dims(T=4, d=128)
+    # x overlapping h, a d that is not a multiple of 64, a negative eps, a misaligned gain
+    assert lib.moe_pre_norm(ctypes.byref(d), fake, fake, 1e-6, ctypes.c_void_p((1 << 20) + 512), None) == N.MOE_ERR_INVALID_ARG
+    assert lib.moe_pre_norm(ctypes.byref(_dims(T=4, d=100)), fake, fake, 1e-6, fake, None) == N.MOE_ERR_UNSUPPORTED
+    far = ctypes.c_void_p(1 << 24)
+    assert lib.moe_pre_norm(ctypes.byref(d), fake, fake, -1.0, far, None) == N.MOE_ERR_INVALID_ARG
+    assert lib.moe_pre_norm(ctypes.byref(d), fake, ctypes.c_void_p((1 << 20) + 8), 1e-6, far, None) == N.MOE_ERR_INVALID_ARG
+    assert lib.moe_pre_norm(ctypes.byref(_dims(T=0, d=128)), None, None, 1e-6, None, None) == N.MOE_OK
+    w = N.MoeExpertWeights(fake, fake, fake)
+    dd = _dims()
+    ws_bytes = lib.moe_workspace_bytes(ctypes.byref(dd))
+    # step 0 and d > 8192 are rejected before the pre-norm is enqueued
+    assert lib.moe_sublayer(ctypes.byref(dd), fake, fake, fake, 1e-6, 0, fake, None, ctypes.byref(w), far,
+                            None, None, fake, ws_bytes, None) == N.MOE_ERR_INVALID_ARG
+    big = _dims(d=16384)
+    assert lib.moe_sublayer(ctypes.byref(big), fake, fake, fake, 1e-6, 2, fake, None, ctypes.byref(w),
+                            ctypes.c_void_p(1 << 30), None, None, fake, ws_bytes, None) == N.MOE_ERR_UNSUPPORTED

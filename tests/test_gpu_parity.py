@@ -479,3 +479,52 @@ def test_forward_residual_parity():
     out = O.forward_tokens(cfg, inp["x"], ref_idx, ref_w, np.arange(cfg.T), dw.host)
     ref = O.residual_update(out, h_old, gain_bits, 1e-6, 7)
     check_output(host_bits(resid), ref, TOL_BF16)
+
+
+@pytest.mark.parametrize("T,d", [(7, 64), (300, 5120), (1, 16384)])
+def test_pre_norm_parity(T, d):
+    """Pre-norm of the sublayer input (release article, section "Residual stream"): the FP32
+    kernel against the oracle's exact value rounded to FP32 and then bf16. Reduction order can
+    move an element across a bf16 rounding boundary, so a few elements may differ by one ulp."""
+    h = W.normal_bf16(61, W.TID_AUX, 0, T * d, 2.0).reshape(T, d)
+    gain = W.normal_bf16(61, W.TID_AUX + 1, 0, d, 0.1)
+    gain = torch.from_numpy(W.bf16_to_f32(gain) + 1.0).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    x = torch.full((T, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    bm.moe_pre_norm(bm.Dims(T, d, 1, 1, 1, 1, 64), dev(h), dev(gain), 1e-6, x)
+    torch.cuda.synchronize()
+    got = host_bits(x).astype(np.int32)
+    ref = O.pre_norm(h, gain, 1e-6).astype(np.int32)
+    diff = np.abs(got - ref)  # same-sign bf16 patterns: one ulp = 1
+    assert diff.max() <= 1
+    assert np.count_nonzero(diff) <= max(2, diff.size // 1000)
+
+
+def test_sublayer_parity():
+    """Pre-norm, block forward and post-norm residual update in one call, against the oracle's
+    pre_norm -> route -> forward_tokens -> residual_update on the x the kernel produced."""
+    cfg = TINY.with_tokens(80)
+    inp = W.make_host_inputs(cfg, 29)
+    dw = DeviceWeights(cfg, 29)
+    dims = bm.Dims.from_config(cfg)
+    ws = bm.allocate_workspace(dims)
+    h_old = W.normal_bf16(29, W.TID_AUX + 3, 0, cfg.T * cfg.d, 1.0).reshape(cfg.T, cfg.d)
+
+    def gain(tid):
+        g = W.normal_bf16(29, tid, 0, cfg.d, 0.05)
+        return torch.from_numpy(W.bf16_to_f32(g) + 1.0).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+    pre, post = gain(W.TID_AUX + 4), gain(W.TID_AUX + 5)
+    resid = dev(h_old)
+    x = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device="cuda")
+    idx = torch.empty((cfg.T, cfg.top_k), dtype=torch.int32, device="cuda")
+    bm.moe_sublayer(dims, resid, dev(pre), dev(post), 1e-6, 5, dev(inp["w_r"]), dw.dev, x, ws, topk_idx=idx)
+    torch.cuda.synchronize()
+    assert bm.moe_get_device_status(ws) == bm.MOE_DEV_OK
+    x_h = host_bits(x)
+    ref_x = O.pre_norm(h_old, pre, 1e-6)
+    assert np.abs(x_h.astype(np.int32) - ref_x.astype(np.int32)).max() <= 1
+    orc = O.route(cfg, x_h, inp["w_r"])
+    _, ref_idx, ref_w = compare_routing_idx_only(cfg, idx.cpu().numpy(), orc)
+    out = O.forward_tokens(cfg, x_h, ref_idx, ref_w, np.arange(cfg.T), dw.host)
+    ref = O.residual_update(out, h_old, post, 1e-6, 5)
+    check_output(host_bits(resid), ref, TOL_BF16)
