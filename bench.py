@@ -306,7 +306,11 @@ def run_ours(args, rank, world, local_rank):
     stream = torch.cuda.current_stream()
     setup_s = time.time() - t_setup
 
-    gain = None
+    gain = pre_gain = None
+    if args.sublayer:
+        args.residual = True
+        pre_gain = (1.0 + 0.05 * torch.randn(cfg.d, generator=torch.Generator().manual_seed(args.seed + 2))).to(
+            torch.bfloat16).cuda()
     if args.residual:  # post-norm gain ~ 1 and a unit-RMS residual stream, updated in place each step
         gain = (1.0 + 0.05 * torch.randn(cfg.d, generator=torch.Generator().manual_seed(args.seed))).to(
             torch.bfloat16).cuda()
@@ -314,7 +318,9 @@ def run_ours(args, rank, world, local_rank):
             torch.bfloat16))
 
     def forward(x_, out_, counts_=None):
-        if args.residual:
+        if args.sublayer:  # x_ is the residual stream (updated in place), out_ the pre-norm output
+            bm.moe_sublayer(dims, x_, pre_gain, gain, 1e-6, RESIDUAL_STEP, w_r, weights, out_, ws, counts=counts_)
+        elif args.residual:
             bm.moe_forward_residual(dims, x_, w_r, weights, gain, 1e-6, RESIDUAL_STEP, out_, ws, counts=counts_)
         else:
             bm.moe_forward(dims, x_, w_r, weights, out_, ws, counts=counts_)
@@ -392,7 +398,8 @@ def run_ours(args, rank, world, local_rank):
                     x_dev[1 - b].view(torch.int16).copy_(x_pin, non_blocking=True)
                     h2d[1 - b].record(copy_stream)
                 copy_stream.wait_event(fwd[b])
-                out_pin[b].copy_(out_dev[b].view(torch.int16), non_blocking=True)
+                res_b = x_dev[b] if args.sublayer else out_dev[b]  # the step's result
+                out_pin[b].copy_(res_b.view(torch.int16), non_blocking=True)
                 d2h[b].record(copy_stream)
         with torch.cuda.stream(copy_stream):
             t1.record(copy_stream)
@@ -432,6 +439,7 @@ def run_ours(args, rank, world, local_rank):
                    "top_k": cfg.top_k, "parallelism": f"replicas x{world}",
                    "last_stage": (f"combine fused with post-norm (RMSNorm) and residual update, step k={RESIDUAL_STEP}"
                                   if args.residual else "combine to out"),
+                   "first_stage": ("pre-norm (RMSNorm) of the residual stream" if args.sublayer else "router on x"),
                    "l2": f"no flush: {touched} experts x {3 * cfg.d * cfg.inter * weight_bytes_per_param(cfg) / 1e6:.1f} MB "
                          f"of weights streamed per step exceed the 126 MB L2"},
         "roofline": {"kernel": f"{kname} (GEMM1 + SwiGLU)", "bound": bound,
@@ -452,7 +460,8 @@ def run_ours(args, rank, world, local_rank):
                 "pipelining": "copies on a second stream, double-buffered: step i+1's input and step i-1's "
                               "output move while step i computes"},
         "router_fp32_recomputed_tokens": int(ws[16:20].view(torch.int32).item()) if cfg.T >= ROUTER_TC_MIN_TOKENS else None,
-        "gpu_launches": kernels_per_step(cfg, torch.cuda.get_device_properties(local_rank).multi_processor_count) * K,
+        "gpu_launches": (kernels_per_step(cfg, torch.cuda.get_device_properties(local_rank).multi_processor_count)
+                         + (1 if args.sublayer else 0)) * K,
         "clocks": clk,
         "setup_s": round(setup_s, 1),
     }
@@ -674,6 +683,9 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-tokens", type=int, default=16, help="tokens per reference-arm step")
+    ap.add_argument("--sublayer", action="store_true",
+                    help="run the whole MoE sublayer (moe_sublayer): pre-norm of the residual stream, the block, "
+                         "post-norm and residual update in place")
     ap.add_argument("--residual", action="store_true",
                     help="end the block with the fused post-norm and depth-scaled residual update "
                          "(moe_forward_residual) instead of writing the output")
