@@ -154,3 +154,23 @@ def test_pre_norm_and_sublayer_host_checks(lib):
     big = _dims(d=16384)
     assert lib.moe_sublayer(ctypes.byref(big), fake, fake, fake, 1e-6, 2, fake, None, ctypes.byref(w),
                             ctypes.c_void_p(1 << 30), None, None, fake, ws_bytes, None) == N.MOE_ERR_UNSUPPORTED
+
+
+def test_header_is_plain_c_and_links_against_the_library(tmp_path):
+    """A C program that includes the header, takes the address of every declared call and links
+    against the built library: the boundary needs no C++ and no torch."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("no C compiler")
+    names = declared_functions()
+    src = tmp_path / "use.c"
+    src.write_text('#include "beammoe.h"\n#include <stdio.h>\nint main(void) {\n  const void* f[] = {'
+                   + ", ".join(f"(const void*){n}" for n in names) + "};\n"
+                   '  printf("%d %s\\n", (int)(sizeof f / sizeof f[0]), moe_version());\n  return 0;\n}\n')
+    lib_path = bm.library_path()
+    exe = tmp_path / "use"
+    subprocess.check_call(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), str(src),
+                           "-o", str(exe), lib_path, f"-Wl,-rpath,{os.path.dirname(lib_path)}"])
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
+    assert int(out[0]) == len(names) and "sm_103a" in " ".join(out[1:])
