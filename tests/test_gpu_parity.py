@@ -528,3 +528,53 @@ def test_sublayer_parity():
     out = O.forward_tokens(cfg, x_h, ref_idx, ref_w, np.arange(cfg.T), dw.host)
     ref = O.residual_update(out, h_old, post, 1e-6, 5)
     check_output(host_bits(resid), ref, TOL_BF16)
+
+
+def test_sublayer_fp8_selection_bias():
+    """Every optional piece at once: FP8 expert weights, a selection bias, the pre-norm and the
+    post-norm residual update, on a 16-expert block with 4 groups (T = 100, ragged tiles)."""
+    cfg = dataclasses.replace(SMALL_NVFP4.with_tokens(100), wfmt="fp8")
+    seed = 33
+    wr_h = W.gen_wr(cfg, seed)
+    bias = (0.2 * (W.uniform_f64(seed, W.TID_AUX + 7, 0, cfg.E) - 0.5)).astype(np.float32)
+    dw = DeviceWeights(cfg, seed)
+    dims = bm.Dims.from_config(cfg)
+    ws = bm.allocate_workspace(dims)
+    h_old = W.normal_bf16(seed, W.TID_AUX + 3, 0, cfg.T * cfg.d, 1.0).reshape(cfg.T, cfg.d)
+
+    def gain(tid):
+        g = W.normal_bf16(seed, tid, 0, cfg.d, 0.05)
+        return torch.from_numpy(W.bf16_to_f32(g) + 1.0).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+    pre, post = gain(W.TID_AUX + 4), gain(W.TID_AUX + 5)
+    resid = dev(h_old)
+    x = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device="cuda")
+    idx = torch.empty((cfg.T, cfg.top_k), dtype=torch.int32, device="cuda")
+    bm.moe_sublayer(dims, resid, dev(pre), dev(post), 1e-6, 3, dev(wr_h), dw.dev, x, ws, topk_idx=idx,
+                    sel_bias=dev(bias))
+    torch.cuda.synchronize()
+    assert bm.moe_get_device_status(ws) == bm.MOE_DEV_OK
+    x_h = host_bits(x)
+    assert np.abs(x_h.astype(np.int32) - O.pre_norm(h_old, pre, 1e-6).astype(np.int32)).max() <= 1
+    orc = O.route(cfg, x_h, wr_h, bias=bias)
+    gi = idx.cpu().numpy()
+    sv = np.take_along_axis(orc["scores"].astype(np.float64), gi.astype(np.int64), 1)
+    w_like = (cfg.routed_scale * sv / sv.sum(1, keepdims=True)).astype(np.float32)
+    _, ref_idx, ref_w = compare_routing(cfg, gi, w_like, orc, bias=bias)
+    out = O.forward_tokens(cfg, x_h, ref_idx, ref_w, np.arange(cfg.T), dw.host)
+    ref = O.residual_update(out, h_old, post, 1e-6, 3)
+    check_output(host_bits(resid), ref, TOL_NVFP4)
+
+
+@pytest.mark.parametrize("wfmt", ["bf16", "nvfp4", "fp8"])
+def test_forward_single_token(wfmt):
+    """T = 1: one token, 4 experts of 16 touched, one 16-row token tile per expert."""
+    cfg = dataclasses.replace(SMALL_NVFP4.with_tokens(1), wfmt=wfmt)
+    x_h, wr_h = W.gen_x(cfg, 35), W.gen_wr(cfg, 35)
+    dw = DeviceWeights(cfg, 35)
+    out, idx, counts, _ = run_forward(cfg, dev(x_h), dev(wr_h), dw.dev)
+    orc = O.route(cfg, x_h, wr_h)
+    _, ref_idx, ref_w = compare_routing_idx_only(cfg, idx.cpu().numpy(), orc)
+    assert counts.cpu().numpy().sum() == cfg.top_k
+    ref = O.forward_tokens(cfg, x_h, ref_idx, ref_w, np.arange(1), dw.host)
+    check_output(host_bits(out), ref, TOL_BF16 if wfmt == "bf16" else TOL_NVFP4)
