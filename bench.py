@@ -284,6 +284,38 @@ def roofline_numbers(cfg, touched, peaks):
     return gemm1, gemm2, layer
 
 
+# FP32 FFMA peak of the SIMT router: 148 SMs x 128 FP32 lanes x 2 FLOP x 2.032 GHz (maximum SM clock)
+FP32_ALU_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
+
+
+def stage_rooflines(cfg, stage_ms, peaks, residual=False):
+    """Achieved HBM bandwidth of the router, permute and combine stages from their algorithmic bytes
+    and live durations (ms), and the router's FP32 rate against the FFMA peak.
+    router: x read, W_r read once, indices and weights written;
+    permute: indices read, x read once, x_perm and the two row maps written, counts and offsets;
+    combine: the K expert rows of every token, its weights and rows read, out written (with the
+    residual update also the stream read and the gain)."""
+    T, d, E, K = cfg.T, cfg.d, cfg.E, cfg.top_k
+    R = T * K
+    by = {"router": T * d * 2 + d * E * 4 + R * 8,
+          "permute": R * 4 + T * d * 2 + R * d * 2 + R * 8 + (2 * E + 1) * 4,
+          "combine": R * d * 2 + R * 8 + T * d * 2 + ((T * d * 2 + d * 2) if residual else 0)}
+    ms = {"router": stage_ms[0], "permute": stage_ms[1], "combine": stage_ms[4]}
+    out = {}
+    for k in by:
+        gbs = by[k] / (ms[k] / 1e3) / 1e9
+        out[k] = {"bytes": int(by[k]), "ms": round(ms[k], 4), "achieved_gbs": round(gbs, 1),
+                  "frac_hbm": round(gbs / peaks["hbm_gbs"], 4)}
+    tf = 2.0 * T * d * E / (ms["router"] / 1e3) / 1e12
+    out["router"]["achieved_fp32_tflops"] = round(tf, 2)
+    if T >= ROUTER_TC_MIN_TOKENS:  # logits on the tensor cores (three exact bf16 terms of W_r)
+        out["router"]["path"] = "tensor cores + fp32 recompute of narrow-margin tokens"
+    else:
+        out["router"]["path"] = "fp32 simt"
+        out["router"]["frac_fp32_alu"] = round(tf / FP32_ALU_TFLOPS, 4)
+    return out
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import sparse_moe_layer_14_b300 as bm
@@ -454,6 +486,7 @@ def run_ours(args, rank, world, local_rank):
                       "schedule+gemm1": round(stage_ms[2], 4), "gemm2": round(stage_ms[3], 4),
                       "combine": round(stage_ms[4], 4)},
         "gemm2_roofline": {"bound": g2["bound"], "frac": round(g2["t_roof_s"] / (stage_ms[3] / 1e3), 4)},
+        "stage_rooflines": stage_rooflines(cfg, stage_ms, peaks, residual=args.residual),
         "e2e": {"value": round(world * cfg.T / (e2e_ms / K / 1e3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": cfg.T * cfg.d * 2, "d2h_bytes_per_step": cfg.T * cfg.d * 2,
                 "ms_per_step": round(e2e_ms / K, 4),
