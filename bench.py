@@ -303,9 +303,12 @@ def stage_rooflines(cfg, stage_ms, peaks, residual=False):
     ms = {"router": stage_ms[0], "permute": stage_ms[1], "combine": stage_ms[4]}
     out = {}
     for k in by:
-        gbs = by[k] / (ms[k] / 1e3) / 1e9
-        out[k] = {"bytes": int(by[k]), "ms": round(ms[k], 4), "achieved_gbs": round(gbs, 1),
-                  "frac_hbm": round(gbs / peaks["hbm_gbs"], 4)}
+        gbs = by[k] / (ms[k] / 1e3) / 1e9 if ms[k] > 0 else None
+        out[k] = {"bytes": int(by[k]), "ms": round(float(ms[k]), 4),
+                  "achieved_gbs": None if gbs is None else round(gbs, 1),
+                  "frac_hbm": None if gbs is None else round(gbs / peaks["hbm_gbs"], 4)}
+    if ms["router"] <= 0:
+        return out
     tf = 2.0 * T * d * E / (ms["router"] / 1e3) / 1e12
     out["router"]["achieved_fp32_tflops"] = round(tf, 2)
     if T >= ROUTER_TC_MIN_TOKENS:  # logits on the tensor cores (three exact bf16 terms of W_r)
