@@ -288,7 +288,8 @@ void moe_set_wait_bound(int64_t spins);
  * 1 router, 2 permutation, 3 work-item schedule + expert GEMM1 (SwiGLU),
  * 4 expert GEMM2, 5 combine. cudaEventElapsedTime between consecutive events
  * then gives each stage's device time (moe_dense_mlp records events[0] before
- * its first launch, events[3] after GEMM1 and events[4] after GEMM2). NULL (or
+ * its first launch, events[3] after GEMM1 and events[4] after GEMM2;
+ * moe_sublayer records events[0] after its pre-norm). NULL (or
  * n < 6) turns it off. The
  * setting is process-wide; do not change it while moe_forward calls run on
  * other host threads. */
