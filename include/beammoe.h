@@ -70,6 +70,7 @@ typedef enum {
   MOE_DEV_OK = 0,
   MOE_DEV_BAD_EXPERT = 1,  /* a routing index outside [0, E): the slot is skipped */
   MOE_DEV_BAD_ROW = 2,     /* a permuted-row index outside [0, T*top_k): skipped */
+  MOE_DEV_DUP_EXPERT = 3,  /* a token names one expert in two slots: the slots share one row */
   MOE_DEV_TIMEOUT = 6,     /* a pipeline wait exceeded its bound; the kernel returned early */
   MOE_DEV_ZERO_SUM = 7     /* a token's chosen scores summed to 0: its weights are set to 0 */
 } moe_device_code_t;
@@ -136,7 +137,11 @@ moe_status_t moe_route(const moe_dims_t* dims, const moe_bf16_t* x, const float*
  * permuted row (rows of expert e are offsets[e]..offsets[e+1]-1, tokens
  * ascending); inv_row [T*top_k]: permuted row of token t's slot k at
  * t*top_k+k; x_perm [T*top_k][d] bf16: x[row_token[r]] for every row r.
- * Indices outside [0, E) latch MOE_DEV_BAD_EXPERT and are dropped. */
+ * Indices outside [0, E) latch MOE_DEV_BAD_EXPERT and are dropped. A token
+ * that names the same expert in two slots (the router never does) latches
+ * MOE_DEV_DUP_EXPERT: both slots get one shared row (inv_row equal), counts
+ * count the token once, so offsets[E] = T*top_k minus the repeats; a combine
+ * over inv_row still adds that row once per slot. */
 moe_status_t moe_permute(const moe_dims_t* dims, const moe_bf16_t* x, const int32_t* topk_idx,
                          int32_t* counts, int32_t* offsets, int32_t* row_token, int32_t* inv_row,
                          moe_bf16_t* x_perm, void* ws, size_t ws_bytes, void* stream);
@@ -190,7 +195,8 @@ moe_status_t moe_forward(const moe_dims_t* dims, const moe_bf16_t* x, const floa
  * every call clears its status word and bitmap first, and calls that overlap
  * on the GPU (other streams, other host threads) race on it -- issue them on
  * one stream. device_status (device int32, nullable) receives this call's
- * moe_device_code_t (MOE_DEV_BAD_EXPERT if an index was out of range). */
+ * moe_device_code_t (MOE_DEV_BAD_EXPERT if an index was out of range,
+ * MOE_DEV_DUP_EXPERT if a token repeated an expert; MOE_DEV_OK when T == 0). */
 moe_status_t moe_permute_noalloc(const moe_dims_t* dims, const moe_bf16_t* x, const int32_t* topk_idx,
                                  int32_t* counts, int32_t* offsets, int32_t* row_token, int32_t* inv_row,
                                  moe_bf16_t* x_perm, int32_t* device_status, void* stream);
@@ -277,7 +283,9 @@ moe_status_t moe_dense_mlp(const moe_dims_t* dims, const moe_bf16_t* x, const mo
 moe_status_t moe_get_device_status(void* ws, void* stream, int32_t clear, int32_t* code);
 
 /* Test hook: bound (in spin iterations) of every pipeline wait in the expert
- * GEMM kernels of later calls in this process; 0 restores the default. A
+ * GEMM kernels and in the tensor-core router (its logits kernel and the FP32
+ * recompute of narrow-margin tokens) of later calls in this process; 0
+ * restores the default. A
  * bound of 1 makes a wait give up almost at once, which exercises the
  * timeout path (MOE_DEV_TIMEOUT) without faulting or hanging the GPU. */
 void moe_set_wait_bound(int64_t spins);

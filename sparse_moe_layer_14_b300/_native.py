@@ -14,7 +14,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
                 4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE_STATUS", 6: "MOE_ERR_DEVICE_TIMEOUT",
                 7: "MOE_ERR_SCRATCH_LIMIT"}
 # moe_device_code_t
-MOE_DEV_OK, MOE_DEV_BAD_EXPERT, MOE_DEV_BAD_ROW, MOE_DEV_TIMEOUT, MOE_DEV_ZERO_SUM = 0, 1, 2, 6, 7
+MOE_DEV_OK, MOE_DEV_BAD_EXPERT, MOE_DEV_BAD_ROW, MOE_DEV_DUP_EXPERT, MOE_DEV_TIMEOUT, MOE_DEV_ZERO_SUM = 0, 1, 2, 3, 6, 7
 # moe_wfmt_t
 MOE_W_BF16, MOE_W_NVFP4, MOE_W_FP8 = 0, 1, 2
 

@@ -14,6 +14,7 @@
 // so each call clears what must start at zero (its status word and, inside
 // the permutation launch, the bitmap), and calls that overlap on the GPU race
 // on it (run them on one stream).
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -31,14 +32,26 @@ constexpr size_t kScratchBytes = 256 + 2 * kNoAllocWords * sizeof(uint32_t);
 static __device__ __align__(256) uint8_t g_permute_scratch[kScratchBytes];
 
 // Host code cannot use the array's name as a device address (it names a
-// host-side stand-in), so its device address is looked up once per device.
+// host-side stand-in), so its device address is looked up per device and
+// kept once the lookup has succeeded; a failed lookup is tried again on the
+// next call.
 constexpr int kMaxDevices = 64;
 struct DeviceScratch {
-  std::once_flag once;
-  void* ptr = nullptr;
-  cudaError_t err = cudaSuccess;
+  std::mutex lock;
+  std::atomic<void*> ptr{nullptr};
 };
 DeviceScratch g_scratch[kMaxDevices];
+
+void* scratch_address(int dev) {
+  DeviceScratch& s = g_scratch[dev];
+  void* p = s.ptr.load(std::memory_order_acquire);
+  if (p) return p;
+  std::lock_guard<std::mutex> guard(s.lock);
+  p = s.ptr.load(std::memory_order_relaxed);
+  if (!p && cudaGetSymbolAddress(&p, g_permute_scratch) == cudaSuccess && p)
+    s.ptr.store(p, std::memory_order_release);
+  return p;
+}
 
 moe_status_t check_permute_dims(const moe_dims_t* d) {
   if (!d) return MOE_ERR_INVALID_ARG;
@@ -63,19 +76,23 @@ extern "C" moe_status_t moe_permute_noalloc(const moe_dims_t* dims, const moe_bf
   moe_status_t st = check_permute_dims(dims);
   if (st != MOE_OK) return st;
   if (dims->T > kNoAllocMaxT || dims->E > kNoAllocMaxE) return MOE_ERR_SCRATCH_LIMIT;
-  if (dims->T == 0) return MOE_OK;
+  if (dims->T == 0) {  // nothing to permute; the caller's status word still reports this call
+    if (device_status &&
+        cudaMemsetAsync(device_status, 0, sizeof(int32_t), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    return MOE_OK;
+  }
   if (!aligned16(x) || !topk_idx || !counts || !offsets || !row_token || !inv_row || !aligned16(x_perm))
     return MOE_ERR_INVALID_ARG;
 
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return MOE_ERR_CUDA;
   if (dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
-  DeviceScratch& s = g_scratch[dev];
-  std::call_once(s.once, [&s] { s.err = cudaGetSymbolAddress(&s.ptr, g_permute_scratch); });
-  if (s.err != cudaSuccess || !s.ptr) return MOE_ERR_CUDA;
+  void* scratch = scratch_address(dev);
+  if (!scratch) return MOE_ERR_CUDA;
 
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  uint8_t* base = static_cast<uint8_t*>(s.ptr);
+  uint8_t* base = static_cast<uint8_t*>(scratch);
   int32_t* status = reinterpret_cast<int32_t*>(base);
   uint32_t* bitmap = reinterpret_cast<uint32_t*>(base + 256);
   int32_t* word_prefix = reinterpret_cast<int32_t*>(base + 256 + kNoAllocWords * sizeof(uint32_t));

@@ -28,7 +28,10 @@ __global__ void bitmap_kernel(const int32_t* __restrict__ idx, int T, int E, int
     latch_status(status, MOE_DEV_BAD_EXPERT);
     return;
   }
-  atomicOr(bitmap + static_cast<size_t>(e) * nw + (t >> 5), 1u << (t & 31));
+  const uint32_t bit = 1u << (t & 31);
+  // a bit already set means another slot of this token named the same expert
+  if (atomicOr(bitmap + static_cast<size_t>(e) * nw + (t >> 5), bit) & bit)
+    latch_status(status, MOE_DEV_DUP_EXPERT);
 }
 
 // One block per expert: word_prefix[e][w] = set bits of column e before word w.

@@ -168,6 +168,35 @@ def test_permute_bad_expert_latched():
     assert offsets.cpu().numpy()[-1] == R - 2
 
 
+def test_permute_duplicate_expert_latched():
+    """A token that names one expert in two slots latches MOE_DEV_DUP_EXPERT; both slots share
+    one row, the counts take the token once, and every other row is still exact."""
+    T, E, K, d = 40, 16, 4, 64
+    idx_h = W.random_topk(13, T, E, K)
+    idx_h[7, 3] = idx_h[7, 1]
+    x_h = W.normal_bf16(13, W.TID_X, 0, T * d, 1.0).reshape(T, d)
+    dims = bm.Dims(T, d, E, 1, 1, K, 64)
+    ws = bm.allocate_workspace(dims)
+    R = T * K
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    row_token = torch.full((R,), -7, dtype=torch.int32, device="cuda")
+    inv_row = torch.empty(R, dtype=torch.int32, device="cuda")
+    x_perm = torch.zeros((R, d), dtype=torch.bfloat16, device="cuda")
+    bm.moe_permute(dims, dev(x_h), dev(idx_h), counts, offsets, row_token, inv_row, x_perm, ws)
+    assert bm.moe_get_device_status(ws, clear=True) == bm.MOE_DEV_DUP_EXPERT
+    ir = inv_row.cpu().numpy().reshape(T, K)
+    assert ir[7, 1] == ir[7, 3] >= 0
+    assert offsets.cpu().numpy()[-1] == R - 1
+    # the routing with the repeat removed (slot 3 of token 7 dropped) gives the same rows
+    c = np.bincount(np.delete(idx_h.ravel(), 7 * K + 3), minlength=E)
+    assert np.array_equal(counts.cpu().numpy(), c)
+    pairs = sorted({(int(e), t) for t in range(T) for e in idx_h[t]})  # rows ordered by (expert, token)
+    rt = np.array([t for _, t in pairs], np.int32)
+    assert np.array_equal(row_token.cpu().numpy()[:R - 1], rt)
+    assert np.array_equal(host_bits(x_perm)[:R - 1], x_h[rt])
+
+
 # ---------------------------------------------------------------------------------------- experts
 
 def _ffn_case(d, inter, E, T, K, counts_list, seed, wfmt="bf16"):

@@ -66,3 +66,16 @@ def test_noalloc_refuses_sizes_beyond_its_scratch():
     dims = N.MoeDims(16385, 128, 16, 1, 1, 4, 64, 2.5, 0)
     rc = lib.moe_permute_noalloc(ctypes.byref(dims), fake, fake, fake, fake, fake, fake, fake, None, None)
     assert rc == N.MOE_ERR_SCRATCH_LIMIT
+
+
+def test_noalloc_empty_call_reports_ok():
+    """T = 0 permutes nothing but still writes MOE_DEV_OK to the caller's status word."""
+    lib = N.load()
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    dims = N.MoeDims(0, 128, 16, 1, 1, 4, 64, 2.5, 0)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    rc = lib.moe_permute_noalloc(ctypes.byref(dims), None, None, None, None, None, None, None,
+                                 ctypes.c_void_p(status.data_ptr()), stream)
+    assert rc == N.MOE_OK
+    torch.cuda.synchronize()
+    assert int(status.item()) == bm.MOE_DEV_OK
