@@ -319,27 +319,21 @@ def stage_rooflines(cfg, stage_ms, peaks, residual=False):
     return out
 
 
-def run_ours(args, rank, world, local_rank):
+def measure_block(args, cfg, weights, host_w, rank, world, local_rank, peaks, want_cpu, x_h, wr_h):
+    """Time moe_forward (or the residual / sublayer variants) on one batch of `cfg` with the
+    expert weights already resident: W warm-up steps, K timed steps between barriers, stage
+    events, clocks, the end-to-end run with host copies, and (rank 0, one GPU) the oracle on a
+    token sample with its parity against this run's output. Returns the JSON record (rank 0)."""
     import torch
     import sparse_moe_layer_14_b300 as bm
 
-    torch.cuda.set_device(local_rank)
-    cfg = workload_cfg(args.workload)
-    peaks = load_peaks()
-    want_cpu = (rank == 0 and world == 1 and not args.no_cpu_baseline)
     dims = bm.Dims.from_config(cfg)
-
-    t_setup = time.time()
-    weights, host_w = make_device_weights(cfg, args.seed, torch, keep_host=want_cpu)
-    x_h = W.gen_x(cfg, args.seed + 1000 * rank)
-    wr_h = W.gen_wr(cfg, args.seed)
     x = torch.from_numpy(x_h).view(torch.int16).view(torch.bfloat16).cuda()
     w_r = torch.from_numpy(wr_h).cuda()
     out = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device="cuda")
     counts = torch.empty(cfg.E, dtype=torch.int32, device="cuda")
     ws = bm.allocate_workspace(dims)
     stream = torch.cuda.current_stream()
-    setup_s = time.time() - t_setup
 
     gain = pre_gain = None
     if args.sublayer:
@@ -352,13 +346,13 @@ def run_ours(args, rank, world, local_rank):
         out.copy_(torch.randn((cfg.T, cfg.d), generator=torch.Generator().manual_seed(args.seed + 1)).to(
             torch.bfloat16))
 
-    def forward(x_, out_, counts_=None):
+    def forward(x_, out_, counts_=None, idx_=None):
         if args.sublayer:  # x_ is the residual stream (updated in place), out_ the pre-norm output
             bm.moe_sublayer(dims, x_, pre_gain, gain, 1e-6, RESIDUAL_STEP, w_r, weights, out_, ws, counts=counts_)
         elif args.residual:
             bm.moe_forward_residual(dims, x_, w_r, weights, gain, 1e-6, RESIDUAL_STEP, out_, ws, counts=counts_)
         else:
-            bm.moe_forward(dims, x_, w_r, weights, out_, ws, counts=counts_)
+            bm.moe_forward(dims, x_, w_r, weights, out_, ws, counts=counts_, topk_idx=idx_)
 
     def step():
         forward(x, out, counts)
@@ -399,6 +393,7 @@ def run_ours(args, rank, world, local_rank):
     if bm.moe_get_device_status(ws) != bm.MOE_DEV_OK:
         raise RuntimeError("device status set during the timed region")
     clk = clocks.summary(wall0, wall1) if clocks else None
+    recomputed = int(ws[16:20].view(torch.int32).item()) if cfg.T >= ROUTER_TC_MIN_TOKENS else None
 
     # end to end through the public API: every step copies its x from pinned host memory to the
     # device, runs moe_forward and copies its output back to pinned host memory. The copies run on
@@ -465,10 +460,12 @@ def run_ours(args, rank, world, local_rank):
     kname = {"bf16": "expert_gemm_kernel<GLU>", "nvfp4": "expert_gemm_kernel<GLU, NVFP4>",
              "fp8": "expert_gemm_kernel<GLU, FP8>"}[cfg.wfmt]
     traffic, traffic_src = profiled_traffic(cfg.name, kname, g1["bytes"])
-    line = {
+    rec = {
         "metric": METRIC, "value": round(tokens_per_s, 1), "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16" if cfg.wfmt == "bf16" else f"bf16 ({cfg.wfmt.upper()} weights decoded to bf16)", "data": "synthetic (seeded N(0,1) activations, N(0,1/fan_in) weights)",
+        "vs_baseline": None,
+        "dtype": "bf16" if cfg.wfmt == "bf16" else f"bf16 ({cfg.wfmt.upper()} weights decoded to bf16)",
+        "data": "synthetic (seeded N(0,1) activations, N(0,1/fan_in) weights)",
         "impl": "ours",
         "config": {"workload": describe(cfg), "T": cfg.T, "d": cfg.d, "E": cfg.E, "inter": cfg.inter,
                    "top_k": cfg.top_k, "parallelism": f"replicas x{world}",
@@ -480,11 +477,12 @@ def run_ours(args, rank, world, local_rank):
         "roofline": {"kernel": f"{kname} (GEMM1 + SwiGLU)", "bound": bound,
                      "achieved": round(achieved, 1), "peak": peak, "unit": unit, "frac": round(achieved / peak, 4),
                      "peak_source": f"{peaks['source']} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops'})",
-                     "traffic": traffic, "traffic_source": traffic_src, "algorithmic_bytes": g1["bytes"], "algorithmic_flops": g1["flops"],
-                     "avg_launch_ms": round(stage_ms[2], 4)},
+                     "traffic": traffic, "traffic_source": traffic_src, "algorithmic_bytes": g1["bytes"],
+                     "algorithmic_flops": g1["flops"], "avg_launch_ms": round(stage_ms[2], 4)},
         "layer_roofline": {"bound": layer["bound"], "roofline_ms": round(layer["t_roof_s"] * 1e3, 4),
-                           "frac": round(layer["t_roof_s"] * 1e3 / ms_per_step, 4), "algorithmic_bytes": layer["bytes"],
-                           "algorithmic_flops": layer["flops"], "experts_touched": touched},
+                           "frac": round(layer["t_roof_s"] * 1e3 / ms_per_step, 4),
+                           "algorithmic_bytes": layer["bytes"], "algorithmic_flops": layer["flops"],
+                           "experts_touched": touched},
         "stages_ms": {"router": round(stage_ms[0], 4), "permute": round(stage_ms[1], 4),
                       "schedule+gemm1": round(stage_ms[2], 4), "gemm2": round(stage_ms[3], 4),
                       "combine": round(stage_ms[4], 4)},
@@ -495,14 +493,51 @@ def run_ours(args, rank, world, local_rank):
                 "ms_per_step": round(e2e_ms / K, 4),
                 "pipelining": "copies on a second stream, double-buffered: step i+1's input and step i-1's "
                               "output move while step i computes"},
-        "router_fp32_recomputed_tokens": int(ws[16:20].view(torch.int32).item()) if cfg.T >= ROUTER_TC_MIN_TOKENS else None,
+        "router_fp32_recomputed_tokens": recomputed,
         "gpu_launches": (kernels_per_step(cfg, torch.cuda.get_device_properties(local_rank).multi_processor_count)
                          + (1 if args.sublayer else 0)) * K,
         "clocks": clk,
-        "setup_s": round(setup_s, 1),
     }
     if want_cpu:
-        line["cpu_baseline"] = cpu_baseline(cfg, args, x_h, wr_h, host_w)
+        idx = None
+        if not args.residual:  # the routing of this batch, for the parity report (after the timed region)
+            idx = torch.empty((cfg.T, cfg.top_k), dtype=torch.int32, device="cuda")
+            forward(x, out, None, idx)
+            torch.cuda.synchronize()
+        got = out.view(torch.int16).cpu().numpy().view(np.uint16)
+        rec["cpu_baseline"] = cpu_baseline(cfg, args, x_h, wr_h, host_w,
+                                           gpu=None if idx is None else (idx.cpu().numpy(), got))
+    del ws
+    torch.cuda.empty_cache()
+    return rec
+
+
+def run_ours(args, rank, world, local_rank):
+    """The --workload batch; with the default decode workload, also the prefill batch (T=4096)
+    on the same resident weights, reported as the `prefill` sub-record of the same line."""
+    import torch
+
+    torch.cuda.set_device(local_rank)
+    cfg = workload_cfg(args.workload)
+    peaks = load_peaks()
+    want_cpu = (rank == 0 and world == 1 and not args.no_cpu_baseline)
+    t_setup = time.time()
+    weights, host_w = make_device_weights(cfg, args.seed, torch, keep_host=want_cpu)
+    wr_h = W.gen_wr(cfg, args.seed)
+    setup_s = time.time() - t_setup
+    line = measure_block(args, cfg, weights, host_w, rank, world, local_rank, peaks, want_cpu,
+                         W.gen_x(cfg, args.seed + 1000 * rank), wr_h)
+    if args.workload == "decode" and not args.no_prefill:
+        pcfg = W.CONFIGS["prefill"]  # the same layer (weights, router) with T = 4096
+        sub = measure_block(args, pcfg, weights, host_w, rank, world, local_rank, peaks, want_cpu,
+                            W.gen_x(pcfg, args.seed + 1000 * rank), W.gen_wr(pcfg, args.seed))
+        if line is not None:
+            for k in ("metric", "n_gpus", "steps", "warmup", "higher_is_better", "scaling", "vs_baseline", "dtype",
+                      "data", "impl"):
+                sub.pop(k, None)
+            line["prefill"] = sub
+    if line is not None:
+        line["setup_s"] = round(setup_s, 1)
     return line
 
 
@@ -660,18 +695,44 @@ def cpu_sample_tokens(cfg):
     return min(cfg.T, 64)
 
 
-def cpu_baseline(cfg, args, x_h, wr_h, host_w, n_tok=None):
-    """The CPU oracle, as it stands, on a bounded token sample of the same workload."""
+def cpu_baseline(cfg, args, x_h, wr_h, host_w, n_tok=None, gpu=None):
+    """The CPU oracle, as it stands, on a bounded token sample of the same workload (timed), then
+    its parity against the GPU run on those tokens: gpu = (topk_idx [T, K], out [T, d] bf16 bits)
+    of the timed batch. Routing must match outside near-ties (margins below 1e-6, counted and
+    excluded); the output error is reported against the bar of the weight format."""
     import oracle as O
     n = n_tok or cpu_sample_tokens(cfg)
     sub = cfg.with_tokens(n)
+    toks = np.linspace(0, cfg.T - 1, n).astype(np.int64) if n < cfg.T else np.arange(cfg.T)
+    xs = np.ascontiguousarray(x_h[toks])
     t0 = time.time()
-    r = O.route(sub, x_h[:n], wr_h)
-    O.forward_tokens(sub, x_h[:n], r["idx"], r["w"], np.arange(n), host_w)
+    r = O.route(sub, xs, wr_h)
+    ref = O.forward_tokens(sub, xs, r["idx"], r["w"], np.arange(n), host_w)
     dt = time.time() - t0
-    return {"value": round(n / dt, 3), "unit": "tokens/s", "cores": O.num_threads(), "kind": "oracle",
-            "sample": f"first {n} of the {cfg.T} tokens of the same seeded batch (routing + all {cfg.top_k} experts "
-                      f"per token + combine, fp64 accumulation)", "seconds": round(dt, 2)}
+    rec = {"value": round(n / dt, 3), "unit": "tokens/s", "cores": O.num_threads(), "kind": "oracle",
+           "sample": f"{n} of the {cfg.T} tokens of the same seeded batch, evenly spaced (routing + all "
+                     f"{cfg.top_k} experts per token + combine, fp64 accumulation)", "seconds": round(dt, 2)}
+    if gpu is not None:
+        gi, got = gpu[0][toks], gpu[1][toks]
+        near = (r["margin_group"] < 1e-6) | (r["margin_expert"] < 1e-6)
+        mism = int(np.sum(np.any(np.sort(gi[~near], 1) != np.sort(r["idx"][~near], 1), axis=1)))
+        # near-tie tokens: the reference output under the GPU's choice (checked only for validity in the tests)
+        idx_ref, w_ref = r["idx"].copy(), r["w"].copy()
+        s = r["scores"].astype(np.float64)
+        for t in np.nonzero(near)[0]:
+            idx_ref[t] = gi[t]
+            w_ref[t] = cfg.routed_scale * s[t, gi[t]] / s[t, gi[t]].sum()
+        if near.any():
+            ref = O.forward_tokens(sub, xs, idx_ref, w_ref, np.arange(n), host_w)
+        g = W.bf16_to_f32(got).astype(np.float64)
+        rms = float(np.sqrt(np.mean(ref ** 2)))
+        e = np.abs(g - ref)
+        bar = {"bf16": 2e-2, "nvfp4": 5e-2, "fp8": 3e-2}[cfg.wfmt]
+        rec["parity"] = {"tokens": int(n), "routing_mismatches": mism, "excluded_near_ties": int(near.sum()),
+                         "max_err_over_rms": round(float(e.max()) / rms, 6),
+                         "rms_err_over_rms": round(float(np.sqrt(np.mean(e ** 2))) / rms, 6), "bar": bar,
+                         "ok": bool(mism == 0 and e.max() <= bar * rms)}
+    return rec
 
 
 def run_reference(args):
@@ -718,6 +779,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="with the default decode workload, skip the prefill (T=4096) sub-record")
     ap.add_argument("--ref-tokens", type=int, default=16, help="tokens per reference-arm step")
     ap.add_argument("--sublayer", action="store_true",
                     help="run the whole MoE sublayer (moe_sublayer): pre-norm of the residual stream, the block, "

@@ -26,3 +26,13 @@ def wl():
 
     workload.lib()
     return workload
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Print what the parity checks logged: excluded near-ties and error ratios per case."""
+    support = sys.modules.get("support")
+    lines = getattr(support, "REPORT", None) if support else None
+    if lines:
+        terminalreporter.section("parity report")
+        for line in lines:
+            terminalreporter.write_line(line)

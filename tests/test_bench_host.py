@@ -112,3 +112,31 @@ def test_stage_roofline_arithmetic():
     assert "frac_fp32_alu" not in st["router"]  # T = 4096 routes on the tensor cores
     dec = bench.stage_rooflines(W.CONFIGS["decode"], [0.0474, 0.0213, 1.68, 0.83, 0.0079], peaks)
     assert 0.04 < dec["router"]["frac_fp32_alu"] < 0.05
+
+
+def test_cpu_baseline_parity_report():
+    """The bench's CPU-baseline leg times the oracle on a token sample and reports parity against
+    the GPU run's routing and output: fed the oracle's own routing and its output rounded to bf16,
+    it must report no mismatch and an error within the bf16 rounding; a routing with one token's
+    experts changed must count one mismatch."""
+    import numpy as np
+    import oracle as O
+    cfg = W.CONFIGS["tiny"]
+    inp = W.make_host_inputs(cfg, 3)
+    r = O.route(cfg, inp["x"], inp["w_r"])
+    out = O.forward_tokens(cfg, inp["x"], r["idx"], r["w"], np.arange(cfg.T), inp)
+    bits = torch.from_numpy(out.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+    class A:
+        pass
+    rec = bench.cpu_baseline(cfg, A(), inp["x"], inp["w_r"], inp, n_tok=16, gpu=(r["idx"], bits))
+    p = rec["parity"]
+    assert p["tokens"] == 16 and p["routing_mismatches"] == 0 and p["ok"]
+    assert p["max_err_over_rms"] <= 2.0 ** -8 * np.abs(out).max() / np.sqrt(np.mean(out ** 2))
+    decided = np.nonzero((r["margin_group"] >= 1e-6) & (r["margin_expert"] >= 1e-6))[0]
+    bad = r["idx"].copy()
+    t = int(decided[0])
+    bad[t] = (bad[t] + 1) % cfg.E  # a different expert set for one sampled token (token 0 is sampled)
+    assert t == 0
+    rec2 = bench.cpu_baseline(cfg, A(), inp["x"], inp["w_r"], inp, n_tok=16, gpu=(bad, bits))
+    assert rec2["parity"]["routing_mismatches"] == 1 and not rec2["parity"]["ok"]

@@ -7,7 +7,7 @@ import torch
 import oracle as O
 import workload as W
 import sparse_moe_layer_14_b300 as bm
-from support import TOL_BF16, TOL_NVFP4, DeviceWeights, check_output, dev, host_bits
+from support import TOL, DeviceWeights, check_output, dev, host_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -28,7 +28,7 @@ def _run(cfg, seed, rows=None):
     rows = np.arange(cfg.T) if rows is None else rows
     ref = O.ffn_rows(np.zeros(rows.size, np.int32), x_h[rows], dw.host, cfg.d, cfg.inter, cfg.wfmt)
     got = host_bits(out)[rows]
-    err, rms = check_output(got, ref, TOL_BF16 if cfg.wfmt == "bf16" else TOL_NVFP4)
+    err, rms = check_output(got, ref, TOL[cfg.wfmt])
     return got, ref
 
 
