@@ -90,6 +90,13 @@ PROFILE_CASES = {
     # the FP8 prefill shape with 32 experts (1.3 GB of FP8 weights)
     "profile_fp8": W.MoEConfig("profile_fp8", T=512, d=5120, E=32, n_groups=8, topk_groups=4, top_k=8,
                                inter=2560, wfmt="fp8"),
+    # the router, permutation and combine of the decode and prefill workloads exactly (d = 5120, 256
+    # experts in 8 groups of 32, top-4 groups, top-8) with a 64-wide intermediate, so the experts
+    # hold 0.5 GB instead of 20 GB: for captures of the small stages
+    "profile_stages_decode": W.MoEConfig("profile_stages_decode", T=64, d=5120, E=256, n_groups=8, topk_groups=4,
+                                         top_k=8, inter=64),
+    "profile_stages_prefill": W.MoEConfig("profile_stages_prefill", T=4096, d=5120, E=256, n_groups=8,
+                                          topk_groups=4, top_k=8, inter=64),
 }
 
 # Dense SwiGLU MLP of the first decoder layers. The pages give no intermediate size for them;
@@ -103,7 +110,7 @@ RESIDUAL_STEP = 10  # the residual-addition index k used with --residual (weight
 
 DEFAULT_STEPS = {"dense_prefill": 100, "decode": 300, "prefill": 200, "skewed": 40, "nvfp4": 200, "fp8": 200,
                  "profile_decode": 20, "profile_prefill": 20, "profile_dense": 20, "profile_nvfp4": 20,
-                 "profile_fp8": 20}
+                 "profile_fp8": 20, "profile_stages_decode": 20, "profile_stages_prefill": 20}
 
 
 def workload_cfg(name):
@@ -273,7 +280,7 @@ def roofline_numbers(cfg, touched, peaks):
     bpp = weight_bytes_per_param(cfg)
     w_bytes_expert = 3 * d * I * bpp
     gemm1 = {"bytes": touched * 2 * I * d * bpp + R * d * 2 + R * I * 2, "flops": 2.0 * R * d * 2 * I}
-    gemm2 = {"bytes": touched * d * I * bpp + R * I * 2 + R * d * 2, "flops": 2.0 * R * I * d}
+    gemm2 = {"bytes": touched * d * I * bpp + R * I * 2 + R * d * 4, "flops": 2.0 * R * I * d}
     layer = {"bytes": touched * w_bytes_expert + d * E * 4 + cfg.T * d * 2 * 2,
              "flops": 2.0 * R * 3 * d * I + 2.0 * cfg.T * d * E}
     for x in (gemm1, gemm2, layer):
@@ -293,13 +300,13 @@ def stage_rooflines(cfg, stage_ms, peaks, residual=False):
     and live durations (ms), and the router's FP32 rate against the FFMA peak.
     router: x read, W_r read once, indices and weights written;
     permute: indices read, x read once, x_perm and the two row maps written, counts and offsets;
-    combine: the K expert rows of every token, its weights and rows read, out written (with the
-    residual update also the stream read and the gain)."""
+    combine: the K FP32 expert rows of every token, its weights and rows read, out written (with
+    the residual update also the stream read and the gain)."""
     T, d, E, K = cfg.T, cfg.d, cfg.E, cfg.top_k
     R = T * K
     by = {"router": T * d * 2 + d * E * 4 + R * 8,
           "permute": R * 4 + T * d * 2 + R * d * 2 + R * 8 + (2 * E + 1) * 4,
-          "combine": R * d * 2 + R * 8 + T * d * 2 + ((T * d * 2 + d * 2) if residual else 0)}
+          "combine": R * d * 4 + R * 8 + T * d * 2 + ((T * d * 2 + d * 2) if residual else 0)}
     ms = {"router": stage_ms[0], "permute": stage_ms[1], "combine": stage_ms[4]}
     out = {}
     for k in by:
@@ -374,25 +381,36 @@ def measure_block(args, cfg, weights, host_w, rank, world, local_rank, peaks, wa
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    # timed region: K steps back to back (the block's kernels launch with programmatic
+    # dependencies, so nothing is recorded between them here)
     wall0 = time.time()
     start.record(stream)
     for i in range(K):
-        bm.moe_set_stage_events(ev_sets[i])
         step()
     end.record(stream)
     torch.cuda.synchronize()
     wall1 = time.time()
     if world > 1:
         torch.distributed.barrier()
-    bm.moe_set_stage_events(None)
     elapsed_ms = max_over_ranks(start.elapsed_time(end), world, "cuda")
+    # stage-timed region: K more steps with a CUDA event recorded on the stream between stages
+    # (router, permutation, schedule + GEMM1, GEMM2, combine); the events serialise the launches
+    # at the stage boundaries, so these times are an upper bound on each stage's share
+    for i in range(K):
+        bm.moe_set_stage_events(ev_sets[i])
+        step()
+    torch.cuda.synchronize()
+    wall2 = time.time()
+    bm.moe_set_stage_events(None)
     stage_ms = np.zeros(5)
     for evs in ev_sets:
         stage_ms += np.array([evs[j].elapsed_time(evs[j + 1]) for j in range(5)])
     stage_ms /= K
+    staged_step_ms = float(np.mean([evs[0].elapsed_time(evs[5]) for evs in ev_sets]))
     if bm.moe_get_device_status(ws) != bm.MOE_DEV_OK:
         raise RuntimeError("device status set during the timed region")
     clk = clocks.summary(wall0, wall1) if clocks else None
+    clk_staged = clocks.summary(wall1, wall2) if clocks else None
     recomputed = int(ws[16:20].view(torch.int32).item()) if cfg.T >= ROUTER_TC_MIN_TOKENS else None
 
     # end to end through the public API: every step copies its x from pinned host memory to the
@@ -478,14 +496,20 @@ def measure_block(args, cfg, weights, host_w, rank, world, local_rank, peaks, wa
                      "achieved": round(achieved, 1), "peak": peak, "unit": unit, "frac": round(achieved / peak, 4),
                      "peak_source": f"{peaks['source']} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops'})",
                      "traffic": traffic, "traffic_source": traffic_src, "algorithmic_bytes": g1["bytes"],
-                     "algorithmic_flops": g1["flops"], "avg_launch_ms": round(stage_ms[2], 4)},
+                     "algorithmic_flops": g1["flops"], "avg_launch_ms": round(stage_ms[2], 4),
+                     "duration_from": "CUDA events on the launching stream around schedule + GEMM1, stage-timed "
+                                      "pass (the schedule kernel, ~0.01 ms, is included: a lower bound on frac)"},
         "layer_roofline": {"bound": layer["bound"], "roofline_ms": round(layer["t_roof_s"] * 1e3, 4),
                            "frac": round(layer["t_roof_s"] * 1e3 / ms_per_step, 4),
                            "algorithmic_bytes": layer["bytes"], "algorithmic_flops": layer["flops"],
                            "experts_touched": touched},
         "stages_ms": {"router": round(stage_ms[0], 4), "permute": round(stage_ms[1], 4),
                       "schedule+gemm1": round(stage_ms[2], 4), "gemm2": round(stage_ms[3], 4),
-                      "combine": round(stage_ms[4], 4)},
+                      "combine": round(stage_ms[4], 4), "step_with_stage_events": round(staged_step_ms, 4),
+                      "how": "CUDA events between stages in a second timed pass of the same K steps (the "
+                             "events serialise the launches at stage boundaries); clocks of that pass: "
+                             + ("n/a" if not clk_staged else f"{clk_staged.get('sm_mhz')} MHz median, "
+                                f"reasons {clk_staged.get('reasons')}")},
         "gemm2_roofline": {"bound": g2["bound"], "frac": round(g2["t_roof_s"] / (stage_ms[3] / 1e3), 4)},
         "stage_rooflines": stage_rooflines(cfg, stage_ms, peaks, residual=args.residual),
         "e2e": {"value": round(world * cfg.T / (e2e_ms / K / 1e3), 1), "unit": "tokens/s",
@@ -576,13 +600,16 @@ def run_dense(args, rank, world, local_rank):
     wall0 = time.time()
     start.record(stream)
     for i in range(K):
-        bm.moe_set_stage_events(ev_sets[i])
         bm.moe_dense_mlp(dims, x, weights, out, ws)
     end.record(stream)
     torch.cuda.synchronize()
     wall1 = time.time()
     if world > 1:
         torch.distributed.barrier()
+    for i in range(K):  # stage-timed pass: events around GEMM1 and GEMM2
+        bm.moe_set_stage_events(ev_sets[i])
+        bm.moe_dense_mlp(dims, x, weights, out, ws)
+    torch.cuda.synchronize()
     bm.moe_set_stage_events(None)
     if bm.moe_get_device_status(ws) != bm.MOE_DEV_OK:
         raise RuntimeError("device status set during the timed region")
@@ -727,7 +754,7 @@ def cpu_baseline(cfg, args, x_h, wr_h, host_w, n_tok=None, gpu=None):
         g = W.bf16_to_f32(got).astype(np.float64)
         rms = float(np.sqrt(np.mean(ref ** 2)))
         e = np.abs(g - ref)
-        bar = {"bf16": 2e-2, "nvfp4": 5e-2, "fp8": 3e-2}[cfg.wfmt]
+        bar = {"bf16": 2e-2, "nvfp4": 5e-2, "fp8": 3.5e-2}[cfg.wfmt]
         rec["parity"] = {"tokens": int(n), "routing_mismatches": mism, "excluded_near_ties": int(near.sum()),
                          "max_err_over_rms": round(float(e.max()) / rms, 6),
                          "rms_err_over_rms": round(float(np.sqrt(np.mean(e ** 2))) / rms, 6), "bar": bar,

@@ -150,24 +150,24 @@ moe_status_t moe_permute(const moe_dims_t* dims, const moe_bf16_t* x, const int3
  * intermediate size 2,560; product in FP32 per section "Residual stream").
  * For every expert e and permuted row r in [offsets[e], offsets[e+1]):
  *   h = bf16( silu(x_perm[r] . Wg_e) * (x_perm[r] . Wu_e) )   (FP32 math)
- *   y_perm[r] = bf16( h . Wd_e )                               (FP32 accumulate)
+ *   y_perm[r] = h . Wd_e                                       (FP32 accumulate)
  * x_perm [T*top_k][d] bf16, offsets [E+1] int32 (non-decreasing, offsets[0]=0,
- * offsets[E] <= T*top_k), y_perm [T*top_k][d] bf16 (the expert output in the
- * model's dtype, rounded once from the FP32 accumulator). The GEMMs run on tcgen05
+ * offsets[E] <= T*top_k), y_perm [T*top_k][d] fp32 (the expert output kept in
+ * FP32: the block output is its only rounding after h). The GEMMs run on tcgen05
  * tensor cores with bf16 operands (NVFP4 weights are decoded to exact bf16
  * values on chip, the tensor scale applied to the FP32 accumulator; FP8
  * weights are decoded on chip as bf16(e4m3 * block scale), the product in
  * FP32, rounded once). */
 moe_status_t moe_expert_ffn(const moe_dims_t* dims, const moe_bf16_t* x_perm,
                             const int32_t* offsets, const moe_expert_weights_t* weights,
-                            moe_bf16_t* y_perm, void* ws, size_t ws_bytes, void* stream);
+                            float* y_perm, void* ws, size_t ws_bytes, void* stream);
 
 /* Step 4, combine (article section "Mixture of Experts": weighted by the
  * normalised, 2.5-scaled router weights; no shared expert):
  * out[t] = bf16( sum_k topk_w[t][k] * y_perm[inv_row[t*top_k+k]] ), FP32 sum
- * in slot order. out [T][d] bf16. Rows outside [0, T*top_k) latch
+ * in slot order. y_perm [T*top_k][d] fp32 (16-byte aligned), out [T][d] bf16. Rows outside [0, T*top_k) latch
  * MOE_DEV_BAD_ROW and are skipped; needs no workspace except for that code. */
-moe_status_t moe_combine(const moe_dims_t* dims, const moe_bf16_t* y_perm, const int32_t* inv_row,
+moe_status_t moe_combine(const moe_dims_t* dims, const float* y_perm, const int32_t* inv_row,
                          const float* topk_w, moe_bf16_t* out, void* ws, size_t ws_bytes,
                          void* stream);
 
@@ -230,7 +230,7 @@ moe_status_t moe_forward_ex(const moe_dims_t* dims, const moe_bf16_t* x, const f
  * usual); d <= 8192 (larger d returns MOE_ERR_UNSUPPORTED). moe_forward_residual
  * is moe_forward_ex with this as its
  * last stage instead of writing out. */
-moe_status_t moe_combine_residual(const moe_dims_t* dims, const moe_bf16_t* y_perm, const int32_t* inv_row,
+moe_status_t moe_combine_residual(const moe_dims_t* dims, const float* y_perm, const int32_t* inv_row,
                                   const float* topk_w, const moe_bf16_t* norm_gain, float eps, int32_t step,
                                   moe_bf16_t* resid, void* ws, size_t ws_bytes, void* stream);
 moe_status_t moe_forward_residual(const moe_dims_t* dims, const moe_bf16_t* x, const float* w_r,

@@ -217,7 +217,7 @@ def moe_expert_ffn(dims: Dims, x_perm, offsets, weights: ExpertWeights, y_perm, 
     R = dims.T * dims.top_k
     _expect(x_perm, _BF16, (R, dims.d), "x_perm")
     _expect(offsets, (torch.int32,), (dims.E + 1,), "offsets")
-    _expect(y_perm, _BF16, (R, dims.d), "y_perm")
+    _expect(y_perm, (torch.float32,), (R, dims.d), "y_perm")
     _check_weights(dims, weights)
     _check("moe_expert_ffn", _lib().moe_expert_ffn(ctypes.byref(dims.c()), _ptr(x_perm), _ptr(offsets),
                                                    ctypes.byref(weights.c()), _ptr(y_perm), _ptr(ws), ws.numel(),
@@ -226,7 +226,7 @@ def moe_expert_ffn(dims: Dims, x_perm, offsets, weights: ExpertWeights, y_perm, 
 
 def moe_combine(dims: Dims, y_perm, inv_row, topk_w, out, ws=None, stream=None):
     R = dims.T * dims.top_k
-    _expect(y_perm, _BF16, (R, dims.d), "y_perm")
+    _expect(y_perm, (torch.float32,), (R, dims.d), "y_perm")
     _expect(inv_row, (torch.int32,), (R,), "inv_row")
     _expect(topk_w, (torch.float32,), (dims.T, dims.top_k), "topk_w")
     _expect(out, _BF16, (dims.T, dims.d), "out")
@@ -239,7 +239,7 @@ def moe_combine_residual(dims: Dims, y_perm, inv_row, topk_w, norm_gain, eps: fl
     """Combine + post-norm (RMSNorm with gain norm_gain [d]) + depth-scaled residual update of
     resid [T, d] in place: resid = sqrt((step-1)/step) resid + (1/sqrt(step)) RMSNorm(out)."""
     R = dims.T * dims.top_k
-    _expect(y_perm, _BF16, (R, dims.d), "y_perm")
+    _expect(y_perm, (torch.float32,), (R, dims.d), "y_perm")
     _expect(inv_row, (torch.int32,), (R,), "inv_row")
     _expect(topk_w, (torch.float32,), (dims.T, dims.top_k), "topk_w")
     _expect(norm_gain, _BF16, (dims.d,), "norm_gain")

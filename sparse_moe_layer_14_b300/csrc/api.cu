@@ -2,6 +2,8 @@
 // validation, the workspace layout, and the launch sequence of each step.
 // No call allocates memory or synchronises the host except
 // moe_get_device_status().
+#include <nvtx3/nvToolsExt.h>
+
 #include <algorithm>
 #include <cmath>
 #include <cstring>
@@ -22,6 +24,15 @@ bool g_stage_events_on = false;
 cudaError_t mark(int i, cudaStream_t s) {
   return g_stage_events_on ? cudaEventRecord(g_stage_events[i], s) : cudaSuccess;
 }
+
+// NVTX range around the host-side enqueue of one stage (named as the stage events are), so a
+// timeline tool shows which launches belong to which step of the block; a no-op without a tool.
+struct NvtxStage {
+  explicit NvtxStage(const char* name) { nvtxRangePushA(name); }
+  ~NvtxStage() { nvtxRangePop(); }
+  NvtxStage(const NvtxStage&) = delete;
+  NvtxStage& operator=(const NvtxStage&) = delete;
+};
 
 size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 
@@ -64,7 +75,7 @@ Layout make_layout(const moe_dims_t& d) {
   sz[R_ITEMS2] = sizeof(int4) * static_cast<size_t>(pl.max_items2);
   sz[R_XPERM] = sizeof(uint16_t) * R * d.d;
   sz[R_H] = sizeof(uint16_t) * R * d.inter;
-  sz[R_Y] = sizeof(uint16_t) * R * d.d;
+  sz[R_Y] = sizeof(float) * R * d.d;
   Layout L;
   size_t o = 0;
   for (int i = 0; i < R_NUM; ++i) {
@@ -133,11 +144,13 @@ int32_t* status_word(void* ws) { return ws ? &reinterpret_cast<WsHeader*>(ws)->s
 
 moe_status_t do_route(const moe_dims_t* d, const uint16_t* x, const float* w_r, const float* sel_bias, int32_t* idx,
                       float* w, void* ws, const Layout& L, cudaStream_t s) {
-  if (router_uses_tensor_cores(d->T, d->E, d->d))
+  if (router_uses_tensor_cores(d->T, d->E, d->d)) {
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
     return cuda_status(launch_router_tc(x, w_r, region<uint8_t>(ws, L, R_WSPLIT), region<float>(ws, L, R_PART),
-                                        &reinterpret_cast<WsHeader*>(ws)->router_flagged, d->T, d->d, d->E, d->n_groups,
-                                        d->topk_groups, d->top_k, d->routed_scale, sel_bias, idx, w,
-                                        status_word(ws), num_sms(), s));
+                                        &hdr->router_flagged, hdr->wn_ticket, d->T, d->d, d->E, d->n_groups,
+                                        d->topk_groups, d->top_k, d->routed_scale, sel_bias, idx, w, &hdr->status,
+                                        &hdr->timeout_where, g_wait_spins, num_sms(), s));
+  }
   const int splits = router_splits(d->T, d->d, d->E, num_sms());
   float* part = region<float>(ws, L, R_PART);
   cudaError_t e = launch_router_logits(x, w_r, part, d->T, d->d, d->E, splits, s);
@@ -149,10 +162,10 @@ moe_status_t do_route(const moe_dims_t* d, const uint16_t* x, const float* w_r, 
 
 moe_status_t do_permute(const moe_dims_t* d, const uint16_t* x, const int32_t* idx, int32_t* counts,
                         int32_t* offsets, int32_t* row_token, int32_t* inv_row, uint16_t* x_perm, void* ws,
-                        const Layout& L, cudaStream_t s) {
+                        const Layout& L, cudaStream_t s, bool bitmap_zeroed = false) {
   cudaError_t e = launch_permute(x, idx, d->T, d->d, d->E, d->top_k, region<uint32_t>(ws, L, R_BITMAP),
                                  region<int32_t>(ws, L, R_WPRE), counts, offsets, row_token, inv_row, x_perm,
-                                 status_word(ws), s);
+                                 status_word(ws), s, bitmap_zeroed);
   return cuda_status(e);
 }
 
@@ -172,7 +185,7 @@ ExpertWeightsDev weights_dev(int wfmt, const moe_expert_weights_t* w) {
 }
 
 moe_status_t do_ffn(const moe_dims_t* d, const uint16_t* x_perm, const int32_t* offsets,
-                    const moe_expert_weights_t* w, uint16_t* y, void* ws, const Layout& L, cudaStream_t s,
+                    const moe_expert_weights_t* w, float* y, void* ws, const Layout& L, cudaStream_t s,
                     cudaEvent_t after_gemm1 = nullptr) {
   const ExpertPlan pl = plan_experts(d->T, d->d, d->E, d->top_k, d->inter, d->wfmt != MOE_W_BF16);
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
@@ -180,7 +193,8 @@ moe_status_t do_ffn(const moe_dims_t* d, const uint16_t* x_perm, const int32_t* 
   b.x_perm = x_perm;
   b.offsets = offsets;
   b.h = region<uint16_t>(ws, L, R_H);
-  b.y = y;
+  b.y = nullptr;
+  b.y_f32 = y;
   b.items1 = region<int4>(ws, L, R_ITEMS1);
   b.items2 = region<int4>(ws, L, R_ITEMS2);
   b.n_items = hdr->n_items;
@@ -240,7 +254,7 @@ moe_status_t moe_permute(const moe_dims_t* dims, const moe_bf16_t* x, const int3
 }
 
 moe_status_t moe_expert_ffn(const moe_dims_t* dims, const moe_bf16_t* x_perm, const int32_t* offsets,
-                            const moe_expert_weights_t* weights, moe_bf16_t* y_perm, void* ws, size_t ws_bytes,
+                            const moe_expert_weights_t* weights, float* y_perm, void* ws, size_t ws_bytes,
                             void* stream) {
   moe_status_t st = check_dims(dims);
   if (st != MOE_OK) return st;
@@ -251,7 +265,7 @@ moe_status_t moe_expert_ffn(const moe_dims_t* dims, const moe_bf16_t* x_perm, co
   return do_ffn(dims, x_perm, offsets, weights, y_perm, ws, make_layout(*dims), static_cast<cudaStream_t>(stream));
 }
 
-moe_status_t moe_combine(const moe_dims_t* dims, const moe_bf16_t* y_perm, const int32_t* inv_row, const float* topk_w,
+moe_status_t moe_combine(const moe_dims_t* dims, const float* y_perm, const int32_t* inv_row, const float* topk_w,
                          moe_bf16_t* out, void* ws, size_t ws_bytes, void* stream) {
   moe_status_t st = check_dims(dims);
   if (st != MOE_OK) return st;
@@ -301,19 +315,35 @@ moe_status_t forward_impl(const moe_dims_t* dims, const moe_bf16_t* x, const flo
   int32_t* row_token = region<int32_t>(ws, L, R_ROWTOK);
   int32_t* inv_row = region<int32_t>(ws, L, R_INVROW);
   uint16_t* x_perm = region<uint16_t>(ws, L, R_XPERM);
-  uint16_t* y = region<uint16_t>(ws, L, R_Y);
+  float* y = region<float>(ws, L, R_Y);
+  // the permutation's bitmap is cleared first, so that no copy sits between the block's kernels
+  // (they launch back to back with programmatic dependencies)
+  if (cudaMemsetAsync(region<uint32_t>(ws, L, R_BITMAP), 0, bitmap_bytes(dims->T, dims->E), s) != cudaSuccess)
+    return MOE_ERR_CUDA;
   if (mark(0, s) != cudaSuccess) return MOE_ERR_CUDA;
-  if ((st = do_route(dims, x, w_r, sel_bias, idx, w, ws, L, s)) != MOE_OK) return st;
+  {
+    NvtxStage r("moe router");
+    if ((st = do_route(dims, x, w_r, sel_bias, idx, w, ws, L, s)) != MOE_OK) return st;
+  }
   if (mark(1, s) != cudaSuccess) return MOE_ERR_CUDA;
-  if ((st = do_permute(dims, x, idx, cnt, offs, row_token, inv_row, x_perm, ws, L, s)) != MOE_OK) return st;
+  {
+    NvtxStage r("moe permute");
+    if ((st = do_permute(dims, x, idx, cnt, offs, row_token, inv_row, x_perm, ws, L, s, true)) != MOE_OK) return st;
+  }
   if (mark(2, s) != cudaSuccess) return MOE_ERR_CUDA;
-  if ((st = do_ffn(dims, x_perm, offs, weights, y, ws, L, s, g_stage_events_on ? g_stage_events[3] : nullptr)) !=
-      MOE_OK)
-    return st;
+  {
+    NvtxStage r("moe expert GEMMs");
+    if ((st = do_ffn(dims, x_perm, offs, weights, y, ws, L, s, g_stage_events_on ? g_stage_events[3] : nullptr)) !=
+        MOE_OK)
+      return st;
+  }
   if (mark(4, s) != cudaSuccess) return MOE_ERR_CUDA;
-  st = cuda_status(res ? launch_combine_residual(y, inv_row, w, res->gain, res->eps, res->step, res->resid, dims->T,
-                                                 dims->d, dims->top_k, status_word(ws), s)
-                       : launch_combine(y, inv_row, w, out, dims->T, dims->d, dims->top_k, status_word(ws), s));
+  {
+    NvtxStage r(res ? "moe combine + post-norm residual" : "moe combine");
+    st = cuda_status(res ? launch_combine_residual(y, inv_row, w, res->gain, res->eps, res->step, res->resid, dims->T,
+                                                   dims->d, dims->top_k, status_word(ws), s)
+                         : launch_combine(y, inv_row, w, out, dims->T, dims->d, dims->top_k, status_word(ws), s));
+  }
   if (st != MOE_OK) return st;
   return mark(5, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -332,7 +362,7 @@ moe_status_t moe_forward_residual(const moe_dims_t* dims, const moe_bf16_t* x, c
   return forward_impl(dims, x, w_r, sel_bias, weights, nullptr, &res, topk_idx, counts, ws, ws_bytes, stream);
 }
 
-moe_status_t moe_combine_residual(const moe_dims_t* dims, const moe_bf16_t* y_perm, const int32_t* inv_row,
+moe_status_t moe_combine_residual(const moe_dims_t* dims, const float* y_perm, const int32_t* inv_row,
                                   const float* topk_w, const moe_bf16_t* norm_gain, float eps, int32_t step,
                                   moe_bf16_t* resid, void* ws, size_t ws_bytes, void* stream) {
   moe_status_t st = check_dims(dims);
@@ -432,6 +462,8 @@ DenseLayout make_dense_layout(const moe_dims_t& d) {
 }
 
 __global__ void dense_offsets_kernel(int32_t* offsets, int T) {
+  pdl_launch_dependents();
+  pdl_wait();
   offsets[0] = 0;
   offsets[1] = T;
 }
@@ -484,14 +516,14 @@ moe_status_t moe_dense_mlp(const moe_dims_t* dims, const moe_bf16_t* x, const mo
   uint8_t* base = static_cast<uint8_t*>(ws);
   int32_t* offs = reinterpret_cast<int32_t*>(base + L.offs);
   if (mark(0, s) != cudaSuccess) return MOE_ERR_CUDA;
-  dense_offsets_kernel<<<1, 1, 0, s>>>(offs, dims->T);
-  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_pdl(dense_offsets_kernel, dim3(1), dim3(1), 0, s, offs, dims->T) != cudaSuccess) return MOE_ERR_CUDA;
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
   ExpertBuffers b;
   b.x_perm = x;  // one expert: the permuted rows are the tokens in order
   b.offsets = offs;
   b.h = reinterpret_cast<uint16_t*>(base + L.h);
   b.y = out;
+  b.y_f32 = nullptr;
   b.items1 = reinterpret_cast<int4*>(base + L.items1);
   b.items2 = reinterpret_cast<int4*>(base + L.items2);
   b.n_items = hdr->n_items;

@@ -19,7 +19,8 @@ struct WsHeader {
   int32_t timeout_where; // role id of the first wait that expired (diagnostics)
   int32_t n_items[2];    // expert-GEMM work items (GEMM1, GEMM2) built on the device
   int32_t router_flagged; // tokens the tensor-core router recomputed in fp32 (last call)
-  int32_t pad[59];
+  int32_t wn_ticket[8];   // tensor-core router: blocks done per 32-expert strip of W_r (back to 0 after each call)
+  int32_t pad[51];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
@@ -36,6 +37,25 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
+
+// ------------------------------------------------------------------ programmatic dependent launch
+//
+// Every kernel of the library is launched with programmatic stream
+// serialisation (launch_pdl below), so its blocks may start while the
+// previous kernel on the stream is still finishing. Each kernel therefore
+// (1) lets its own dependents launch at once (pdl_launch_dependents at
+// entry: they still wait for this grid to finish before using its data) and
+// (2) executes pdl_wait before its first access to memory written by earlier
+// work on the stream; everything before that point (barrier set-up, tensor
+// memory allocation, descriptor prefetch) overlaps the previous kernel's
+// tail. Every kernel executes pdl_wait on every path before it exits, so a
+// kernel's completion implies that of all work before it.
+
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ------------------------------------------------------------------ mbarrier
 
@@ -214,5 +234,23 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
 }
 
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
+
+// Launch `kernel` on `stream` with programmatic stream serialisation (see
+// pdl_wait above). Arguments are passed as the kernel declares them.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
+}
 
 }  // namespace beammoe

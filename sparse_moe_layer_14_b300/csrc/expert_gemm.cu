@@ -5,7 +5,7 @@
 // stream": the SwiGLU product is computed in FP32).
 //
 //   GEMM1 + SwiGLU:  h[r][i] = bf16( silu(x_perm[r].Wg_e[i]) * (x_perm[r].Wu_e[i]) )
-//   GEMM2:           y[r][n] = bf16( h[r] . Wd_e[n] )
+//   GEMM2:           y[r][n] = h[r] . Wd_e[n]   (FP32; bf16 for the dense MLP's output)
 //
 // Every work item runs two 128-row weight tiles against the same token tile
 // (two MMAs per K step sharing the token operand): the gate and up tiles of
@@ -85,7 +85,8 @@ struct GemmArgs {
   uint32_t a_col;     // first TMEM column of the decoded weight slots (NVFP4)
   int conv_stages;
   uint16_t* h_out;    // GEMM1 output [R][Nw] bf16
-  uint16_t* y_out;    // GEMM2 output [R][Nw] bf16
+  uint16_t* y_out;    // GEMM2 output [R][Nw] bf16 (the dense MLP's output), or null
+  float* y_f32;       // GEMM2 output [R][Nw] fp32 (the experts' outputs), or null
   const float* ts0;   // per-expert scale applied to accumulator 0 (NVFP4), or null
   const float* ts1;
   const uint8_t* sf0;  // e4m3 block scales [E*Nw][K/16] of matrix 0 (NVFP4)
@@ -201,6 +202,7 @@ __global__ void __launch_bounds__(threads_for(kFmt), 1)
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort = &abort_flag;
+  pdl_launch_dependents();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
@@ -231,6 +233,7 @@ __global__ void __launch_bounds__(threads_for(kFmt), 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_wait();  // the work items, tokens and h come from earlier work on the stream
 
   constexpr bool kConv = kFmt != kFmtBf16;    // weights decoded into tensor memory
   constexpr bool kFp8 = kFmt == kFmtFp8;
@@ -406,6 +409,16 @@ __global__ void __launch_bounds__(threads_for(kFmt), 1)
               }
             }
           }
+        } else if (p.y_f32) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int tok = c + j;
+            if (tok < ntok) {
+              float* yrow = p.y_f32 + static_cast<size_t>(item.z + tok) * p.Nw;
+              if (valid0) yrow[col0] = __uint_as_float(gg[j]) * s0;
+              if (valid1) yrow[col1] = __uint_as_float(uu[j]) * s0;
+            }
+          }
         } else {
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -494,43 +507,69 @@ __global__ void __launch_bounds__(threads_for(kFmt), 1)
       return v;
     };
     uint4 cur = make_uint4(0, 0, 0, 0), nxt = load_group(blockIdx.x, 0);
+    // With three or more decoded slots the arrival that hands a slot to the MMA
+    // is deferred by one slice: the slice's tcgen05.st completes while the next
+    // slice is decoded (into the other register set), and tcgen05.wait::st
+    // then finds it done. With two slots the MMA would wait for that next
+    // decode, so each slice is handed over at once.
+    const bool defer = p.conv_stages >= 3;
+    int pend = -1;  // slot whose store is in flight and not yet handed over
     bool ok = true;
-    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-      for (int kb = 0; kb < kblocks; ++kb) {
-        if ((kb & 3) == 0) {
-          cur = nxt;
-          nxt = kb + 4 < kblocks ? load_group(it, (kb >> 2) + 1) : load_group(it + gridDim.x, 0);
+    uint32_t va[32], vb[32];
+    auto slice = [&](int it, int kb, uint32_t (&v)[32]) {
+      if ((kb & 3) == 0) {
+        cur = nxt;
+        nxt = kb + 4 < kblocks ? load_group(it, (kb >> 2) + 1) : load_group(it + gridDim.x, 0);
+      }
+      // tcgen05.st is warp-collective: the whole warp proceeds or stops together
+      const bool ready = __all_sync(
+          0xffffffffu, mbar_wait_bounded(&full_bar[stage], phase, p.wait_spins, kWaitNs, abort) &&
+                           mbar_wait_bounded(&conv_empty_bar[cstage], cphase ^ 1u, p.wait_spins, kWaitNs, abort));
+      if (!ready) {
+        if (lane == 0 && !*abort) fail(p, abort, 5);
+        return false;
+      }
+      tc_fence_after();  // the MMAs that read this slot have completed
+      const uint8_t* packed = smem + static_cast<size_t>(stage) * p.stage_bytes + p.p_offset + t * kPB;
+      const int g = kb & 3;
+      if constexpr (kFp8) {
+        decode_row_fp8(packed, r, __uint_as_float(g < 2 ? cur.x : cur.y), v);
+      } else {
+        decode_row(packed, r, g == 0 ? cur.x : g == 1 ? cur.y : g == 2 ? cur.z : cur.w, v);
+      }
+      if (defer) {
+        if (pend >= 0) {  // the previous slice's store (issued one decode ago)
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(&conv_bar[pend]);
         }
-        // tcgen05.st is warp-collective: the whole warp proceeds or stops together
-        const bool ready = __all_sync(
-            0xffffffffu, mbar_wait_bounded(&full_bar[stage], phase, p.wait_spins, kWaitNs, abort) &&
-                             mbar_wait_bounded(&conv_empty_bar[cstage], cphase ^ 1u, p.wait_spins, kWaitNs, abort));
-        if (!ready) {
-          if (lane == 0 && !*abort) fail(p, abort, 5);
-          ok = false;
-          break;
-        }
-        tc_fence_after();  // the MMAs that read this slot have completed
-        const uint8_t* packed = smem + static_cast<size_t>(stage) * p.stage_bytes + p.p_offset + t * kPB;
-        const int g = kb & 3;
-        uint32_t v[32];
-        if constexpr (kFp8) {
-          decode_row_fp8(packed, r, __uint_as_float(g < 2 ? cur.x : cur.y), v);
-        } else {
-          decode_row(packed, r, g == 0 ? cur.x : g == 1 ? cur.y : g == 2 ? cur.z : cur.w, v);
-        }
+        tmem_st_32x32b_x32(t_lane + static_cast<uint32_t>(cstage * kConvCols), v);
+        pend = cstage;
+      } else {
         tmem_st_32x32b_x32(t_lane + static_cast<uint32_t>(cstage * kConvCols), v);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&conv_bar[cstage]);
-        if (++cstage == p.conv_stages) {
-          cstage = 0;
-          cphase ^= 1u;
-        }
-        if (++stage == p.stages) {
-          stage = 0;
-          phase ^= 1u;
-        }
+      }
+      if (++cstage == p.conv_stages) {
+        cstage = 0;
+        cphase ^= 1u;
+      }
+      if (++stage == p.stages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+      return true;
+    };
+    // kblocks is even (K is a multiple of 128 for both decoded formats): two slices per
+    // iteration keep each register set in place
+    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x)
+      for (int kb = 0; kb < kblocks && ok; kb += 2) ok = slice(it, kb, va) && slice(it, kb + 1, vb);
+    if (pend >= 0) {  // after an abort too: no store may be in flight when TMEM is released
+      tmem_st_wait();
+      if (ok) {
+        tc_fence_before();
+        mbar_arrive(&conv_bar[pend]);
       }
     }
   }
@@ -569,6 +608,8 @@ __global__ void __launch_bounds__(256) schedule_kernel(const int32_t* __restrict
                                                        int4* __restrict__ items2, int32_t* __restrict__ n_items,
                                                        int32_t* status) {
   __shared__ int warp_sums[8];
+  pdl_launch_dependents();
+  pdl_wait();
   const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
   int n = 0, row0 = 0, ntiles = 0, tsz = 16;
   if (e < E) {
@@ -713,8 +754,8 @@ cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUte
   cudaError_t err = cudaFuncSetAttribute(expert_gemm_kernel<kGLU, kFmt>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s.smem));
   if (err != cudaSuccess) return err;
-  expert_gemm_kernel<kGLU, kFmt><<<grid, threads_for(kFmt), s.smem, stream>>>(a0, a1, b[0], b[1], b[2], args);
-  return cudaGetLastError();
+  return launch_pdl(expert_gemm_kernel<kGLU, kFmt>, dim3(grid), dim3(threads_for(kFmt)), s.smem, stream, a0, a1, b[0],
+                    b[1], b[2], args);
 }
 
 }  // namespace
@@ -749,9 +790,8 @@ cudaError_t launch_expert_ffn(const ExpertPlan& plan, const ExpertBuffers& buf, 
   if (fmt != MOE_W_BF16 && fmt != MOE_W_NVFP4 && fmt != MOE_W_FP8) return cudaErrorInvalidValue;
   if (fmt == MOE_W_NVFP4 && ((d % 256) || (inter % 256))) return cudaErrorNotSupported;
   if (fmt == MOE_W_FP8 && ((d % 128) || (inter % 128))) return cudaErrorNotSupported;
-  schedule_kernel<<<1, 256, 0, stream>>>(buf.offsets, E, R, plan.n_max, plan.wtiles1, plan.wtiles2, buf.items1,
-                                         buf.items2, buf.n_items, buf.status);
-  cudaError_t err = cudaGetLastError();
+  cudaError_t err = launch_pdl(schedule_kernel, dim3(1), dim3(256), 0, stream, buf.offsets, E, R, plan.n_max,
+                               plan.wtiles1, plan.wtiles2, buf.items1, buf.items2, buf.n_items, buf.status);
   if (err != cudaSuccess) return err;
 
   CUtensorMap tg, tu, td, tx[3], th[3];
@@ -810,6 +850,7 @@ cudaError_t launch_expert_ffn(const ExpertPlan& plan, const ExpertBuffers& buf, 
   a2.Nw = d;
   a2.E = E;
   a2.y_out = buf.y;
+  a2.y_f32 = buf.y_f32;
   a2.status = buf.status;
   a2.timeout_where = buf.timeout_where;
   a2.wait_spins = wait_spins;

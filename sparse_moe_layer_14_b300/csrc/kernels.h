@@ -31,17 +31,24 @@ int router_epad(int E);
 bool router_uses_tensor_cores(int T, int E, int d);
 size_t router_tc_scratch_bytes(int T, int d, int E);
 int router_tc_splits(int T, int d, int num_sms);  // partial-logit buffers: [splits][T][E] fp32 in `part`
+// `hdr_ticket` (8 ints, zero before the first call; the kernels return them
+// to zero) and `timeout_where` live in the workspace header; `wait_spins`
+// bounds the router's pipeline waits (see moe_set_wait_bound).
 cudaError_t launch_router_tc(const uint16_t* x, const float* w_r, void* scratch, float* part, int32_t* flagged_count,
-                             int T, int d, int E, int n_groups, int topk_groups, int top_k, float routed_scale,
-                             const float* sel_bias, int32_t* topk_idx, float* topk_w, int32_t* status, int num_sms,
+                             int32_t* hdr_ticket, int T, int d, int E, int n_groups, int topk_groups, int top_k,
+                             float routed_scale, const float* sel_bias, int32_t* topk_idx, float* topk_w,
+                             int32_t* status, int32_t* timeout_where, long long wait_spins, int num_sms,
                              cudaStream_t stream);
 
 // ---- permutation (permute.cu) ----
 int bitmap_words(int T);
+size_t bitmap_bytes(int T, int E);
+// bitmap_zeroed: the caller has already cleared the bitmap on `stream` (otherwise a memset is
+// enqueued first).
 cudaError_t launch_permute(const uint16_t* x, const int32_t* topk_idx, int T, int d, int E, int top_k,
                            uint32_t* bitmap, int32_t* word_prefix, int32_t* counts, int32_t* offsets,
                            int32_t* row_token, int32_t* inv_row, uint16_t* x_perm, int32_t* status,
-                           cudaStream_t stream);
+                           cudaStream_t stream, bool bitmap_zeroed = false);
 
 // ---- expert FFN (expert_gemm.cu) ----
 struct ExpertPlan {
@@ -58,7 +65,8 @@ struct ExpertBuffers {
   const uint16_t* x_perm;  // [R][d]
   const int32_t* offsets;  // [E+1]
   uint16_t* h;             // [R][inter]
-  uint16_t* y;             // [R][d] bf16
+  uint16_t* y;             // [R][d] bf16 output (dense MLP), or null
+  float* y_f32;            // [R][d] fp32 output (the experts), or null
   int4* items1;            // GEMM1 work items {e, wtile, row0, ntok}
   int4* items2;
   int32_t* n_items;        // [2]
@@ -86,10 +94,10 @@ cudaError_t launch_pre_norm(const uint16_t* h, const uint16_t* gain, float eps, 
 // combine + post-norm (RMSNorm, gain [d]) + depth-scaled residual update of
 // resid [T][d] in place at step `step` (>= 1); d <= 8192 (one cluster of
 // <= 8 blocks per row).
-cudaError_t launch_combine_residual(const uint16_t* y_perm, const int32_t* inv_row, const float* topk_w,
+cudaError_t launch_combine_residual(const float* y_perm, const int32_t* inv_row, const float* topk_w,
                                     const uint16_t* gain, float eps, int step, uint16_t* resid, int T, int d,
                                     int top_k, int32_t* status, cudaStream_t stream);
-cudaError_t launch_combine(const uint16_t* y_perm, const int32_t* inv_row, const float* topk_w, uint16_t* out,
+cudaError_t launch_combine(const float* y_perm, const int32_t* inv_row, const float* topk_w, uint16_t* out,
                            int T, int d, int top_k, int32_t* status, cudaStream_t stream);
 
 }  // namespace beammoe

@@ -30,6 +30,8 @@ __device__ __forceinline__ uint32_t scale_pair(uint32_t v, uint32_t g, float inv
 __global__ void __launch_bounds__(kNormThreads) pre_norm_kernel(const uint16_t* __restrict__ h,
                                                                 const uint16_t* __restrict__ gain, float eps,
                                                                 int d, uint16_t* __restrict__ x) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int nv = d >> 3;  // 16-byte vectors per row (d is a multiple of 64)
   const uint4* row = reinterpret_cast<const uint4*>(h + static_cast<size_t>(blockIdx.x) * d);
   float ss = 0.f;
@@ -66,8 +68,7 @@ __global__ void __launch_bounds__(kNormThreads) pre_norm_kernel(const uint16_t* 
 cudaError_t launch_pre_norm(const uint16_t* h, const uint16_t* gain, float eps, uint16_t* x, int T, int d,
                             cudaStream_t stream) {
   if (T <= 0) return cudaSuccess;
-  pre_norm_kernel<<<T, kNormThreads, 0, stream>>>(h, gain, eps, d, x);
-  return cudaGetLastError();
+  return launch_pdl(pre_norm_kernel, dim3(T), dim3(kNormThreads), 0, stream, h, gain, eps, d, x);
 }
 
 }  // namespace beammoe

@@ -20,6 +20,8 @@ namespace {
 
 __global__ void bitmap_kernel(const int32_t* __restrict__ idx, int T, int E, int K, int nw,
                               uint32_t* __restrict__ bitmap, int32_t* status) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= static_cast<int64_t>(T) * K) return;
   const int t = static_cast<int>(i / K);
@@ -39,6 +41,8 @@ __global__ void __launch_bounds__(256) column_scan_kernel(const uint32_t* __rest
                                                           int32_t* __restrict__ word_prefix,
                                                           int32_t* __restrict__ counts) {
   __shared__ int32_t warp_sums[8];
+  pdl_launch_dependents();
+  pdl_wait();
   const int e = blockIdx.x;
   const uint32_t* col = bitmap + static_cast<size_t>(e) * nw;
   int32_t* pre = word_prefix + static_cast<size_t>(e) * nw;
@@ -74,6 +78,8 @@ __global__ void __launch_bounds__(256) column_scan_kernel(const uint32_t* __rest
 __global__ void __launch_bounds__(1024) offsets_kernel(const int32_t* __restrict__ counts, int E,
                                                        int32_t* __restrict__ offsets) {
   __shared__ int32_t warp_sums[32];
+  pdl_launch_dependents();
+  pdl_wait();
   const int i = threadIdx.x, lane = i & 31, warp = i >> 5;
   const int v = (i < E) ? counts[i] : 0;
   int incl = v;
@@ -100,6 +106,8 @@ __global__ void __launch_bounds__(32 * kGatherWarps) gather_kernel(
     const uint32_t* __restrict__ bitmap, const int32_t* __restrict__ word_prefix,
     const int32_t* __restrict__ offsets, int32_t* __restrict__ row_token, int32_t* __restrict__ inv_row,
     uint16_t* __restrict__ x_perm) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int t = blockIdx.x;
   const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * d);
@@ -127,21 +135,25 @@ __global__ void __launch_bounds__(32 * kGatherWarps) gather_kernel(
 
 int bitmap_words(int T) { return (T + 31) / 32; }
 
+size_t bitmap_bytes(int T, int E) { return sizeof(uint32_t) * static_cast<size_t>(E) * bitmap_words(T); }
+
 cudaError_t launch_permute(const uint16_t* x, const int32_t* topk_idx, int T, int d, int E, int top_k,
                            uint32_t* bitmap, int32_t* word_prefix, int32_t* counts, int32_t* offsets,
                            int32_t* row_token, int32_t* inv_row, uint16_t* x_perm, int32_t* status,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, bool bitmap_zeroed) {
   const int nw = bitmap_words(T);
-  cudaError_t err = cudaMemsetAsync(bitmap, 0, sizeof(uint32_t) * static_cast<size_t>(E) * nw, stream);
-  if (err != cudaSuccess) return err;
+  cudaError_t err = cudaSuccess;
+  if (!bitmap_zeroed && (err = cudaMemsetAsync(bitmap, 0, bitmap_bytes(T, E), stream)) != cudaSuccess) return err;
   const int64_t slots = static_cast<int64_t>(T) * top_k;
-  bitmap_kernel<<<static_cast<unsigned>((slots + 255) / 256), 256, 0, stream>>>(topk_idx, T, E, top_k, nw, bitmap,
-                                                                                status);
-  column_scan_kernel<<<E, 256, 0, stream>>>(bitmap, nw, word_prefix, counts);
-  offsets_kernel<<<1, 1024, 0, stream>>>(counts, E, offsets);
-  gather_kernel<<<T, 32 * kGatherWarps, 0, stream>>>(x, topk_idx, T, d, E, top_k, nw, bitmap, word_prefix, offsets,
-                                                      row_token, inv_row, x_perm);
-  return cudaGetLastError();
+  if ((err = launch_pdl(bitmap_kernel, dim3(static_cast<unsigned>((slots + 255) / 256)), dim3(256), 0, stream, topk_idx,
+                        T, E, top_k, nw, bitmap, status)) != cudaSuccess)
+    return err;
+  if ((err = launch_pdl(column_scan_kernel, dim3(E), dim3(256), 0, stream, bitmap, nw, word_prefix, counts)) !=
+      cudaSuccess)
+    return err;
+  if ((err = launch_pdl(offsets_kernel, dim3(1), dim3(1024), 0, stream, counts, E, offsets)) != cudaSuccess) return err;
+  return launch_pdl(gather_kernel, dim3(T), dim3(32 * kGatherWarps), 0, stream, x, topk_idx, T, d, E, top_k, nw,
+                    bitmap, word_prefix, offsets, row_token, inv_row, x_perm);
 }
 
 }  // namespace beammoe

@@ -15,18 +15,24 @@
 // Large batches (prefill):
 //  wr_split_kernel       W_r (fp32, [d][E]) -> three bf16 matrices hi, mid,
 //                        lo ([E_pad][d], K-contiguous) with hi + mid + lo = W_r
-//                        (8 + 8 + 8 significant bits cover fp32's 24).
+//                        (8 + 8 + 8 significant bits cover fp32's 24), and the
+//                        largest column norm of W_r (a fixed-order reduction).
 //  router_tc_kernel      per 128 tokens and one range of the hidden dimension:
 //                        partial logits x.hi + x.mid + x.lo on the tcgen05
 //                        tensor cores (x is exact in bf16, so every product is
 //                        exact in fp32).
 //  router_select_flag_kernel  one warp per token: partials summed, sigmoid,
 //                        group-limited selection and the two decision margins.
-//                        The tensor cores' fp32 accumulation is measurably
-//                        coarser than FFMA (logit errors up to ~4e-5 with the
-//                        small mid/lo products in their own accumulator, ~5e-6
-//                        for FFMA, on Beam-shape inputs), so its decisions are
-//                        kept only where every margin is wide:
+//                        The tensor cores' fp32 accumulation is coarser than
+//                        FFMA, so a decision is kept only where every margin
+//                        exceeds a bound on the logit error that scales with
+//                        the token: kappa * 2^-23 * sqrt(d/16) * |x_t| *
+//                        max_e |W_r[:, e]| (every partial sum of x_t . W_r[:, e]
+//                        is at most |x_t| |W_r[:, e]| by Cauchy-Schwarz, and
+//                        d/16 MMA steps each round once; kappa is set from
+//                        measured errors with a wide margin). |x_t| comes from
+//                        the tensor-core kernel's epilogue warps, the column
+//                        norms of W_r from wr_split_kernel. Elsewhere:
 //  router_flagged_logits_kernel, router_flagged_select_kernel: tokens with a
 //                        narrow margin get all logits in fp32 FFMA and the
 //                        full warp selection.
@@ -49,6 +55,8 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const uint16_t* __re
                                                             int k_per_split) {
   __shared__ __align__(16) float xs[RK][RT + 4];  // xs[k][t]
   __shared__ __align__(16) float ws[RK][RE];      // ws[k][e]
+  pdl_launch_dependents();
+  pdl_wait();
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
   const int e0 = blockIdx.x * RE, t0 = blockIdx.y * RT;
   const int kbeg = blockIdx.z * k_per_split, kend = kbeg + k_per_split;
@@ -115,6 +123,8 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const uint16_t* __re
 // over s = 0,4,8,.. / 1,5,.. / 2,6,.. / 3,7,.. (independent loads in flight),
 // then (c0 + c1) + (c2 + c3).
 __global__ void __launch_bounds__(256) split_reduce_kernel(float* __restrict__ part, int splits, int64_t n) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= n) return;
   float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
@@ -325,6 +335,8 @@ __global__ void __launch_bounds__(256) router_select_kernel(const float* __restr
                                                             const float* __restrict__ bias,
                                                             int32_t* __restrict__ topk_idx,
                                                             float* __restrict__ topk_w, int32_t* status) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (t >= T) return;
@@ -347,18 +359,34 @@ constexpr uint64_t kTcWaitNs = 2000000000ull;
 constexpr uint64_t kTcDrainNs = 1000000000ull;
 
 // out[s][e][k] = bf16 split s of W_r[k][e] (rows e >= E are zero). Also
-// resets the flagged-token count.
+// resets the flagged-token count, and finds the largest column norm of W_r in
+// a fixed order: every block writes the sums of squares of its 32 x 32 tile's
+// columns to colss[k block][e]; the last block to finish a 32-expert strip
+// (counted in ticket[strip], which it returns to 0) adds them up in k order
+// and writes the strip's largest norm to wn_strip[strip].
 __global__ void __launch_bounds__(256) wr_split_kernel(const float* __restrict__ wr, int d, int E, int E_pad,
-                                                       uint16_t* __restrict__ out, int32_t* __restrict__ flagged_count) {
+                                                       uint16_t* __restrict__ out, float* __restrict__ colss,
+                                                       float* __restrict__ wn_strip, int32_t* __restrict__ ticket,
+                                                       int32_t* __restrict__ flagged_count) {
   __shared__ float tile[32][33];
+  __shared__ int is_last;
+  pdl_launch_dependents();
+  pdl_wait();
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *flagged_count = 0;
   const int k0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
+  const int E32 = gridDim.y * 32;  // row stride of colss
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
   for (int i = ty; i < 32; i += 8) {
     const int e = e0 + tx;
     tile[i][tx] = (e < E) ? wr[static_cast<size_t>(k0 + i) * E + e] : 0.f;
   }
   __syncthreads();
+  if (ty == 0) {
+    float ss = 0.f;
+#pragma unroll 8
+    for (int k = 0; k < 32; ++k) ss = fmaf(tile[k][tx], tile[k][tx], ss);
+    colss[static_cast<size_t>(blockIdx.x) * E32 + e0 + tx] = ss;
+  }
   for (int i = ty; i < 32; i += 8) {
     const int e = e0 + i, k = k0 + tx;
     if (e >= E_pad) continue;
@@ -373,16 +401,41 @@ __global__ void __launch_bounds__(256) wr_split_kernel(const float* __restrict__
     out[plane + o] = __bfloat16_as_ushort(mid);
     out[2 * plane + o] = __bfloat16_as_ushort(lo);
   }
+  __threadfence();  // this block's column sums are visible before it is counted
+  __syncthreads();
+  if (threadIdx.x == 0) is_last = atomicAdd(&ticket[blockIdx.y], 1) == static_cast<int>(gridDim.x) - 1;
+  __syncthreads();
+  if (is_last && ty == 0) {
+    float ss = 0.f;
+    for (int kx = 0; kx < static_cast<int>(gridDim.x); ++kx) ss += __ldcg(colss + static_cast<size_t>(kx) * E32 + e0 + tx);
+    float nrm = sqrtf(ss);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) nrm = fmaxf(nrm, __shfl_xor_sync(0xffffffffu, nrm, off));
+    if (tx == 0) {
+      wn_strip[blockIdx.y] = nrm;
+      ticket[blockIdx.y] = 0;
+    }
+  }
 }
 
 struct TcArgs {
   int T, d, E, E_pad;
   int kb_per_split;  // K slices of one CTA (the hidden dimension is split over blockIdx.y)
   float* part;       // [splits][T][E] partial logits
+  const uint16_t* x; // [T][d] (read by the epilogue warps for the token norms)
+  float* xss;        // [splits][T] partial sums of squares of x over each CTA's hidden range
   int32_t* status;
+  int32_t* timeout_where;
+  long long wait_spins;
   uint32_t stage_bytes;
   uint32_t tmem_cols;
 };
+
+__device__ __forceinline__ void tc_fail(const TcArgs& a, volatile int* abort, int where) {
+  latch_status(a.status, MOE_DEV_TIMEOUT);
+  if (a.timeout_where) atomicCAS(a.timeout_where, 0, where);
+  *abort = 1;
+}
 
 // Partial logits of 128 tokens x E_pad experts over one range of the hidden
 // dimension: hi products accumulate in D1 (TMEM columns [0, E_pad)), the small
@@ -399,6 +452,7 @@ __global__ void __launch_bounds__(192, 1) router_tc_kernel(const __grid_constant
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort = &abort_flag;
+  pdl_launch_dependents();
   const int t0 = blockIdx.x * kTcTokens;
   const int kb0 = blockIdx.y * a.kb_per_split, kb1 = kb0 + a.kb_per_split;
   const uint32_t wtile = static_cast<uint32_t>(a.E_pad) * kTcBK * 2;  // one split's tile
@@ -423,6 +477,7 @@ __global__ void __launch_bounds__(192, 1) router_tc_kernel(const __grid_constant
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_wait();  // x and the split W_r come from earlier work on the stream
   const uint32_t tmem_base = tmem_slot;
   long long fills = 0;
 
@@ -431,11 +486,8 @@ __global__ void __launch_bounds__(192, 1) router_tc_kernel(const __grid_constant
       int stage = 0;
       uint32_t phase = 0;
       for (int kb = kb0; kb < kb1; ++kb) {
-        if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, 1ll << 40, kTcWaitNs, abort)) {
-          if (!*abort) {
-            latch_status(a.status, MOE_DEV_TIMEOUT);
-            *abort = 1;
-          }
+        if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, a.wait_spins, kTcWaitNs, abort)) {
+          if (!*abort) tc_fail(a, abort, 11);
           break;
         }
         uint8_t* st = smem + static_cast<size_t>(stage) * a.stage_bytes;
@@ -457,11 +509,8 @@ __global__ void __launch_bounds__(192, 1) router_tc_kernel(const __grid_constant
       const uint32_t idesc = idesc_bf16_f32(kTcTokens, a.E_pad);
       bool ok = true;
       for (int kb = kb0; kb < kb1; ++kb) {
-        if (!mbar_wait_bounded(&full_bar[stage], phase, 1ll << 40, kTcWaitNs, abort)) {
-          if (!*abort) {
-            latch_status(a.status, MOE_DEV_TIMEOUT);
-            *abort = 1;
-          }
+        if (!mbar_wait_bounded(&full_bar[stage], phase, a.wait_spins, kTcWaitNs, abort)) {
+          if (!*abort) tc_fail(a, abort, 12);
           ok = false;
           break;
         }
@@ -485,12 +534,30 @@ __global__ void __launch_bounds__(192, 1) router_tc_kernel(const __grid_constant
     }
     __syncwarp();
   } else {
-    // epilogue: thread r owns token t0 + r (TMEM lane r); partial logits to global
+    // epilogue: thread r owns token t0 + r (TMEM lane r). While the MMAs run it
+    // sums the squares of its token's x over this CTA's hidden range (the
+    // token norm of the flag bound); then the partial logits go to global.
     const int q = warp & 3, r = q * 32 + lane;
-    const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&accf_bar, 0, 1ll << 40, kTcWaitNs, abort));
+    const int t = t0 + r;
+    if (t < a.T) {
+      const int k0 = kb0 * kTcBK, n8 = (kb1 - kb0) * kTcBK / 8;
+      const uint4* row = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(t) * a.d + k0);
+      float ss = 0.f;
+      for (int i = 0; i < n8; ++i) {
+        const uint4 v = __ldg(row + i);
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float lo = __uint_as_float(w4[j] << 16), hi = __uint_as_float(w4[j] & 0xFFFF0000u);
+          ss = fmaf(lo, lo, ss);
+          ss = fmaf(hi, hi, ss);
+        }
+      }
+      a.xss[static_cast<size_t>(blockIdx.y) * a.T + t] = ss;
+    }
+    const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&accf_bar, 0, a.wait_spins, kTcWaitNs, abort));
     if (ok) {
       tc_fence_after();
-      const int t = t0 + r;
       float* dst = a.part + (static_cast<size_t>(blockIdx.y) * a.T + t) * a.E;
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
       for (int c = 0; c < a.E_pad; c += 16) {
@@ -505,8 +572,7 @@ __global__ void __launch_bounds__(192, 1) router_tc_kernel(const __grid_constant
         }
       }
     } else if (lane == 0 && !*abort) {
-      latch_status(a.status, MOE_DEV_TIMEOUT);
-      *abort = 1;
+      tc_fail(a, abort, 13);
     }
   }
 
@@ -540,22 +606,31 @@ __global__ void __launch_bounds__(192, 1) router_tc_kernel(const __grid_constant
 // of all its logits; elsewhere the decisions equal those of exact fp32
 // logits and only the weights carry the tensor-core error (about 1e-6
 // relative).
+//   logit error bound  e_l = err_coef * |x_t| * max_e |W_r[:, e]|,
+//                      err_coef = kappa * 2^-23 * sqrt(d / 16)
+//   score error bound  e_s = e_l / 4 (the sigmoid's slope is at most 1/4)
+// A group score sums two scores and a group margin compares two group
+// scores (4 e_s); expert margins and slot gaps compare two scores (2 e_s).
 __global__ void __launch_bounds__(256) router_select_flag_kernel(const float* __restrict__ part, int splits, int T,
                                                                  int E, int G, int Gk, int K, float scale,
                                                                  const float* __restrict__ bias,
-                                                                 int32_t* __restrict__ topk_idx,
+                                                                 const float* __restrict__ xss,
+                                                                 const float* __restrict__ wn_strip, int n_strips,
+                                                                 float err_coef, int32_t* __restrict__ topk_idx,
                                                                  float* __restrict__ topk_w,
                                                                  int32_t* __restrict__ flagged,
                                                                  int32_t* __restrict__ flagged_count,
                                                                  int32_t* status) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (t >= T) return;
   float s[kMaxPerLane];
-  float lmax = 0.f;
   float l[kMaxPerLane];
 #pragma unroll
   for (int i = 0; i < kMaxPerLane; ++i) l[i] = 0.f;
+  float xs = 0.f;
   for (int sp = 0; sp < splits; ++sp) {  // eight independent loads per split, summed in split order
     const float* row = part + (static_cast<size_t>(sp) * T + t) * E;
     float v[kMaxPerLane];
@@ -563,25 +638,18 @@ __global__ void __launch_bounds__(256) router_select_flag_kernel(const float* __
     for (int i = 0; i < kMaxPerLane; ++i) v[i] = (lane + 32 * i < E) ? row[lane + 32 * i] : 0.f;
 #pragma unroll
     for (int i = 0; i < kMaxPerLane; ++i) l[i] += v[i];
+    xs += xss[static_cast<size_t>(sp) * T + t];
   }
+  float wn = 0.f;
+  for (int i = 0; i < n_strips; ++i) wn = fmaxf(wn, wn_strip[i]);
 #pragma unroll
   for (int i = 0; i < kMaxPerLane; ++i) {
     const int e = lane + 32 * i;
-    s[i] = -1.0f;
-    if (e < E) {
-      lmax = fmaxf(lmax, fabsf(l[i]));
-      s[i] = 1.0f / (1.0f + expf(-l[i]));
-    }
+    s[i] = (e < E) ? 1.0f / (1.0f + expf(-l[i])) : -1.0f;
   }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, off));
   const float2 margin = warp_select(s, bias, lane, t, E, G, Gk, K, scale, topk_idx, topk_w, status);
-  // Score error bound of the tensor-core logits: measured at most 4.7e-6 on
-  // Beam-shape inputs (|logit| <= 6, over a million scores); e_s keeps a factor
-  // of at least 2.5. A group score sums two scores and a group margin compares
-  // two group scores (4 e_s); expert margins and slot gaps compare two scores.
-  const float e_s = 1e-5f + 5e-7f * lmax;
-  const bool narrow = margin.x < 4.f * e_s || margin.y < 2.f * e_s;
+  const float e_s = 0.25f * err_coef * sqrtf(xs) * wn;
+  const bool narrow = !(margin.x >= 4.f * e_s && margin.y >= 2.f * e_s);  // NaN margins are narrow too
   if (lane == 0 && narrow) flagged[atomicAdd(flagged_count, 1)] = t;
 }
 
@@ -605,7 +673,7 @@ int flag_splits(int d) { return d % (kFlagSplits * kFlagRows) == 0 ? kFlagSplits
 __global__ void __launch_bounds__(kFlagThreads) router_flagged_logits_kernel(
     const uint16_t* __restrict__ x, const float* __restrict__ wr, int d, int E,
     const int32_t* __restrict__ flagged, const int32_t* __restrict__ flagged_count, float* __restrict__ part_out,
-    int splits, int32_t* status) {
+    int splits, int32_t* status, int32_t* timeout_where, long long wait_spins) {
   extern __shared__ __align__(16) uint8_t fsm[];
   float4* xs4 = reinterpret_cast<float4*>(fsm);                      // [d / splits]: x of <= 4 tokens at k
   float* wring = reinterpret_cast<float*>(fsm + sizeof(float4) * (d / splits));  // [ring][rows][E]
@@ -613,6 +681,8 @@ __global__ void __launch_bounds__(kFlagThreads) router_flagged_logits_kernel(
   __shared__ __align__(8) uint64_t bar[kFlagRing];
   __shared__ int abort_flag;
   volatile int* abort = &abort_flag;
+  pdl_launch_dependents();
+  pdl_wait();
   const int n = *flagged_count;
   if (n == 0) return;
   const int groups = (n + kFlagTokens - 1) / kFlagTokens;
@@ -661,8 +731,9 @@ __global__ void __launch_bounds__(kFlagThreads) router_flagged_logits_kernel(
       const uint32_t slot = consumed % kFlagRing;
       // On a timeout every later wait returns at once (the loop stays the same
       // for all threads, so the barriers below match); the status is latched.
-      if (!mbar_wait_bounded(&bar[slot], (consumed / kFlagRing) & 1u, 1ll << 40, 2000000000ull, abort) && !*abort) {
+      if (!mbar_wait_bounded(&bar[slot], (consumed / kFlagRing) & 1u, wait_spins, 2000000000ull, abort) && !*abort) {
         latch_status(status, MOE_DEV_TIMEOUT);
+        if (timeout_where) atomicCAS(timeout_where, 0, 14);
         *abort = 1;
       }
       ++consumed;
@@ -713,6 +784,8 @@ __global__ void __launch_bounds__(256) router_flagged_select_kernel(const float*
                                                                    const int32_t* __restrict__ flagged_count,
                                                                    int32_t* __restrict__ topk_idx,
                                                                    float* __restrict__ topk_w, int32_t* status) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int n = *flagged_count;
   const int lane = threadIdx.x & 31;
   for (int i = blockIdx.x * 8 + (threadIdx.x >> 5); i < n; i += gridDim.x * 8) {
@@ -782,31 +855,70 @@ int router_tc_splits(int T, int d, int num_sms) {
   return best;
 }
 
-size_t router_tc_scratch_bytes(int T, int d, int E) {
-  const size_t a = sizeof(uint16_t) * 3 * router_epad(E) * static_cast<size_t>(d);
-  return ((a + 255) & ~size_t(255)) + ((sizeof(int32_t) * T + 255) & ~size_t(255));
+// Splits of the hidden dimension the scratch is sized for (the split grows with
+// the SM count; 1024 SMs bound every device).
+int router_tc_max_splits(int T, int d) { return router_tc_splits(std::max(T, 1), d, 1024); }
+
+namespace {
+
+size_t up256(size_t b) { return (b + 255) & ~size_t(255); }
+
+// Tensor-core router scratch: the split W_r [3][E_pad][d] bf16, the flagged
+// tokens [T], the column sums of squares [d/32][E32] and the strips' largest
+// column norms [8] fp32, and the token sums of squares [splits][T] fp32.
+struct TcScratch {
+  uint16_t* w_split;
+  int32_t* flagged;
+  float* colss;
+  float* wn_strip;
+  float* xss;
+  size_t bytes;
+};
+
+TcScratch tc_scratch(void* base, int T, int d, int E) {
+  const int E_pad = router_epad(E), E32 = (E_pad + 31) / 32 * 32;
+  uint8_t* p = static_cast<uint8_t*>(base);
+  size_t o = 0;
+  TcScratch s;
+  s.w_split = reinterpret_cast<uint16_t*>(p + o);
+  o += up256(sizeof(uint16_t) * 3 * E_pad * static_cast<size_t>(d));
+  s.flagged = reinterpret_cast<int32_t*>(p + o);
+  o += up256(sizeof(int32_t) * static_cast<size_t>(T));
+  s.colss = reinterpret_cast<float*>(p + o);
+  o += up256(sizeof(float) * static_cast<size_t>(d / 32) * E32);
+  s.wn_strip = reinterpret_cast<float*>(p + o);
+  o += 256;
+  s.xss = reinterpret_cast<float*>(p + o);
+  o += up256(sizeof(float) * static_cast<size_t>(router_tc_max_splits(T, d)) * T);
+  s.bytes = o;
+  return s;
 }
 
+}  // namespace
+
+size_t router_tc_scratch_bytes(int T, int d, int E) { return tc_scratch(nullptr, T, d, E).bytes; }
+
+// Tensor-core accumulation error constant of the flag bound (kappa): the
+// largest measured |logit error| / (2^-23 sqrt(d/16) |x_t| |W_r[:, e]|) over
+// Beam-shape inputs (normal, outlier channels, router columns aligned with
+// the tokens, scaled by powers of two) times a safety factor.
+constexpr float kTcErrKappa = 0.25f;
+
 cudaError_t launch_router_tc(const uint16_t* x, const float* w_r, void* scratch, float* part, int32_t* flagged_count,
-                             int T, int d, int E, int n_groups, int topk_groups, int top_k, float routed_scale,
-                             const float* sel_bias, int32_t* topk_idx, float* topk_w, int32_t* status, int num_sms,
+                             int32_t* hdr_ticket, int T, int d, int E, int n_groups, int topk_groups, int top_k,
+                             float routed_scale, const float* sel_bias, int32_t* topk_idx, float* topk_w,
+                             int32_t* status, int32_t* timeout_where, long long wait_spins, int num_sms,
                              cudaStream_t stream) {
   const int E_pad = router_epad(E);
-  uint8_t* p = static_cast<uint8_t*>(scratch);
-  auto take = [&p](size_t bytes) {
-    uint8_t* q = p;
-    p += (bytes + 255) & ~size_t(255);
-    return q;
-  };
-  uint16_t* w_split = reinterpret_cast<uint16_t*>(take(sizeof(uint16_t) * 3 * E_pad * static_cast<size_t>(d)));
-  int32_t* flagged = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * T));
-  wr_split_kernel<<<dim3(d / 32, (E_pad + 31) / 32), 256, 0, stream>>>(w_r, d, E, E_pad, w_split, flagged_count);
-  cudaError_t err = cudaGetLastError();
+  const TcScratch sc = tc_scratch(scratch, T, d, E);
+  const dim3 split_grid(d / 32, (E_pad + 31) / 32);
+  cudaError_t err = launch_pdl(wr_split_kernel, split_grid, dim3(256), 0, stream, w_r, d, E, E_pad, sc.w_split, sc.colss,
+                               sc.wn_strip, hdr_ticket, flagged_count);
   if (err != cudaSuccess) return err;
   CUtensorMap tmX, tmW;
-  if (encode_router_map(&tmX, x, d, T, kTcTokens) || encode_router_map(&tmW, w_split, d, 3ull * E_pad, E_pad))
+  if (encode_router_map(&tmX, x, d, T, kTcTokens) || encode_router_map(&tmW, sc.w_split, d, 3ull * E_pad, E_pad))
     return cudaErrorInvalidValue;
-  const int splits = router_tc_splits(T, d, num_sms);
+  const int splits = std::min(router_tc_splits(T, d, num_sms), router_tc_max_splits(T, d));
   TcArgs a;
   a.T = T;
   a.d = d;
@@ -814,17 +926,25 @@ cudaError_t launch_router_tc(const uint16_t* x, const float* w_r, void* scratch,
   a.E_pad = E_pad;
   a.kb_per_split = d / kTcBK / splits;
   a.part = part;
+  a.x = x;
+  a.xss = sc.xss;
   a.status = status;
+  a.timeout_where = timeout_where;
+  a.wait_spins = wait_spins;
   a.stage_bytes = ((kTcTokens * kTcBK * 2 + 3 * E_pad * kTcBK * 2) + 1023u) & ~1023u;
   a.tmem_cols = 32;
   while (a.tmem_cols < static_cast<uint32_t>(2 * E_pad)) a.tmem_cols <<= 1;
   const size_t smem = 1024 + static_cast<size_t>(kTcStages) * a.stage_bytes;
   err = cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  router_tc_kernel<<<dim3((T + kTcTokens - 1) / kTcTokens, splits), 192, smem, stream>>>(tmX, tmW, a);
-  router_select_flag_kernel<<<(T + 7) / 8, 256, 0, stream>>>(part, splits, T, E, n_groups, topk_groups, top_k,
-                                                             routed_scale, sel_bias, topk_idx, topk_w, flagged,
-                                                             flagged_count, status);
+  err = launch_pdl(router_tc_kernel, dim3((T + kTcTokens - 1) / kTcTokens, splits), dim3(192), smem, stream, tmX, tmW,
+                   a);
+  if (err != cudaSuccess) return err;
+  const float err_coef = kTcErrKappa * 0x1p-23f * sqrtf(static_cast<float>(d) / 16.0f);
+  err = launch_pdl(router_select_flag_kernel, dim3((T + 7) / 8), dim3(256), 0, stream, part, splits, T, E, n_groups,
+                   topk_groups, top_k, routed_scale, sel_bias, sc.xss, sc.wn_strip, static_cast<int>(split_grid.y),
+                   err_coef, topk_idx, topk_w, sc.flagged, flagged_count, status);
+  if (err != cudaSuccess) return err;
   // the tensor-core partials were consumed by the selection: reuse `part` for the recompute
   const int fsplits = flag_splits(d);
   const size_t xs_bytes = sizeof(float4) * static_cast<size_t>(d / fsplits) +
@@ -832,12 +952,11 @@ cudaError_t launch_router_tc(const uint16_t* x, const float* w_r, void* scratch,
   err = cudaFuncSetAttribute(router_flagged_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(xs_bytes));
   if (err != cudaSuccess) return err;
-  router_flagged_logits_kernel<<<num_sms, kFlagThreads, xs_bytes, stream>>>(x, w_r, d, E, flagged, flagged_count,
-                                                                            part, fsplits, status);
-  router_flagged_select_kernel<<<num_sms, 256, 0, stream>>>(part, fsplits, E, n_groups, topk_groups, top_k,
-                                                            routed_scale, sel_bias, flagged, flagged_count, topk_idx,
-                                                            topk_w, status);
-  return cudaGetLastError();
+  err = launch_pdl(router_flagged_logits_kernel, dim3(num_sms), dim3(kFlagThreads), xs_bytes, stream, x, w_r, d, E,
+                   sc.flagged, flagged_count, part, fsplits, status, timeout_where, wait_spins);
+  if (err != cudaSuccess) return err;
+  return launch_pdl(router_flagged_select_kernel, dim3(num_sms), dim3(256), 0, stream, part, fsplits, E, n_groups,
+                    topk_groups, top_k, routed_scale, sel_bias, sc.flagged, flagged_count, topk_idx, topk_w, status);
 }
 
 // Smallest split of the hidden dimension (into >= 64-element slices) that
@@ -857,9 +976,8 @@ int router_splits(int T, int d, int E, int num_sms) {
 
 cudaError_t launch_router_logits(const uint16_t* x, const float* w_r, float* partial, int T, int d, int E,
                                  int splits, cudaStream_t stream) {
-  dim3 grid((E + RE - 1) / RE, (T + RT - 1) / RT, splits);
-  router_logits_kernel<<<grid, 256, 0, stream>>>(x, w_r, partial, T, d, E, d / splits);
-  return cudaGetLastError();
+  const dim3 grid((E + RE - 1) / RE, (T + RT - 1) / RT, splits);
+  return launch_pdl(router_logits_kernel, grid, dim3(256), 0, stream, x, w_r, partial, T, d, E, d / splits);
 }
 
 cudaError_t launch_router_select(float* partial, int splits, int T, int E, int n_groups, int topk_groups,
@@ -867,11 +985,12 @@ cudaError_t launch_router_select(float* partial, int splits, int T, int E, int n
                                  float* topk_w, int32_t* status, cudaStream_t stream) {
   if (splits > 1) {
     const int64_t n = static_cast<int64_t>(T) * E;
-    split_reduce_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(partial, splits, n);
+    const cudaError_t err = launch_pdl(split_reduce_kernel, dim3(static_cast<unsigned>((n + 255) / 256)), dim3(256), 0,
+                                       stream, partial, splits, n);
+    if (err != cudaSuccess) return err;
   }
-  router_select_kernel<<<(T + 7) / 8, 256, 0, stream>>>(partial, T, E, n_groups, topk_groups, top_k, routed_scale,
-                                                         sel_bias, topk_idx, topk_w, status);
-  return cudaGetLastError();
+  return launch_pdl(router_select_kernel, dim3((T + 7) / 8), dim3(256), 0, stream, partial, T, E, n_groups,
+                    topk_groups, top_k, routed_scale, sel_bias, topk_idx, topk_w, status);
 }
 
 }  // namespace beammoe

@@ -19,11 +19,12 @@ import sparse_moe_layer_14_b300 as bm
 TIE_EPS = 1e-6
 TOL_BF16 = 2e-2   # max |err| <= TOL * RMS(oracle output), bf16 weights
 TOL_NVFP4 = 5e-2  # ... NVFP4 weights
-# FP8 weights: the max bar follows from the typical error of the on-chip weight rounding (a
-# relative RMS of ~3.9e-3, reproduced by the CPU model in test_fp8_error_model.py, which derives
-# this bar) and the largest comparison a test makes (~4e6 elements): a Gaussian tail reaches
-# sqrt(2 ln 4e6) ~ 5.5 times the RMS there, 2.2e-2; the bar keeps a third above that.
-TOL_FP8 = 3e-2
+# FP8 weights: the max bar follows from the error of the on-chip weight rounding bf16(e4m3 x
+# scale), which a CPU model of exactly these roundings reproduces (test_fp8_error_model.py, which
+# derives this bar): a relative RMS of ~3.5e-3 with tails up to ~1.45 x Gaussian at small
+# reduction lengths, so over the largest comparison a test makes (~4e6 elements) the max is
+# expected near 2.8e-2; the bar keeps a fifth above that.
+TOL_FP8 = 3.5e-2
 TOL = {"bf16": TOL_BF16, "nvfp4": TOL_NVFP4, "fp8": TOL_FP8}
 # Typical (RMS) error bar of the expert FFN relative to the RMS output. bf16 and
 # NVFP4 weights reach the tensor cores exactly, leaving fp32 summation order and
@@ -214,8 +215,9 @@ def _valid_under_ties(s, gs, chosen, gsz, Gk, K, kept):
 def check_output(gpu_out_bits: np.ndarray, ref: np.ndarray, tol: float, label: str | None = None,
                  rms_bar: float | None = None):
     """max |gpu - ref| <= tol * RMS(ref) (and, given rms_bar, RMS(gpu - ref) <= rms_bar * RMS(ref));
-    logs both ratios under `label`; returns (max_err, rms)."""
-    g = bf16_to_f64(gpu_out_bits)
+    logs both ratios under `label`; returns (max_err, rms). gpu_out_bits: bf16 bit patterns
+    (uint16) or float32 values."""
+    g = bf16_to_f64(gpu_out_bits) if gpu_out_bits.dtype == np.uint16 else gpu_out_bits.astype(np.float64)
     rms = float(np.sqrt(np.mean(ref ** 2)))
     e = np.abs(g - ref)
     err = float(np.max(e))

@@ -3,7 +3,7 @@
 The expert GEMMs take bf16 operands, so FP8 weights are dequantised on chip as
 bf16(fp32(e4m3 * block scale)); the oracle keeps the exact product. This test
 repeats exactly those roundings in numpy (bf16 weights, FP32 SwiGLU, bf16 h,
-bf16 y) and measures their error against the oracle: it must sit below the
+FP32 y) and measures their error against the oracle: it must sit below the
 bar the GPU tests use, and removing the weight rounding must bring it back
 below the bf16 bar. A bar that merely hid a kernel bug would not be explained
 by this model.
@@ -36,7 +36,7 @@ def _model(x, row_e, host, d, inter, round_weights):
         g = (deq["gate"][e] @ xf[i]).astype(np.float32)
         u = (deq["up"][e] @ xf[i]).astype(np.float32)
         h = _bf16(g / (1 + np.exp(-g)) * u).astype(np.float64)
-        y[i] = _bf16((deq["down"][e] @ h).astype(np.float32))
+        y[i] = (deq["down"][e] @ h).astype(np.float32)
     return y
 
 
@@ -74,21 +74,23 @@ def _model_batched(x, row_e, host, E, round_weights=True):
         g = (xf[r] @ deq["gate"].T).astype(np.float32)
         u = (xf[r] @ deq["up"].T).astype(np.float32)
         h = _bf16(g / (1 + np.exp(-g)) * u).astype(np.float64)
-        y[r] = _bf16((h @ deq["down"].T).astype(np.float32))
+        y[r] = (h @ deq["down"].T).astype(np.float32)
     return y
 
 
 def test_fp8_max_bar_follows_from_the_model():
-    """The max-error bar of the FP8 tests, from the model at the Beam shape (d = 5120,
-    inter = 2560): over n elements its max error is close to Gaussian, c * RMS * sqrt(2 ln n) with
-    c ~ 1.14 (measured here; 1.14 again at 3.9e6 elements), so over the largest GPU comparison
-    (~4e6 elements) the max is expected at c * RMS * sqrt(2 ln 4e6) ~ 2.4e-2 of the output RMS.
-    TOL_FP8 sits 1.15-2x above that: tight, unlike the NVFP4 bar it replaced."""
-    x, row_e, host, d, inter, ref = _case(n=96, d=5120, inter=2560, E=2, seed=5)
-    rms = np.sqrt(np.mean(ref ** 2))
-    err = np.abs(_model_batched(x, row_e, host, 2) - ref) / rms
-    rel_rms, rel_max = float(np.sqrt(np.mean(err ** 2))), float(err.max())
-    c = rel_max / (rel_rms * np.sqrt(2 * np.log(err.size)))
-    assert 3e-3 < rel_rms < RMS_BAR["fp8"] and c <= 1.25, (rel_rms, rel_max, c)
-    expected = c * rel_rms * np.sqrt(2 * np.log(4e6))
-    assert 1.15 * expected <= TOL_FP8 <= 2.0 * expected, (expected, TOL_FP8)
+    """The max-error bar of the FP8 tests, from the model: over n compared elements its max error
+    behaves like c * RMS * sqrt(2 ln n), with c from 1.0 (Beam shape, d = 5120) to ~1.45 (small
+    reduction lengths, d = 256: fewer terms, heavier tails). Over the largest GPU comparison
+    (~4e6 elements) the worst shape's max is expected at c * RMS * sqrt(2 ln 4e6) ~ 2.8e-2 of the
+    output RMS; TOL_FP8 sits 1.15-2x above that (not at the NVFP4 bar)."""
+    worst = 0.0
+    for n, d, inter in ((384, 256, 384), (96, 5120, 2560)):
+        x, row_e, host, _, _, ref = _case(n=n, d=d, inter=inter, E=2, seed=5)
+        rms = np.sqrt(np.mean(ref ** 2))
+        err = np.abs(_model_batched(x, row_e, host, 2) - ref) / rms
+        rel_rms, rel_max = float(np.sqrt(np.mean(err ** 2))), float(err.max())
+        c = rel_max / (rel_rms * np.sqrt(2 * np.log(err.size)))
+        assert 2.5e-3 < rel_rms < RMS_BAR["fp8"] and c <= 1.6, (d, rel_rms, rel_max, c)
+        worst = max(worst, c * rel_rms * np.sqrt(2 * np.log(4e6)))
+    assert 1.15 * worst <= TOL_FP8 <= 2.0 * worst, (worst, TOL_FP8)
