@@ -56,15 +56,24 @@ def router_splits(T, d, E, num_sms):
 ROUTER_TC_MIN_TOKENS = 1024  # the library routes batches this large on the tensor cores
 
 
+def permute_uses_plan_kernel(T, E):
+    """The library's small-batch permutation rule (permute.cu): one plan kernel when the token x
+    expert bitmap (E * ceil(T/32) words) fits in 8192 words of shared memory."""
+    return E <= 256 and E * ((T + 31) // 32) <= 8192
+
+
 def kernels_per_step(cfg, num_sms):
     """Kernels one moe_forward launches: router (tensor-core: W_r split, tensor-core logits,
     selection, narrow-margin recompute (logits + selection); SIMT: logits [+ split reduce] +
-    select), permute (4), schedule, GEMM1, GEMM2, combine."""
+    select), permutation (small batches: plan kernel, which also builds the GEMM work items, +
+    gather; otherwise bitmap, column scan, offsets, gather + the GEMMs' schedule kernel),
+    GEMM1, GEMM2, combine."""
     if cfg.T >= ROUTER_TC_MIN_TOKENS:
         router = 5
     else:
         router = 2 + (1 if router_splits(cfg.T, cfg.d, cfg.E, num_sms) > 1 else 0)
-    return router + 4 + 1 + 2 + 1
+    permute_and_schedule = 2 if permute_uses_plan_kernel(cfg.T, cfg.E) else 5
+    return router + permute_and_schedule + 2 + 1
 
 
 def max_over_ranks(value, world, device):
@@ -159,6 +168,77 @@ def profiled_traffic(workload, kernel, algorithmic_bytes):
     measured = k["dram_bytes_read"] + k["dram_bytes_write"]
     return int(round(measured * algorithmic_bytes / k["algorithmic_bytes"])), (
         f"ncu dram__bytes_read+write of {cap_name} ({cap['workload']}), scaled by algorithmic bytes")
+
+
+# kernel names in ncu's launch list -> the names bench.py reports (template <GLU, format>)
+NCU_GEMM_NAMES = {"<1, 0>": "expert_gemm_kernel<GLU>", "<0, 0>": "expert_gemm_kernel<plain>",
+                  "<1, 1>": "expert_gemm_kernel<GLU, NVFP4>", "<0, 1>": "expert_gemm_kernel<plain, NVFP4>",
+                  "<1, 2>": "expert_gemm_kernel<GLU, FP8>", "<0, 2>": "expert_gemm_kernel<plain, FP8>"}
+TRAFFIC_SOURCES = ["sparse_moe_layer_14_b300/csrc/expert_gemm.cu", "sparse_moe_layer_14_b300/csrc/common.cuh",
+                   "sparse_moe_layer_14_b300/csrc/schedule.cuh"]
+TRAFFIC_CAPTURES = {"decode": "profile_decode", "prefill": "profile_prefill", "skewed": "profile_dense",
+                    "nvfp4": "profile_nvfp4", "fp8": "profile_fp8"}
+
+
+def parse_ncu_csv(path):
+    """ncu --csv --log-file output -> list of (kernel name, {metric: value in base units}) per launch."""
+    import csv
+    rows = [r for r in csv.reader(open(path)) if r]
+    hi = next(i for i, r in enumerate(rows) if r[0] == "ID")
+    hdr = rows[hi]
+    ki, mi, ni, ui = (hdr.index(c) for c in ("Kernel Name", "Metric Value", "Metric Name", "Metric Unit"))
+    scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "ns": 1, "us": 1e3, "usecond": 1e3, "ms": 1e6,
+             "msecond": 1e6, "nsecond": 1}
+    launches = {}
+    for r in rows[hi + 1:]:
+        if len(r) <= mi:
+            continue
+        d = launches.setdefault(r[0], [r[ki], {}])
+        d[1][r[ni]] = float(r[mi].replace(",", "")) * scale.get(r[ui], 1)
+    return [tuple(v) for _, v in sorted(launches.items(), key=lambda kv: int(kv[0]))]
+
+
+def record_traffic(directory, out=None):
+    """Write profiles/dram_traffic.json from captures in `directory`: for every small case named in
+    TRAFFIC_CAPTURES, <case>.json (its plain bench line: experts touched) and <case>.csv (ncu
+    --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum over its GEMM1 and
+    GEMM2 launches). Algorithmic bytes per launch are this file's roofline_numbers for the case."""
+    import hashlib
+    peaks = load_peaks()
+    rec = {"sources": TRAFFIC_SOURCES, "note": "DRAM bytes of one launch from ncu on one B300; bench.py scales "
+           "them to its workload by algorithmic bytes", "capture_for_workload": {}, "captures": {}}
+    h = hashlib.sha256()
+    for src in TRAFFIC_SOURCES:
+        h.update(open(os.path.join(ROOT, src), "rb").read())
+    rec["source_sha256"] = h.hexdigest()
+    for workload, case in TRAFFIC_CAPTURES.items():
+        jpath, cpath = os.path.join(directory, case + ".json"), os.path.join(directory, case + ".csv")
+        if not (os.path.exists(jpath) and os.path.exists(cpath)):
+            continue
+        line = json.loads(open(jpath).read().strip().splitlines()[-1])
+        cfg = workload_cfg(case)
+        touched = line["layer_roofline"]["experts_touched"]
+        g1, g2, _ = roofline_numbers(cfg, touched, peaks)
+        kernels = {}
+        for name, m in parse_ncu_csv(cpath):
+            tmpl = name[name.index("<"):name.index(">") + 1] if "expert_gemm_kernel" in name else None
+            if tmpl not in NCU_GEMM_NAMES:
+                continue
+            kname = NCU_GEMM_NAMES[tmpl]
+            kernels[kname] = {"dram_bytes_read": int(m["dram__bytes_read.sum"]),
+                              "dram_bytes_write": int(m["dram__bytes_write.sum"]),
+                              "algorithmic_bytes": int((g1 if "GLU" in kname else g2)["bytes"]),
+                              "gpu_time_ns_serialised": int(m["gpu__time_duration.sum"])}
+        rec["captures"][case] = {"workload": describe(cfg), "experts_touched": touched, "kernels": kernels,
+                                 "command": f"ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,"
+                                            f"gpu__time_duration.sum --clock-control none -k regex:expert_gemm_kernel "
+                                            f"-s 6 -c 2 --csv python bench.py --workload {case} --steps 2 --warmup 3 "
+                                            f"--no-cpu-baseline"}
+        rec["capture_for_workload"][workload] = case
+        rec["capture_for_workload"][case] = case
+    out = out or os.path.join(ROOT, "profiles", "dram_traffic.json")
+    json.dump(rec, open(out, "w"), indent=1)
+    return out
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -815,7 +895,12 @@ def main():
     ap.add_argument("--residual", action="store_true",
                     help="end the block with the fused post-norm and depth-scaled residual update "
                          "(moe_forward_residual) instead of writing the output")
+    ap.add_argument("--record-traffic", metavar="DIR",
+                    help="write profiles/dram_traffic.json from the ncu captures and bench lines in DIR, then exit")
     args = ap.parse_args()
+    if args.record_traffic:
+        print(record_traffic(args.record_traffic))
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.steps is None:

@@ -72,7 +72,8 @@ typedef enum {
   MOE_DEV_BAD_ROW = 2,     /* a permuted-row index outside [0, T*top_k): skipped */
   MOE_DEV_DUP_EXPERT = 3,  /* a token names one expert in two slots: the slots share one row */
   MOE_DEV_TIMEOUT = 6,     /* a pipeline wait exceeded its bound; the kernel returned early */
-  MOE_DEV_ZERO_SUM = 7     /* a token's chosen scores summed to 0: its weights are set to 0 */
+  MOE_DEV_ZERO_SUM = 7,    /* a token's chosen scores summed to 0: its weights are set to 0 */
+  MOE_DEV_CHECK = 8        /* debug build only: an index failed its bounds check; the access was skipped */
 } moe_device_code_t;
 
 typedef enum { MOE_W_BF16 = 0, MOE_W_NVFP4 = 1, MOE_W_FP8 = 2 } moe_wfmt_t;

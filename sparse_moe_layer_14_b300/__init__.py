@@ -20,8 +20,8 @@ from dataclasses import dataclass
 import torch
 
 from . import _native as N
-from ._native import (MOE_DEV_BAD_EXPERT, MOE_DEV_BAD_ROW, MOE_DEV_DUP_EXPERT, MOE_DEV_OK, MOE_DEV_TIMEOUT,  # noqa: F401
-                      MOE_DEV_ZERO_SUM, MOE_W_BF16, MOE_W_FP8, MOE_W_NVFP4, MoeDims, MoeExpertWeights)
+from ._native import (MOE_DEV_BAD_EXPERT, MOE_DEV_BAD_ROW, MOE_DEV_CHECK, MOE_DEV_DUP_EXPERT, MOE_DEV_OK,  # noqa: F401
+                      MOE_DEV_TIMEOUT, MOE_DEV_ZERO_SUM, MOE_W_BF16, MOE_W_FP8, MOE_W_NVFP4, MoeDims, MoeExpertWeights)
 
 __all__ = ["MoEError", "Dims", "ExpertWeights", "moe_workspace_bytes", "moe_workspace_init", "moe_route",
            "moe_permute", "moe_permute_noalloc", "moe_expert_ffn", "moe_combine", "moe_combine_residual",
@@ -29,7 +29,7 @@ __all__ = ["MoEError", "Dims", "ExpertWeights", "moe_workspace_bytes", "moe_work
            "moe_dense_mlp",
            "moe_get_device_status", "moe_set_wait_bound", "moe_set_stage_events", "moe_version",
            "allocate_workspace", "allocate_dense_workspace", "library_path",
-           "MOE_DEV_OK", "MOE_DEV_BAD_EXPERT", "MOE_DEV_BAD_ROW", "MOE_DEV_DUP_EXPERT", "MOE_DEV_TIMEOUT", "MOE_DEV_ZERO_SUM",
+           "MOE_DEV_OK", "MOE_DEV_BAD_EXPERT", "MOE_DEV_BAD_ROW", "MOE_DEV_DUP_EXPERT", "MOE_DEV_CHECK", "MOE_DEV_TIMEOUT", "MOE_DEV_ZERO_SUM",
            "MOE_W_BF16", "MOE_W_NVFP4", "MOE_W_FP8"]
 
 

@@ -5,7 +5,8 @@ import ctypes
 import os
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libbeammoe.so")
+# BEAMMOE_LIBRARY=debug selects the build with bounds checks (python -m sparse_moe_layer_14_b300.build --debug)
+LIB_PATH = os.path.join(HERE, "libbeammoe_debug.so" if os.environ.get("BEAMMOE_LIBRARY") == "debug" else "libbeammoe.so")
 
 # moe_status_t
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA = 0, 1, 2, 3, 4
@@ -15,6 +16,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
                 7: "MOE_ERR_SCRATCH_LIMIT"}
 # moe_device_code_t
 MOE_DEV_OK, MOE_DEV_BAD_EXPERT, MOE_DEV_BAD_ROW, MOE_DEV_DUP_EXPERT, MOE_DEV_TIMEOUT, MOE_DEV_ZERO_SUM = 0, 1, 2, 3, 6, 7
+MOE_DEV_CHECK = 8  # debug build only
 # moe_wfmt_t
 MOE_W_BF16, MOE_W_NVFP4, MOE_W_FP8 = 0, 1, 2
 
@@ -45,7 +47,8 @@ def load(path: str = LIB_PATH):
     if _lib is not None and path == LIB_PATH:
         return _lib
     if not os.path.exists(path):
-        raise RuntimeError(f"{path} is missing: build it with `python -m sparse_moe_layer_14_b300.build`")
+        raise RuntimeError(f"{path} is missing: build it with `python -m sparse_moe_layer_14_b300.build`"
+                           + (" --debug" if path.endswith("_debug.so") else ""))
     L = ctypes.CDLL(path)
     vp, sz, st = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
     pd, pw = ctypes.POINTER(MoeDims), ctypes.POINTER(MoeExpertWeights)

@@ -10,6 +10,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "schedule.cuh"
 
 using namespace beammoe;
 
@@ -162,10 +163,11 @@ moe_status_t do_route(const moe_dims_t* d, const uint16_t* x, const float* w_r, 
 
 moe_status_t do_permute(const moe_dims_t* d, const uint16_t* x, const int32_t* idx, int32_t* counts,
                         int32_t* offsets, int32_t* row_token, int32_t* inv_row, uint16_t* x_perm, void* ws,
-                        const Layout& L, cudaStream_t s, bool bitmap_zeroed = false) {
+                        const Layout& L, cudaStream_t s, bool bitmap_zeroed = false,
+                        const ScheduleArgs* sched = nullptr) {
   cudaError_t e = launch_permute(x, idx, d->T, d->d, d->E, d->top_k, region<uint32_t>(ws, L, R_BITMAP),
                                  region<int32_t>(ws, L, R_WPRE), counts, offsets, row_token, inv_row, x_perm,
-                                 status_word(ws), s, bitmap_zeroed);
+                                 status_word(ws), s, bitmap_zeroed, sched);
   return cuda_status(e);
 }
 
@@ -184,10 +186,7 @@ ExpertWeightsDev weights_dev(int wfmt, const moe_expert_weights_t* w) {
   return wd;
 }
 
-moe_status_t do_ffn(const moe_dims_t* d, const uint16_t* x_perm, const int32_t* offsets,
-                    const moe_expert_weights_t* w, float* y, void* ws, const Layout& L, cudaStream_t s,
-                    cudaEvent_t after_gemm1 = nullptr) {
-  const ExpertPlan pl = plan_experts(d->T, d->d, d->E, d->top_k, d->inter, d->wfmt != MOE_W_BF16);
+ExpertBuffers expert_buffers(const uint16_t* x_perm, const int32_t* offsets, float* y, void* ws, const Layout& L) {
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
   ExpertBuffers b;
   b.x_perm = x_perm;
@@ -200,10 +199,18 @@ moe_status_t do_ffn(const moe_dims_t* d, const uint16_t* x_perm, const int32_t* 
   b.n_items = hdr->n_items;
   b.status = &hdr->status;
   b.timeout_where = &hdr->timeout_where;
+  return b;
+}
+
+moe_status_t do_ffn(const moe_dims_t* d, const uint16_t* x_perm, const int32_t* offsets,
+                    const moe_expert_weights_t* w, float* y, void* ws, const Layout& L, cudaStream_t s,
+                    cudaEvent_t after_gemm1 = nullptr, bool items_ready = false) {
+  const ExpertPlan pl = plan_experts(d->T, d->d, d->E, d->top_k, d->inter, d->wfmt != MOE_W_BF16);
+  const ExpertBuffers b = expert_buffers(x_perm, offsets, y, ws, L);
   const ExpertWeightsDev wd = weights_dev(d->wfmt, w);
   int cu_err = 0;
   const cudaError_t e = launch_expert_ffn(pl, b, wd, d->T, d->d, d->E, d->top_k, d->inter, num_sms(), g_wait_spins,
-                                          s, &cu_err, after_gemm1);
+                                          s, &cu_err, after_gemm1, items_ready);
   if (e == cudaErrorNotSupported) return MOE_ERR_UNSUPPORTED;
   return cuda_status(e);
 }
@@ -316,9 +323,15 @@ moe_status_t forward_impl(const moe_dims_t* dims, const moe_bf16_t* x, const flo
   int32_t* inv_row = region<int32_t>(ws, L, R_INVROW);
   uint16_t* x_perm = region<uint16_t>(ws, L, R_XPERM);
   float* y = region<float>(ws, L, R_Y);
-  // the permutation's bitmap is cleared first, so that no copy sits between the block's kernels
-  // (they launch back to back with programmatic dependencies)
-  if (cudaMemsetAsync(region<uint32_t>(ws, L, R_BITMAP), 0, bitmap_bytes(dims->T, dims->E), s) != cudaSuccess)
+  // Small batches: the permutation's plan kernel also builds the expert GEMMs' work items.
+  // Larger ones: the permutation's bitmap is cleared first, so that no copy sits between the
+  // block's kernels (they launch back to back with programmatic dependencies).
+  const bool plan_kernel = permute_uses_plan_kernel(dims->T, dims->E);
+  const ExpertPlan plan = plan_experts(dims->T, dims->d, dims->E, dims->top_k, dims->inter, dims->wfmt != MOE_W_BF16);
+  const ScheduleArgs sched =
+      schedule_args(plan, expert_buffers(x_perm, offs, y, ws, L), dims->T * dims->top_k);
+  if (!plan_kernel &&
+      cudaMemsetAsync(region<uint32_t>(ws, L, R_BITMAP), 0, bitmap_bytes(dims->T, dims->E), s) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (mark(0, s) != cudaSuccess) return MOE_ERR_CUDA;
   {
@@ -328,13 +341,15 @@ moe_status_t forward_impl(const moe_dims_t* dims, const moe_bf16_t* x, const flo
   if (mark(1, s) != cudaSuccess) return MOE_ERR_CUDA;
   {
     NvtxStage r("moe permute");
-    if ((st = do_permute(dims, x, idx, cnt, offs, row_token, inv_row, x_perm, ws, L, s, true)) != MOE_OK) return st;
+    if ((st = do_permute(dims, x, idx, cnt, offs, row_token, inv_row, x_perm, ws, L, s, true,
+                         plan_kernel ? &sched : nullptr)) != MOE_OK)
+      return st;
   }
   if (mark(2, s) != cudaSuccess) return MOE_ERR_CUDA;
   {
     NvtxStage r("moe expert GEMMs");
-    if ((st = do_ffn(dims, x_perm, offs, weights, y, ws, L, s, g_stage_events_on ? g_stage_events[3] : nullptr)) !=
-        MOE_OK)
+    if ((st = do_ffn(dims, x_perm, offs, weights, y, ws, L, s, g_stage_events_on ? g_stage_events[3] : nullptr,
+                     plan_kernel)) != MOE_OK)
       return st;
   }
   if (mark(4, s) != cudaSuccess) return MOE_ERR_CUDA;

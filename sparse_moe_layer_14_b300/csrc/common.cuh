@@ -28,6 +28,19 @@ __device__ __forceinline__ void latch_status(int32_t* status, int32_t code) {
   if (status) atomicCAS(status, 0, code);
 }
 
+// Bounds checks of the debug build (compiled with BEAMMOE_DEBUG_CHECKS): a
+// data-dependent index that fails its check latches MOE_DEV_CHECK and the
+// access is skipped. The release build compiles them out (the kernels' own
+// checks of routing indices and rows stay in both).
+#ifdef BEAMMOE_DEBUG_CHECKS
+__device__ __forceinline__ bool dcheck(bool ok, int32_t* status) {
+  if (!ok) latch_status(status, MOE_DEV_CHECK);
+  return ok;
+}
+#else
+__device__ __forceinline__ bool dcheck(bool, int32_t*) { return true; }
+#endif
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -88,12 +101,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Wait for the phase of `parity` to complete, giving up after `max_spins`
 // failed polls or `max_ns` nanoseconds, or as soon as *abort is set.
-// Returns true when the phase completed.
+// Returns true when the phase completed. With sleep_ns > 0 the thread sleeps
+// that long between polls, so a warp that waits off the critical path leaves
+// its scheduler's issue slots to the warps that work (the single thread that
+// issues the MMAs shares a scheduler with them).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, long long max_spins,
-                                                  uint64_t max_ns, volatile int* abort) {
+                                                  uint64_t max_ns, volatile int* abort, unsigned sleep_ns = 0) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (long long i = 1; i < max_spins; ++i) {
+    if (sleep_ns) __nanosleep(sleep_ns);
     if (mbar_try_wait(bar, parity)) return true;
     if (abort && *abort) return false;
     if ((i & 63) == 0 && globaltimer_ns() - t0 > max_ns) return false;
@@ -193,16 +210,14 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-// 32 lanes x 32 consecutive 32-bit columns: thread i of the warp writes
-// lane (base lane + i), columns [col, col+32).
-__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
+// 32 lanes x 16 consecutive 32-bit columns: thread i of the warp writes
+// lane (base lane + i), columns [col, col+16).
+__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
       "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
-      "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
-      "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
 }
 

@@ -24,14 +24,19 @@
 //   warp 0      TMA producer: weight tile(s) + token rows per 64-wide K slice
 //   warp 1      TMEM allocator and single-thread tcgen05.mma issuer
 //   warps 2..9  epilogue, two warpgroups splitting the token columns:
-//               tcgen05.ld, SwiGLU in FP32 (GEMM1) or the bf16 output (GEMM2)
-//   warps 10..17 (NVFP4 weights only) converters: e2m1 codes times their e4m3
-//               block scale, which is exact in bf16, written to tensor memory,
-//               from where the MMA reads its A operand (so decoded weights
-//               cost no shared-memory bandwidth, which the token operand and
-//               the copies need); the fp32 tensor scale is applied to the
-//               accumulator in the epilogue. The TMA ring holds packed codes
-//               and token rows; decoded tiles cycle through 2-4 TMEM slots.
+//               tcgen05.ld, SwiGLU in FP32 (GEMM1) or the FP32 expert output
+//               (GEMM2; bf16 for the dense MLP)
+//   warps 10..17 (NVFP4 and FP8 weights) converters: e2m1 codes times their
+//               e4m3 block scale (exact in bf16), or e4m3 codes times their
+//               fp32 block scale (rounded once to bf16), written to tensor
+//               memory, from where the MMA reads its A operand; the NVFP4 fp32
+//               tensor scale is applied to the accumulator in the epilogue.
+//               The TMA ring holds packed codes and token rows; decoded tiles
+//               cycle through 2-4 TMEM slots. (Decoded tiles staged in shared
+//               memory instead, read like bf16 tiles, measured slower.)
+// Waits off the critical path sleep between polls: the MMA issuer shares a
+// scheduler with epilogue and converter warps, and their spinning took its
+// issue slots (MMA slices up to 1.5x slower).
 // Work items {expert, weight tile, first row, tokens} are built on the device
 // from the expert offsets (no host synchronisation) and taken round-robin.
 // Every mbarrier wait is bounded; on expiry the CTA latches MOE_DEV_TIMEOUT,
@@ -40,6 +45,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "schedule.cuh"
 
 namespace beammoe {
 
@@ -50,8 +56,10 @@ constexpr int BK = 64;        // K elements per pipeline stage (128 bytes of bf1
 constexpr int TOK_BOX = 16;   // token rows per TMA box
 constexpr int kMaxStages = 8;
 constexpr int kMaxAcc = 4;
-constexpr int kMaxConv = 4;   // decoded NVFP4 weight slots in TMEM
-constexpr int kConvCols = 64;  // TMEM columns of one slot: two 128 x 64 bf16 tiles
+constexpr int kMaxConv = 4;   // decoded-weight slots in TMEM
+// TMEM columns of one slot: a K slice (64 elements) of both weight tiles, tile 0 in columns
+// [0, 32), tile 1 in [32, 64) (two bf16 a column)
+constexpr int kConvCols = 64;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kATileBytes = BM * BK * 2;            // 16 KB bf16 weight tile
 constexpr uint32_t kPTileBytes = BM * BK / 2;            // 4 KB packed e2m1 weight tile
@@ -63,6 +71,11 @@ constexpr uint32_t kTokBoxBytes = TOK_BOX * BK * 2;      // 2 KB
 constexpr uint64_t kDrainNs = 1000000000ull;             // 1 s bound for draining on abort
 constexpr uint64_t kWaitNs = 2000000000ull;              // 2 s bound of a pipeline wait
 constexpr int kSmemLimit = 232448;                       // 227 KB opt-in per block
+// Sleep between polls of a wait off the critical path (nanoseconds): the producer and
+// converters wait a slot at a time, the epilogue a whole item. The single thread that issues
+// the MMAs never sleeps; it shares a scheduler with two epilogue warps (and with converter
+// warps), and spinning neighbours would take its issue slots.
+constexpr unsigned kSleepSlotNs = 32, kSleepItemNs = 512;
 
 constexpr int kEpiThreads = 256;    // two epilogue warpgroups
 constexpr int kConvBase = 320;      // first converter thread (NVFP4)
@@ -75,6 +88,7 @@ struct GemmArgs {
   int K;           // reduction length
   int Nw;          // weight rows per expert = output columns
   int E;           // experts
+  int R;           // rows of the token operand (T * top_k)
   int n_max;       // max tokens per item (multiple of 16)
   int stages;
   int acc_bufs;
@@ -82,7 +96,7 @@ struct GemmArgs {
   uint32_t stage_bytes;
   uint32_t b_offset;  // token tile offset inside a stage
   uint32_t p_offset;  // packed weight tile offset inside a stage (NVFP4)
-  uint32_t a_col;     // first TMEM column of the decoded weight slots (NVFP4)
+  uint32_t a_col;     // first TMEM column of the decoded weight slots (NVFP4, FP8)
   int conv_stages;
   uint16_t* h_out;    // GEMM1 output [R][Nw] bf16
   uint16_t* y_out;    // GEMM2 output [R][Nw] bf16 (the dense MLP's output), or null
@@ -135,25 +149,20 @@ __device__ __forceinline__ uint32_t scale_pair(uint32_t byte) {
   return s;
 }
 
-// Decode row r of one packed 128 x 64 weight tile (64 e2m1 codes in 32 bytes)
-// with its four e4m3 block scales `sc` (byte j: elements 16j..16j+15) into 32
-// bf16x2 words in element order: word c holds elements 2c (low half) and 2c+1.
-__device__ __forceinline__ void decode_row(const uint8_t* packed_tile, int r, uint32_t sc, uint32_t (&out)[32]) {
-  const uint4 p0 = *reinterpret_cast<const uint4*>(packed_tile + r * 32);
-  const uint4 p1 = *reinterpret_cast<const uint4*>(packed_tile + r * 32 + 16);
-  const uint32_t w[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint32_t s2 = scale_pair((sc >> (8 * j)) & 0xFFu);
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const uint4 v = decode8(w[2 * j + hh], s2);
-      out[8 * j + 4 * hh + 0] = v.x;
-      out[8 * j + 4 * hh + 1] = v.y;
-      out[8 * j + 4 * hh + 2] = v.z;
-      out[8 * j + 4 * hh + 3] = v.w;
-    }
-  }
+// Decode half h of row r of one packed 128 x 64 weight tile (the row's 64
+// e2m1 codes are 32 bytes; half h is elements 32h..32h+31, bytes 16h..16h+15)
+// with its two e4m3 block scales (bytes 2h and 2h+1 of `sc`, the row's four
+// scales of the slice) into 16 bf16x2 words in element order: word c holds
+// elements 32h + 2c (low half) and 32h + 2c + 1.
+__device__ __forceinline__ void decode_half(const uint8_t* packed_tile, int r, int h, uint32_t sc,
+                                            uint32_t (&out)[16]) {
+  const uint4 p = *reinterpret_cast<const uint4*>(packed_tile + r * 32 + h * 16);
+  const uint32_t s2a = scale_pair((sc >> (16 * h)) & 0xFFu), s2b = scale_pair((sc >> (16 * h + 8)) & 0xFFu);
+  const uint4 v0 = decode8(p.x, s2a), v1 = decode8(p.y, s2a), v2 = decode8(p.z, s2b), v3 = decode8(p.w, s2b);
+  out[0] = v0.x, out[1] = v0.y, out[2] = v0.z, out[3] = v0.w;
+  out[4] = v1.x, out[5] = v1.y, out[6] = v1.z, out[7] = v1.w;
+  out[8] = v2.x, out[9] = v2.y, out[10] = v2.z, out[11] = v2.w;
+  out[12] = v3.x, out[13] = v3.y, out[14] = v3.z, out[15] = v3.w;
 }
 
 // Two e4m3 codes (low byte = lower element) times the fp32 block scale `s`:
@@ -166,13 +175,14 @@ __device__ __forceinline__ uint32_t e4m3x2_scaled_bf16x2(uint32_t two, float s) 
   return *reinterpret_cast<const uint32_t*>(&b);
 }
 
-// Row r of one 128 x 64 FP8 weight tile (64 e4m3 codes, element k in byte k)
-// scaled and rounded as above: 32 bf16x2 words in element order, word c
-// holding elements 2c (low half) and 2c+1.
-__device__ __forceinline__ void decode_row_fp8(const uint8_t* packed_tile, int r, float s, uint32_t (&out)[32]) {
-  const uint4* row = reinterpret_cast<const uint4*>(packed_tile + r * 64);
+// Half h of row r of one 128 x 64 FP8 weight tile (64 e4m3 codes, element k in
+// byte k; half h is bytes 32h..32h+31) scaled and rounded as above: 16 bf16x2
+// words in element order.
+__device__ __forceinline__ void decode_half_fp8(const uint8_t* packed_tile, int r, int h, float s,
+                                                uint32_t (&out)[16]) {
+  const uint4* row = reinterpret_cast<const uint4*>(packed_tile + r * 64 + h * 32);
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
+  for (int q = 0; q < 2; ++q) {
     const uint4 p = row[q];
     const uint32_t w[4] = {p.x, p.y, p.z, p.w};
 #pragma unroll
@@ -258,7 +268,7 @@ __global__ void __launch_bounds__(threads_for(kFmt), 1)
         const int nbox = (item.w + TOK_BOX - 1) / TOK_BOX;
         const uint32_t bytes = (kConv ? kPB : kATileBytes) * nA + static_cast<uint32_t>(nbox) * kTokBoxBytes;
         for (int kb = 0; kb < kblocks; ++kb) {
-          if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, p.wait_spins, kWaitNs, abort)) {
+          if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, p.wait_spins, kWaitNs, abort, kSleepSlotNs)) {
             if (!*abort) fail(p, abort, 1);
             ok = false;
             break;
@@ -314,39 +324,47 @@ __global__ void __launch_bounds__(threads_for(kFmt), 1)
         const uint32_t d1 = d0 + static_cast<uint32_t>(p.n_max);
         bool ok = true;
         for (int kb = 0; kb < kblocks; ++kb) {
-          // NVFP4 / FP8: the decoded slot is ready only after its raw stage landed
-          if (!mbar_wait_bounded(kConv ? &conv_bar[cstage] : &full_bar[stage], kConv ? cphase : phase, p.wait_spins,
-                                 kWaitNs, abort)) {
-            if (!*abort) fail(p, abort, 3);
-            ok = false;
-            break;
-          }
-          tc_fence_after();
           const uint32_t st_addr = smem_u32(smem + static_cast<size_t>(stage) * p.stage_bytes);
-          const uint32_t sb = st_addr + p.b_offset;
-          // NVFP4 / FP8: slot cstage holds tile 0 in columns [0, 32), tile 1 in [32, 64);
-          // 8 columns per 16-wide K step
-          const uint32_t ta = tmem_base + p.a_col + static_cast<uint32_t>(cstage * kConvCols);
-#pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
-            const uint64_t bdesc = sdesc_kmajor_sw128(sb + k * 32);
-            const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
-            if (kConv) {
-              mma_bf16_ts(d0, ta + k * 8, bdesc, idesc, accum);
-              mma_bf16_ts(d1, ta + kConvCols / 2 + k * 8, bdesc, idesc, accum);
-            } else {
-              mma_bf16_ss(d0, sdesc_kmajor_sw128(st_addr + k * 32), bdesc, idesc, accum);
-              mma_bf16_ss(d1, sdesc_kmajor_sw128(st_addr + kATileBytes + k * 32), bdesc, idesc, accum);
+          // one shared-memory descriptor per operand; a 16-wide K step (32 bytes) adds 2 to
+          // the start address field (bits 0-13, bytes >> 4), which never carries out of it
+          const uint64_t b0 = sdesc_kmajor_sw128(st_addr + p.b_offset);
+          if constexpr (kConv) {
+            // NVFP4 / FP8: the decoded slot is ready only after its raw stage landed. Slot
+            // columns: tile 0 [0, 32), tile 1 [32, 64), 8 per 16-wide K step.
+            if (!mbar_wait_bounded(&conv_bar[cstage], cphase, p.wait_spins, kWaitNs, abort)) {
+              if (!*abort) fail(p, abort, 3);
+              ok = false;
+              break;
             }
-          }
-          mma_commit(&empty_bar[stage]);
-          if (kConv) {
+            tc_fence_after();
+            const uint32_t ta = tmem_base + p.a_col + static_cast<uint32_t>(cstage * kConvCols);
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k) {
+              const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
+              mma_bf16_ts(d0, ta + k * 8, b0 + 2 * k, idesc, accum);
+              mma_bf16_ts(d1, ta + kConvCols / 2 + k * 8, b0 + 2 * k, idesc, accum);
+            }
             mma_commit(&conv_empty_bar[cstage]);
             if (++cstage == p.conv_stages) {
               cstage = 0;
               cphase ^= 1u;
             }
+          } else {
+            if (!mbar_wait_bounded(&full_bar[stage], phase, p.wait_spins, kWaitNs, abort)) {
+              if (!*abort) fail(p, abort, 3);
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t a0 = sdesc_kmajor_sw128(st_addr), a1 = sdesc_kmajor_sw128(st_addr + kATileBytes);
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k) {
+              const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
+              mma_bf16_ss(d0, a0 + 2 * k, b0 + 2 * k, idesc, accum);
+              mma_bf16_ss(d1, a1 + 2 * k, b0 + 2 * k, idesc, accum);
+            }
           }
+          mma_commit(&empty_bar[stage]);
           if (++stage == p.stages) {
             stage = 0;
             phase ^= 1u;
@@ -371,19 +389,24 @@ __global__ void __launch_bounds__(threads_for(kFmt), 1)
     for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
       const int4 item = p.items[it];
       // tcgen05.ld is warp-collective: the whole warp proceeds or stops together
-      const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&accf_bar[acc], acc_phase, p.wait_spins, kWaitNs, abort));
+      const bool ok = __all_sync(
+          0xffffffffu, mbar_wait_bounded(&accf_bar[acc], acc_phase, p.wait_spins, kWaitNs, abort, kSleepItemNs));
       if (!ok) {
         if (lane == 0 && !*abort) fail(p, abort, 4);
         break;
       }
       tc_fence_after();
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * p.acc_cols);
+      // debug build: the item's rows and expert lie inside the buffers
+      const bool item_ok = dcheck(item.x >= 0 && item.x < p.E && item.z >= 0 && item.w >= 0 && item.w <= p.n_max &&
+                                      static_cast<int64_t>(item.z) + item.w <= p.R,
+                                  p.status);
       const int col0 = item.y * kItemRows + r;       // output column of accumulator 0
       const int col1 = col0 + kRow1;                 // ... of accumulator 1 (GEMM2)
       const bool valid0 = col0 < p.Nw, valid1 = col1 < p.Nw;
-      const int ntok = item.w;
-      const float s0 = p.ts0 ? p.ts0[item.x] : 1.0f;
-      const float s1 = p.ts1 ? p.ts1[item.x] : s0;
+      const int ntok = item_ok ? item.w : 0;
+      const float s0 = p.ts0 && item_ok ? p.ts0[item.x] : 1.0f;
+      const float s1 = p.ts1 && item_ok ? p.ts1[item.x] : s0;
       // 16-token chunks eg*16, eg*16 + 32, ...: the TMEM loads of the next chunk
       // are in flight while this one is computed and stored, and the
       // accumulator is handed back to the MMA as soon as the last chunk's loads
@@ -478,7 +501,7 @@ __global__ void __launch_bounds__(threads_for(kFmt), 1)
     const int r = q * 32 + lane;
     const int row_off = t ? kRow1 : 0;
     const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + p.a_col +
-                            static_cast<uint32_t>(t * (kConvCols / 2));
+                            static_cast<uint32_t>(t * (kConvCols / 2));  // this tile's 32 columns of a slot
     int stage = 0, cstage = 0;
     uint32_t phase = 0, cphase = 0;
     // scale group g of item `it`: slices 4g .. 4g+3
@@ -486,6 +509,7 @@ __global__ void __launch_bounds__(threads_for(kFmt), 1)
       uint4 v = make_uint4(0, 0, 0, 0);
       if (it >= n_items) return v;
       const int4 item = p.items[it];
+      if (!dcheck(item.x >= 0 && item.x < p.E, p.status)) return v;
       if constexpr (kFp8) {
         const int nbr = p.Nw / BM, kbr = p.K / BM;  // 128-blocks per expert: rows, K
         const int br = (item.y * kItemRows + row_off) / BM;
@@ -507,69 +531,48 @@ __global__ void __launch_bounds__(threads_for(kFmt), 1)
       return v;
     };
     uint4 cur = make_uint4(0, 0, 0, 0), nxt = load_group(blockIdx.x, 0);
-    // With three or more decoded slots the arrival that hands a slot to the MMA
-    // is deferred by one slice: the slice's tcgen05.st completes while the next
-    // slice is decoded (into the other register set), and tcgen05.wait::st
-    // then finds it done. With two slots the MMA would wait for that next
-    // decode, so each slice is handed over at once.
-    const bool defer = p.conv_stages >= 3;
-    int pend = -1;  // slot whose store is in flight and not yet handed over
     bool ok = true;
-    uint32_t va[32], vb[32];
-    auto slice = [&](int it, int kb, uint32_t (&v)[32]) {
-      if ((kb & 3) == 0) {
-        cur = nxt;
-        nxt = kb + 4 < kblocks ? load_group(it, (kb >> 2) + 1) : load_group(it + gridDim.x, 0);
-      }
-      // tcgen05.st is warp-collective: the whole warp proceeds or stops together
-      const bool ready = __all_sync(
-          0xffffffffu, mbar_wait_bounded(&full_bar[stage], phase, p.wait_spins, kWaitNs, abort) &&
-                           mbar_wait_bounded(&conv_empty_bar[cstage], cphase ^ 1u, p.wait_spins, kWaitNs, abort));
-      if (!ready) {
-        if (lane == 0 && !*abort) fail(p, abort, 5);
-        return false;
-      }
-      tc_fence_after();  // the MMAs that read this slot have completed
-      const uint8_t* packed = smem + static_cast<size_t>(stage) * p.stage_bytes + p.p_offset + t * kPB;
-      const int g = kb & 3;
-      if constexpr (kFp8) {
-        decode_row_fp8(packed, r, __uint_as_float(g < 2 ? cur.x : cur.y), v);
-      } else {
-        decode_row(packed, r, g == 0 ? cur.x : g == 1 ? cur.y : g == 2 ? cur.z : cur.w, v);
-      }
-      if (defer) {
-        if (pend >= 0) {  // the previous slice's store (issued one decode ago)
-          tmem_st_wait();
-          tc_fence_before();
-          mbar_arrive(&conv_bar[pend]);
+    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if ((kb & 3) == 0) {
+          cur = nxt;
+          nxt = kb + 4 < kblocks ? load_group(it, (kb >> 2) + 1) : load_group(it + gridDim.x, 0);
         }
-        tmem_st_32x32b_x32(t_lane + static_cast<uint32_t>(cstage * kConvCols), v);
-        pend = cstage;
-      } else {
-        tmem_st_32x32b_x32(t_lane + static_cast<uint32_t>(cstage * kConvCols), v);
+        const uint8_t* packed = smem + static_cast<size_t>(stage) * p.stage_bytes + p.p_offset + t * kPB;
+        const int g = kb & 3;
+        // tcgen05.st is warp-collective: the whole warp proceeds or stops together
+        const bool ready = __all_sync(
+            0xffffffffu,
+            mbar_wait_bounded(&full_bar[stage], phase, p.wait_spins, kWaitNs, abort, kSleepSlotNs) &&
+                mbar_wait_bounded(&conv_empty_bar[cstage], cphase ^ 1u, p.wait_spins, kWaitNs, abort, kSleepSlotNs));
+        if (!ready) {
+          if (lane == 0 && !*abort) fail(p, abort, 5);
+          ok = false;
+          break;
+        }
+        tc_fence_after();  // the MMAs that read this slot have completed
+        // the row's two 32-element halves, each stored as soon as it is decoded
+#pragma unroll
+        for (int hk = 0; hk < 2; ++hk) {
+          uint32_t v[16];
+          if constexpr (kFp8) {
+            decode_half_fp8(packed, r, hk, __uint_as_float(g < 2 ? cur.x : cur.y), v);
+          } else {
+            decode_half(packed, r, hk, g == 0 ? cur.x : g == 1 ? cur.y : g == 2 ? cur.z : cur.w, v);
+          }
+          tmem_st_32x32b_x16(t_lane + static_cast<uint32_t>(cstage * kConvCols + hk * 16), v);
+        }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&conv_bar[cstage]);
-      }
-      if (++cstage == p.conv_stages) {
-        cstage = 0;
-        cphase ^= 1u;
-      }
-      if (++stage == p.stages) {
-        stage = 0;
-        phase ^= 1u;
-      }
-      return true;
-    };
-    // kblocks is even (K is a multiple of 128 for both decoded formats): two slices per
-    // iteration keep each register set in place
-    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x)
-      for (int kb = 0; kb < kblocks && ok; kb += 2) ok = slice(it, kb, va) && slice(it, kb + 1, vb);
-    if (pend >= 0) {  // after an abort too: no store may be in flight when TMEM is released
-      tmem_st_wait();
-      if (ok) {
-        tc_fence_before();
-        mbar_arrive(&conv_bar[pend]);
+        if (++cstage == p.conv_stages) {
+          cstage = 0;
+          cphase ^= 1u;
+        }
+        if (++stage == p.stages) {
+          stage = 0;
+          phase ^= 1u;
+        }
       }
     }
   }
@@ -599,60 +602,13 @@ __global__ void __launch_bounds__(threads_for(kFmt), 1)
   if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
 }
 
-// Work items from the expert offsets: one thread per expert (E <= 256).
-// Tokens of an expert are split into ceil(n/n_max) tiles of near-equal size
-// (multiples of 16). Items are ordered expert, weight tile, token tile so the
-// token tiles of one weight tile run side by side and share it through L2.
-__global__ void __launch_bounds__(256) schedule_kernel(const int32_t* __restrict__ offsets, int E, int R, int n_max,
-                                                       int wt1, int wt2, int4* __restrict__ items1,
-                                                       int4* __restrict__ items2, int32_t* __restrict__ n_items,
+// Work items from the expert offsets (build_work_items): one thread per expert (E <= 256).
+__global__ void __launch_bounds__(256) schedule_kernel(const int32_t* __restrict__ offsets, int E, ScheduleArgs s,
                                                        int32_t* status) {
   __shared__ int warp_sums[8];
   pdl_launch_dependents();
   pdl_wait();
-  const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
-  int n = 0, row0 = 0, ntiles = 0, tsz = 16;
-  if (e < E) {
-    const int a = offsets[e], b = offsets[e + 1];
-    if (a < 0 || b < a || b > R) {
-      latch_status(status, MOE_DEV_BAD_ROW);
-    } else {
-      n = b - a;
-      row0 = a;
-    }
-    if (n > 0) {
-      ntiles = (n + n_max - 1) / n_max;
-      tsz = ((n + ntiles - 1) / ntiles + 15) & ~15;
-      if (tsz > n_max) tsz = n_max;
-      ntiles = (n + tsz - 1) / tsz;
-    }
-  }
-  int incl = ntiles;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int o = __shfl_up_sync(0xffffffffu, incl, off);
-    if (lane >= off) incl += o;
-  }
-  if (lane == 31) warp_sums[warp] = incl;
-  __syncthreads();
-  int base = 0, total = 0;
-  for (int w = 0; w < 8; ++w) {
-    if (w < warp) base += warp_sums[w];
-    total += warp_sums[w];
-  }
-  const int tile0 = base + incl - ntiles;  // tiles before this expert
-  for (int wt = 0; wt < wt1; ++wt)
-    for (int j = 0; j < ntiles; ++j)
-      items1[static_cast<size_t>(tile0) * wt1 + wt * ntiles + j] =
-          make_int4(e, wt, row0 + j * tsz, min(tsz, n - j * tsz));
-  for (int wt = 0; wt < wt2; ++wt)
-    for (int j = 0; j < ntiles; ++j)
-      items2[static_cast<size_t>(tile0) * wt2 + wt * ntiles + j] =
-          make_int4(e, wt, row0 + j * tsz, min(tsz, n - j * tsz));
-  if (threadIdx.x == 0) {
-    n_items[0] = total * wt1;
-    n_items[1] = total * wt2;
-  }
+  build_work_items(offsets, E, s, status, warp_sums);
 }
 
 // ------------------------------------------------------------------ host side
@@ -781,18 +737,35 @@ ExpertPlan plan_experts(int T, int d, int E, int top_k, int inter, bool decoded)
   return p;
 }
 
+ScheduleArgs schedule_args(const ExpertPlan& plan, const ExpertBuffers& buf, int R) {
+  ScheduleArgs s;
+  s.n_max = plan.n_max;
+  s.wt1 = plan.wtiles1;
+  s.wt2 = plan.wtiles2;
+  s.R = R;
+  s.items1 = buf.items1;
+  s.items2 = buf.items2;
+  s.n_items = buf.n_items;
+  s.cap1 = plan.max_items1;
+  s.cap2 = plan.max_items2;
+  return s;
+}
+
 cudaError_t launch_expert_ffn(const ExpertPlan& plan, const ExpertBuffers& buf, const ExpertWeightsDev& w, int T,
                               int d, int E, int top_k, int inter, int num_sms, long long wait_spins,
-                              cudaStream_t stream, int* cu_error, cudaEvent_t after_gemm1) {
+                              cudaStream_t stream, int* cu_error, cudaEvent_t after_gemm1, bool items_ready) {
   *cu_error = 0;
   const int R = T * top_k;
   const int fmt = w.wfmt;
   if (fmt != MOE_W_BF16 && fmt != MOE_W_NVFP4 && fmt != MOE_W_FP8) return cudaErrorInvalidValue;
   if (fmt == MOE_W_NVFP4 && ((d % 256) || (inter % 256))) return cudaErrorNotSupported;
   if (fmt == MOE_W_FP8 && ((d % 128) || (inter % 128))) return cudaErrorNotSupported;
-  cudaError_t err = launch_pdl(schedule_kernel, dim3(1), dim3(256), 0, stream, buf.offsets, E, R, plan.n_max,
-                               plan.wtiles1, plan.wtiles2, buf.items1, buf.items2, buf.n_items, buf.status);
-  if (err != cudaSuccess) return err;
+  cudaError_t err = cudaSuccess;
+  if (!items_ready) {  // otherwise the permutation's plan kernel built them
+    err = launch_pdl(schedule_kernel, dim3(1), dim3(256), 0, stream, buf.offsets, E, schedule_args(plan, buf, R),
+                     buf.status);
+    if (err != cudaSuccess) return err;
+  }
 
   CUtensorMap tg, tu, td, tx[3], th[3];
   int rc = 0;
@@ -824,6 +797,7 @@ cudaError_t launch_expert_ffn(const ExpertPlan& plan, const ExpertBuffers& buf, 
   a1.K = d;
   a1.Nw = inter;
   a1.E = E;
+  a1.R = R;
   a1.h_out = buf.h;
   a1.status = buf.status;
   a1.timeout_where = buf.timeout_where;
@@ -849,6 +823,7 @@ cudaError_t launch_expert_ffn(const ExpertPlan& plan, const ExpertBuffers& buf, 
   a2.K = inter;
   a2.Nw = d;
   a2.E = E;
+  a2.R = R;
   a2.y_out = buf.y;
   a2.y_f32 = buf.y_f32;
   a2.status = buf.status;

@@ -7,6 +7,8 @@
 
 namespace beammoe {
 
+struct ScheduleArgs;  // schedule.cuh
+
 // ---- router (router.cu) ----
 // Split-K factor of the router logits GEMM for a batch of T tokens.
 int router_splits(int T, int d, int E, int num_sms);
@@ -43,12 +45,16 @@ cudaError_t launch_router_tc(const uint16_t* x, const float* w_r, void* scratch,
 // ---- permutation (permute.cu) ----
 int bitmap_words(int T);
 size_t bitmap_bytes(int T, int E);
-// bitmap_zeroed: the caller has already cleared the bitmap on `stream` (otherwise a memset is
-// enqueued first).
+// Small batches (the bitmap fits in one CTA's shared memory) take one plan kernel for the
+// bitmap, prefixes, counts and offsets; it needs no cleared bitmap, and given `sched` it also
+// builds the expert GEMMs' work items.
+bool permute_uses_plan_kernel(int T, int E);
+// bitmap_zeroed: the caller has already cleared the bitmap on `stream` (otherwise, unless the
+// plan kernel runs, a memset is enqueued first).
 cudaError_t launch_permute(const uint16_t* x, const int32_t* topk_idx, int T, int d, int E, int top_k,
                            uint32_t* bitmap, int32_t* word_prefix, int32_t* counts, int32_t* offsets,
                            int32_t* row_token, int32_t* inv_row, uint16_t* x_perm, int32_t* status,
-                           cudaStream_t stream, bool bitmap_zeroed = false);
+                           cudaStream_t stream, bool bitmap_zeroed = false, const ScheduleArgs* sched = nullptr);
 
 // ---- expert FFN (expert_gemm.cu) ----
 struct ExpertPlan {
@@ -81,9 +87,13 @@ struct ExpertWeightsDev {
   const float *gate_ts, *up_ts, *down_ts;
 };
 
+// items_ready: the work items were already built on the stream (by the permutation's plan
+// kernel, from the same plan and buffers); otherwise a schedule kernel builds them first.
 cudaError_t launch_expert_ffn(const ExpertPlan& plan, const ExpertBuffers& buf, const ExpertWeightsDev& w, int T,
                               int d, int E, int top_k, int inter, int num_sms, long long wait_spins,
-                              cudaStream_t stream, int* cu_error, cudaEvent_t after_gemm1 = nullptr);
+                              cudaStream_t stream, int* cu_error, cudaEvent_t after_gemm1 = nullptr,
+                              bool items_ready = false);
+ScheduleArgs schedule_args(const ExpertPlan& plan, const ExpertBuffers& buf, int R);
 
 // ---- pre-norm (norm.cu) ----
 // x [T][d] = bf16(RMSNorm(h) * gain), FP32; d a multiple of 64; x must not overlap h.

@@ -671,7 +671,7 @@ constexpr int kFlagSplits = kRouterFlagSplits;  // hidden-dimension parts per to
 int flag_splits(int d) { return d % (kFlagSplits * kFlagRows) == 0 ? kFlagSplits : kFlagSplits / 2; }
 
 __global__ void __launch_bounds__(kFlagThreads) router_flagged_logits_kernel(
-    const uint16_t* __restrict__ x, const float* __restrict__ wr, int d, int E,
+    const uint16_t* __restrict__ x, const float* __restrict__ wr, int T, int d, int E,
     const int32_t* __restrict__ flagged, const int32_t* __restrict__ flagged_count, float* __restrict__ part_out,
     int splits, int32_t* status, int32_t* timeout_where, long long wait_spins) {
   extern __shared__ __align__(16) uint8_t fsm[];
@@ -684,7 +684,7 @@ __global__ void __launch_bounds__(kFlagThreads) router_flagged_logits_kernel(
   pdl_launch_dependents();
   pdl_wait();
   const int n = *flagged_count;
-  if (n == 0) return;
+  if (n == 0 || !dcheck(n <= T, status)) return;
   const int groups = (n + kFlagTokens - 1) / kFlagTokens;
   const int e = threadIdx.x & 255, q = threadIdx.x >> 8;
   const uint32_t chunk_bytes = static_cast<uint32_t>(kFlagRows) * E * sizeof(float);
@@ -706,7 +706,9 @@ __global__ void __launch_bounds__(kFlagThreads) router_flagged_logits_kernel(
       float v[kFlagTokens];
 #pragma unroll
       for (int j = 0; j < kFlagTokens; ++j)
-        v[j] = (j < nt) ? bf16_bits_to_float(x[static_cast<size_t>(flagged[i0 + j]) * d + k0 + k]) : 0.f;
+        v[j] = (j < nt && dcheck(flagged[i0 + j] >= 0 && flagged[i0 + j] < T, status))
+                   ? bf16_bits_to_float(x[static_cast<size_t>(flagged[i0 + j]) * d + k0 + k])
+                   : 0.f;
       xs4[k] = make_float4(v[0], v[1], v[2], v[3]);
     }
     if (threadIdx.x == 0) {
@@ -776,7 +778,8 @@ __global__ void __launch_bounds__(kFlagThreads) router_flagged_logits_kernel(
 
 // One warp per flagged token: the parts' partial logits summed in order,
 // sigmoid and the full selection.
-__global__ void __launch_bounds__(256) router_flagged_select_kernel(const float* __restrict__ part, int splits, int E,
+__global__ void __launch_bounds__(256) router_flagged_select_kernel(const float* __restrict__ part, int splits, int T,
+                                                                   int E,
                                                                    int G,
                                                                    int Gk, int K, float scale,
                                                                    const float* __restrict__ bias,
@@ -787,6 +790,7 @@ __global__ void __launch_bounds__(256) router_flagged_select_kernel(const float*
   pdl_launch_dependents();
   pdl_wait();
   const int n = *flagged_count;
+  if (!dcheck(n <= T, status)) return;
   const int lane = threadIdx.x & 31;
   for (int i = blockIdx.x * 8 + (threadIdx.x >> 5); i < n; i += gridDim.x * 8) {
     float sv[kMaxPerLane];
@@ -800,6 +804,7 @@ __global__ void __launch_bounds__(256) router_flagged_select_kernel(const float*
         sv[j] = 1.0f / (1.0f + expf(-l));
       }
     }
+    if (!dcheck(flagged[i] >= 0 && flagged[i] < T, status)) continue;
     warp_select(sv, bias, lane, flagged[i], E, G, Gk, K, scale, topk_idx, topk_w, status);
   }
 }
@@ -898,11 +903,14 @@ TcScratch tc_scratch(void* base, int T, int d, int E) {
 
 size_t router_tc_scratch_bytes(int T, int d, int E) { return tc_scratch(nullptr, T, d, E).bytes; }
 
-// Tensor-core accumulation error constant of the flag bound (kappa): the
-// largest measured |logit error| / (2^-23 sqrt(d/16) |x_t| |W_r[:, e]|) over
-// Beam-shape inputs (normal, outlier channels, router columns aligned with
-// the tokens, scaled by powers of two) times a safety factor.
-constexpr float kTcErrKappa = 0.25f;
+// Tensor-core accumulation error constant of the flag bound (kappa). Measured
+// |logit error| / (2^-23 sqrt(d/16) |x_t| |W_r[:, e]|), maximum over a million
+// logits per input: 0.047-0.057 for normal activations and router weights
+// (also scaled by 3 and 0.7, with 1 % outlier channels at 20x, heavy-tailed,
+// and the skewed workload), 0.067 at d = 256, and 0.096 with router columns
+// strongly aligned with the tokens (logits up to 12.5, partial sums near
+// their Cauchy-Schwarz bound). kappa keeps a factor of 3 above the worst.
+constexpr float kTcErrKappa = 0.3f;
 
 cudaError_t launch_router_tc(const uint16_t* x, const float* w_r, void* scratch, float* part, int32_t* flagged_count,
                              int32_t* hdr_ticket, int T, int d, int E, int n_groups, int topk_groups, int top_k,
@@ -952,10 +960,10 @@ cudaError_t launch_router_tc(const uint16_t* x, const float* w_r, void* scratch,
   err = cudaFuncSetAttribute(router_flagged_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(xs_bytes));
   if (err != cudaSuccess) return err;
-  err = launch_pdl(router_flagged_logits_kernel, dim3(num_sms), dim3(kFlagThreads), xs_bytes, stream, x, w_r, d, E,
-                   sc.flagged, flagged_count, part, fsplits, status, timeout_where, wait_spins);
+  err = launch_pdl(router_flagged_logits_kernel, dim3(num_sms), dim3(kFlagThreads), xs_bytes, stream, x, w_r, T, d,
+                   E, sc.flagged, flagged_count, part, fsplits, status, timeout_where, wait_spins);
   if (err != cudaSuccess) return err;
-  return launch_pdl(router_flagged_select_kernel, dim3(num_sms), dim3(256), 0, stream, part, fsplits, E, n_groups,
+  return launch_pdl(router_flagged_select_kernel, dim3(num_sms), dim3(256), 0, stream, part, fsplits, T, E, n_groups,
                     topk_groups, top_k, routed_scale, sel_bias, sc.flagged, flagged_count, topk_idx, topk_w, status);
 }
 

@@ -41,6 +41,14 @@ def test_library_exports_every_declared_symbol(lib):
     assert "sm_103a" in bm.moe_version()
 
 
+def test_debug_build_exports_every_declared_symbol():
+    """The bounds-checked build (BEAMMOE_LIBRARY=debug) is the same library with extra checks."""
+    path = build(debug=True)
+    dbg = ctypes.CDLL(path)
+    for name in declared_functions():
+        assert hasattr(dbg, name), f"{name} not exported by the debug build"
+
+
 def _dims(**kw):
     base = dict(T=64, d=5120, E=256, n_groups=8, topk_groups=4, top_k=8, inter=2560, routed_scale=2.5, wfmt=0)
     base.update(kw)
@@ -52,8 +60,8 @@ def test_workspace_bytes(lib):
     n4k = lib.moe_workspace_bytes(ctypes.byref(_dims(T=4096)))
     assert 0 < n64 < n4k
     R = 4096 * 8
-    # x_perm + h + y (all bf16) dominate: R*(2d + 2I + 2d) bytes
-    assert n4k >= R * (2 * 5120 + 2 * 2560 + 2 * 5120)
+    # x_perm (bf16) + h (bf16) + y (fp32) dominate: R*(2d + 2I + 4d) bytes
+    assert n4k >= R * (2 * 5120 + 2 * 2560 + 4 * 5120)
     assert lib.moe_workspace_bytes(ctypes.byref(_dims(T=0))) > 0
 
 

@@ -93,7 +93,9 @@ def test_router_split_rule():
     assert bench.router_splits(4096, 5120, 256, 148) == 2
     assert bench.router_splits(32768, 5120, 256, 148) == 1
     assert bench.kernels_per_step(W.CONFIGS["skewed"], 148) == 13   # tensor-core router: 5 kernels
-    assert bench.kernels_per_step(W.CONFIGS["decode"], 148) == 11   # SIMT logits + reduce + select
+    # SIMT logits + reduce + select; plan kernel (with the GEMM schedule) + gather; GEMM1, GEMM2, combine
+    assert bench.kernels_per_step(W.CONFIGS["decode"], 148) == 8
+    assert bench.permute_uses_plan_kernel(1024, 256) and not bench.permute_uses_plan_kernel(1025, 256)
 
 
 def test_stage_roofline_arithmetic():
@@ -140,3 +142,30 @@ def test_cpu_baseline_parity_report():
     assert t == 0
     rec2 = bench.cpu_baseline(cfg, A(), inp["x"], inp["w_r"], inp, n_tok=16, gpu=(bad, bits))
     assert rec2["parity"]["routing_mismatches"] == 1 and not rec2["parity"]["ok"]
+
+
+def test_record_traffic_from_ncu_csv(tmp_path):
+    """bench.py --record-traffic: ncu's CSV launch list and the plain bench line of a small case
+    become the DRAM-traffic record the roofline's `traffic` reads (scaled by algorithmic bytes)."""
+    import json
+    hdr = '"ID","Process ID","Process Name","Host Name","Kernel Name","Context","Stream","Block Size",' \
+          '"Grid Size","Device","CC","Section Name","Metric Name","Metric Unit","Metric Value"'
+    rows = []
+    for i, (name, rd, wr, t) in enumerate([("expert_gemm_kernel<1, 1>(CUtensorMap_st)", "525.5", "17.8", "285.3"),
+                                           ("expert_gemm_kernel<0, 1>(CUtensorMap_st)", "257.6", "27.4", "142.2")]):
+        for m, u, v in (("dram__bytes_read.sum", "Mbyte", rd), ("dram__bytes_write.sum", "Mbyte", wr),
+                        ("gpu__time_duration.sum", "usecond", t)):
+            rows.append(f'"{i}","1","python","h","{name}","1","7","(576, 1, 1)","(148, 1, 1)","0","10.3","",'
+                        f'"{m}","{u}","{v}"')
+    (tmp_path / "profile_nvfp4.csv").write_text("==PROF== note\n" + hdr + "\n" + "\n".join(rows) + "\n")
+    (tmp_path / "profile_nvfp4.json").write_text(json.dumps({"layer_roofline": {"experts_touched": 32}}) + "\n")
+    out = bench.record_traffic(str(tmp_path), out=str(tmp_path / "traffic.json"))
+    rec = json.load(open(out))
+    assert rec["capture_for_workload"]["nvfp4"] == "profile_nvfp4"
+    k = rec["captures"]["profile_nvfp4"]["kernels"]
+    assert k["expert_gemm_kernel<GLU, NVFP4>"]["dram_bytes_read"] == 525_500_000
+    assert k["expert_gemm_kernel<plain, NVFP4>"]["gpu_time_ns_serialised"] == 142_200
+    g1, _, _ = bench.roofline_numbers(W.CONFIGS["nvfp4"].__class__(**{**W.CONFIGS["nvfp4"].__dict__, "name": "x",
+                                                                      "T": 512, "E": 32, "n_groups": 8}), 32,
+                                      {"hbm_gbs": 6497.4, "bf16_tflops": 1811.4})
+    assert k["expert_gemm_kernel<GLU, NVFP4>"]["algorithmic_bytes"] == int(g1["bytes"])
