@@ -38,19 +38,14 @@ import workload as W  # noqa: E402  (seeded input generators only)
 METRIC = "MoE-layer tokens/s at Beam shape (T=64 decode, T=4096 prefill); % of roofline"
 
 
-def router_splits(T, d, E, num_sms):
-    """The library's split of the router's hidden dimension (same rule as router.cu)."""
-    tiles = -(-T // 64) * -(-E // 128)
-    target = -(-num_sms // tiles)
-    chunks = d // 32
-    best = 1
-    for s in range(1, chunks + 1):
-        if chunks % s or d // s < 64:
-            continue
-        best = s
-        if s >= target:
-            break
-    return best
+ROUTE_TICKETS = 192  # groups of 8 tokens whose selection the SIMT logits kernel can run itself
+
+
+def simt_router_kernels(T, E):
+    """Kernels of the library's SIMT router (router.cu): the logits kernel (which also selects
+    while ceil(T/64) * 8 <= ROUTE_TICKETS), a selection kernel otherwise, and a W_r padding copy
+    when E is not a multiple of 4."""
+    return 1 + (0 if -(-T // 64) * 8 <= ROUTE_TICKETS else 1) + (1 if E % 4 else 0)
 
 
 ROUTER_TC_MIN_TOKENS = 1024  # the library routes batches this large on the tensor cores
@@ -64,14 +59,14 @@ def permute_uses_plan_kernel(T, E):
 
 def kernels_per_step(cfg, num_sms):
     """Kernels one moe_forward launches: router (tensor-core: W_r split, tensor-core logits,
-    selection, narrow-margin recompute (logits + selection); SIMT: logits [+ split reduce] +
-    select), permutation (small batches: plan kernel, which also builds the GEMM work items, +
+    selection, narrow-margin recompute (logits + selection); SIMT: logits with the selection,
+    see simt_router_kernels), permutation (small batches: plan kernel, which also builds the GEMM work items, +
     gather; otherwise bitmap, column scan, offsets, gather + the GEMMs' schedule kernel),
     GEMM1, GEMM2, combine."""
     if cfg.T >= ROUTER_TC_MIN_TOKENS:
         router = 5
     else:
-        router = 2 + (1 if router_splits(cfg.T, cfg.d, cfg.E, num_sms) > 1 else 0)
+        router = simt_router_kernels(cfg.T, cfg.E)
     permute_and_schedule = 2 if permute_uses_plan_kernel(cfg.T, cfg.E) else 5
     return router + permute_and_schedule + 2 + 1
 

@@ -54,16 +54,14 @@ constexpr int kMaxSmsForLayout = 1024;
 Layout make_layout(const moe_dims_t& d) {
   const int64_t T = d.T, R = T * d.top_k;
   const int Tc = d.T > 0 ? d.T : 1;
-  const int splits = std::max(router_splits(Tc, d.d, d.E, kMaxSmsForLayout),
-                              router_uses_tensor_cores(d.T, d.E, d.d)
-                                  ? std::max(kRouterFlagSplits, router_tc_splits(Tc, d.d, kMaxSmsForLayout))
-                                  : 1);
+  const bool tc = router_uses_tensor_cores(d.T, d.E, d.d);
+  const int splits = tc ? std::max(kRouterFlagSplits, router_tc_splits(Tc, d.d, kMaxSmsForLayout)) : 1;
   const ExpertPlan pl = plan_experts(d.T, d.d, d.E, d.top_k, d.inter, d.wfmt != MOE_W_BF16);
   const int64_t nw = bitmap_words(d.T);
   size_t sz[R_NUM];
   sz[R_HDR] = sizeof(WsHeader);
   sz[R_PART] = sizeof(float) * static_cast<size_t>(splits) * T * d.E;
-  sz[R_WSPLIT] = router_uses_tensor_cores(d.T, d.E, d.d) ? router_tc_scratch_bytes(d.T, d.d, d.E) : 0;
+  sz[R_WSPLIT] = tc ? router_tc_scratch_bytes(d.T, d.d, d.E) : router_simt_scratch_bytes(d.d, d.E);
   sz[R_BITMAP] = sizeof(uint32_t) * static_cast<size_t>(d.E) * nw;
   sz[R_WPRE] = sizeof(int32_t) * static_cast<size_t>(d.E) * nw;
   sz[R_COUNTS] = sizeof(int32_t) * d.E;
@@ -152,13 +150,11 @@ moe_status_t do_route(const moe_dims_t* d, const uint16_t* x, const float* w_r, 
                                         d->topk_groups, d->top_k, d->routed_scale, sel_bias, idx, w, &hdr->status,
                                         &hdr->timeout_where, g_wait_spins, num_sms(), s));
   }
-  const int splits = router_splits(d->T, d->d, d->E, num_sms());
-  float* part = region<float>(ws, L, R_PART);
-  cudaError_t e = launch_router_logits(x, w_r, part, d->T, d->d, d->E, splits, s);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
-  e = launch_router_select(part, splits, d->T, d->E, d->n_groups, d->topk_groups, d->top_k, d->routed_scale,
-                           sel_bias, idx, w, status_word(ws), s);
-  return cuda_status(e);
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+  return cuda_status(launch_router_simt(x, w_r, region<uint8_t>(ws, L, R_WSPLIT), region<float>(ws, L, R_PART),
+                                        hdr->route_ticket, d->T, d->d, d->E, d->n_groups, d->topk_groups, d->top_k,
+                                        d->routed_scale, sel_bias, idx, w, &hdr->status, &hdr->timeout_where,
+                                        g_wait_spins, num_sms(), s));
 }
 
 moe_status_t do_permute(const moe_dims_t* d, const uint16_t* x, const int32_t* idx, int32_t* counts,

@@ -13,16 +13,18 @@
 
 namespace beammoe {
 
-// Workspace header: first 256 bytes of every workspace.
+// Workspace header: first 1024 bytes of every workspace (zeroed once by
+// moe_workspace_init; the ticket arrays return to zero at the end of every call).
 struct WsHeader {
   int32_t status;        // first moe_device_code_t latched by any kernel
   int32_t timeout_where; // role id of the first wait that expired (diagnostics)
   int32_t n_items[2];    // expert-GEMM work items (GEMM1, GEMM2) built on the device
   int32_t router_flagged; // tokens the tensor-core router recomputed in fp32 (last call)
   int32_t wn_ticket[8];   // tensor-core router: blocks done per 32-expert strip of W_r (back to 0 after each call)
+  int32_t route_ticket[192];  // SIMT router: CTAs done per group of 8 tokens (kRouteTickets; back to 0 after each call)
   int32_t pad[51];
 };
-static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+static_assert(sizeof(WsHeader) == 1024, "header is 1024 bytes");
 
 __device__ __forceinline__ void latch_status(int32_t* status, int32_t code) {
   if (status) atomicCAS(status, 0, code);
@@ -119,6 +121,16 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 }
 
 // ------------------------------------------------------------------ TMA
+// Orders this thread's generic-proxy shared-memory accesses before later
+// async-proxy (TMA, bulk copy) accesses made after a barrier or mbarrier hand-
+// over. A stage that threads read with ordinary loads is refilled by TMA only
+// after every reader has executed this fence and then released the stage:
+// without it the refill can overwrite the stage under reads still in flight
+// (seen as wrong partial sums with two CTAs per SM).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 
 // 2-D tiled bulk tensor load global -> shared, completion counted in bytes on
 // `bar`. c0 is the innermost (contiguous) coordinate in elements.

@@ -563,6 +563,7 @@ __global__ void __launch_bounds__(threads_for(kFmt), 1)
           tmem_st_32x32b_x16(t_lane + static_cast<uint32_t>(cstage * kConvCols + hk * 16), v);
         }
         tmem_st_wait();
+        fence_proxy_async_smem();  // the packed tile's reads complete before TMA may refill the stage
         tc_fence_before();
         mbar_arrive(&conv_bar[cstage]);
         if (++cstage == p.conv_stages) {

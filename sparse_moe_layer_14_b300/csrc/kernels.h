@@ -10,17 +10,22 @@ namespace beammoe {
 struct ScheduleArgs;  // schedule.cuh
 
 // ---- router (router.cu) ----
-// Split-K factor of the router logits GEMM for a batch of T tokens.
-int router_splits(int T, int d, int E, int num_sms);
-// partial[s][t][e] = sum over k in split s of x[t][k] * w_r[k][e]  (fp32)
-cudaError_t launch_router_logits(const uint16_t* x, const float* w_r, float* partial, int T, int d, int E,
-                                 int splits, cudaStream_t stream);
-// sums the split partials (in place into split 0), then sigmoid scores,
-// group-limited top-k (on scores + sel_bias when sel_bias [E] is given) and
-// normalised weights (unbiased scores).
-cudaError_t launch_router_select(float* partial, int splits, int T, int E, int n_groups, int topk_groups,
-                                 int top_k, float routed_scale, const float* sel_bias, int32_t* topk_idx,
-                                 float* topk_w, int32_t* status, cudaStream_t stream);
+// FP32 SIMT router for small batches: logits[T][E] = x . W_r (a fixed-order
+// split over the hidden dimension inside thread-block clusters), then sigmoid
+// scores, group-limited top-k (on scores + sel_bias when sel_bias [E] is
+// given) and normalised weights (unbiased scores). With
+// router_simt_selects(T) the logits kernel selects too, counting finished CTAs
+// in `ticket` (kRouteTickets ints, zero before the first call; the kernel
+// returns them to zero); otherwise a selection kernel follows. `scratch` holds
+// router_simt_scratch_bytes(d, E) bytes (a W_r copy with rows padded to a
+// multiple of 4 experts when E is not one).
+constexpr int kRouteTickets = 192;
+bool router_simt_selects(int T);
+size_t router_simt_scratch_bytes(int d, int E);
+cudaError_t launch_router_simt(const uint16_t* x, const float* w_r, void* scratch, float* logits, int32_t* ticket,
+                               int T, int d, int E, int n_groups, int topk_groups, int top_k, float routed_scale,
+                               const float* sel_bias, int32_t* topk_idx, float* topk_w, int32_t* status,
+                               int32_t* timeout_where, long long wait_spins, int num_sms, cudaStream_t stream);
 
 // Tensor-core router for large batches (T >= kRouterTcMinTokens): W_r split
 // into three bf16 terms, partial logits on the tensor cores, a warp-per-token

@@ -38,284 +38,151 @@
 //                        full warp selection.
 #include <algorithm>
 
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "kernels.h"
 
 namespace beammoe {
 
+namespace cg = cooperative_groups;
+
 namespace {
 
-constexpr int RT = 64;   // tokens per block
-constexpr int RE = 128;  // experts per block
-constexpr int RK = 32;   // hidden elements per smem stage
-
-__global__ void __launch_bounds__(256) router_logits_kernel(const uint16_t* __restrict__ x,
-                                                            const float* __restrict__ wr,
-                                                            float* __restrict__ part, int T, int d, int E,
-                                                            int k_per_split) {
-  __shared__ __align__(16) float xs[RK][RT + 4];  // xs[k][t]
-  __shared__ __align__(16) float ws[RK][RE];      // ws[k][e]
-  pdl_launch_dependents();
-  pdl_wait();
-  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-  const int e0 = blockIdx.x * RE, t0 = blockIdx.y * RT;
-  const int kbeg = blockIdx.z * k_per_split, kend = kbeg + k_per_split;
-  const bool vec_w = (E & 3) == 0;
-  float acc[4][8];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
-
-  for (int k0 = kbeg; k0 < kend; k0 += RK) {
-    {
-      const int r = tid >> 2, kc = (tid & 3) * 8, t = t0 + r;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (t < T) v = *reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * d + k0 + kc);
-      const uint16_t* h = reinterpret_cast<const uint16_t*>(&v);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) xs[kc + i][r] = bf16_bits_to_float(h[i]);
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int q = tid + 256 * i, kk = q >> 5, ec = (q & 31) * 4, e = e0 + ec;
-      const float* src = wr + static_cast<size_t>(k0 + kk) * E + e;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (vec_w && e + 3 < E) {
-        v = *reinterpret_cast<const float4*>(src);
-      } else {
-        if (e + 0 < E) v.x = src[0];
-        if (e + 1 < E) v.y = src[1];
-        if (e + 2 < E) v.z = src[2];
-        if (e + 3 < E) v.w = src[3];
-      }
-      *reinterpret_cast<float4*>(&ws[kk][ec]) = v;
-    }
-    __syncthreads();
-#pragma unroll 8
-    for (int kk = 0; kk < RK; ++kk) {
-      const float4 a = *reinterpret_cast<const float4*>(&xs[kk][ty * 4]);
-      const float4 b0 = *reinterpret_cast<const float4*>(&ws[kk][tx * 8]);
-      const float4 b1 = *reinterpret_cast<const float4*>(&ws[kk][tx * 8 + 4]);
-      const float av[4] = {a.x, a.y, a.z, a.w};
-      const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
-    }
-    __syncthreads();
-  }
-  float* dst = part + static_cast<size_t>(blockIdx.z) * T * E;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int t = t0 + ty * 4 + i;
-    if (t >= T) continue;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int e = e0 + tx * 8 + j;
-      if (e < E) dst[static_cast<size_t>(t) * E + e] = acc[i][j];
-    }
-  }
+// Selection keys: an order-preserving map of a float score to an unsigned
+// integer (a larger score gives a larger key; -0 and +0 share a key), so the
+// warp finds a maximum with one redux.sync instead of a shuffle tree. Key 0
+// is below every number's key and marks "no candidate" (experts outside the
+// kept groups, taken ones, padding); a NaN score also maps to 0 and is never
+// chosen.
+__device__ __forceinline__ uint32_t score_key(float v) {
+  uint32_t b = __float_as_uint(v);
+  if (v != v) return 0u;
+  if (b == 0x80000000u) b = 0u;
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
-// part[0][t][e] = sum over s of part[s][t][e] in a fixed order: four chains
-// over s = 0,4,8,.. / 1,5,.. / 2,6,.. / 3,7,.. (independent loads in flight),
-// then (c0 + c1) + (c2 + c3).
-__global__ void __launch_bounds__(256) split_reduce_kernel(float* __restrict__ part, int splits, int64_t n) {
-  pdl_launch_dependents();
-  pdl_wait();
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= n) return;
-  float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
-  int sp = 0;
-  for (; sp + 4 <= splits; sp += 4) {
-    c0 += part[static_cast<size_t>(sp) * n + i];
-    c1 += part[static_cast<size_t>(sp + 1) * n + i];
-    c2 += part[static_cast<size_t>(sp + 2) * n + i];
-    c3 += part[static_cast<size_t>(sp + 3) * n + i];
-  }
-  for (; sp < splits; ++sp) c0 += part[static_cast<size_t>(sp) * n + i];
-  part[i] = (c0 + c1) + (c2 + c3);
-}
-
-// (value, index) order of the selection: larger value first, ties to the
-// lower index.
-__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
-  return v > bv || (v == bv && i < bi);
-}
-
-__device__ __forceinline__ void warp_argmax(float& v, int& i) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    const float ov = __shfl_xor_sync(0xffffffffu, v, off);
-    const int oi = __shfl_xor_sync(0xffffffffu, i, off);
-    if (better(ov, oi, v, i)) {
-      v = ov;
-      i = oi;
-    }
-  }
+__device__ __forceinline__ float key_score(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
 constexpr int kMaxPerLane = 8;  // E <= 256
+constexpr uint32_t kFull = 0xffffffffu;
 
 // Group-limited selection of one token by one warp. Lane l holds the scores
-// of experts l, l+32, l+64, ... in s[]; `bias` ([E] fp32, nullable) is the
-// per-expert selection bias of DeepSeek-V3-style balancing: groups and
-// experts are chosen on s + bias, the weights use s. Writes the token's K
-// expert ids (slot order: descending selection score, ties to the lower id)
-// and weights. Returns, in every lane, the decision margins (on selection
+// of experts l, l+32, l+64, ... in s_in[] (entries of experts >= E are
+// ignored); `bias` ([E] fp32, nullable) is the per-expert selection bias of
+// DeepSeek-V3-style balancing: groups and experts are chosen on s + bias, the
+// weights use s. Every choice takes the larger selection score, ties to the
+// lower index. Writes the token's K expert ids (slot order: descending
+// selection score) and weights scale * s_e / sum of the chosen s (summed in
+// slot order). Returns, in every lane, the decision margins (on selection
 // scores): x = worst kept group score - best dropped one; y = the smaller of
 // (worst chosen score - best unchosen candidate) and the gaps between
-// consecutive slots.
+// consecutive slots (1 where there is nothing to compare).
 __device__ float2 warp_select(const float (&s_in)[kMaxPerLane], const float* __restrict__ bias, int lane, int t,
                               int E, int G, int Gk, int K, float scale, int32_t* __restrict__ topk_idx,
                               float* __restrict__ topk_w, int32_t* status) {
   const int gsz = E / G;
-  constexpr float kMasked = -1.0f;  // below every sigmoid score
-  float s[kMaxPerLane];             // selection scores
+  uint32_t sk[kMaxPerLane];  // selection keys
+  int grp[kMaxPerLane];      // group of each of this lane's experts (32 = none)
 #pragma unroll
   for (int i = 0; i < kMaxPerLane; ++i) {
     const int e = lane + 32 * i;
-    s[i] = (bias && e < E) ? s_in[i] + bias[e] : s_in[i];
-  }
-  int grp[kMaxPerLane];             // group of each of this lane's experts (E = none)
-#pragma unroll
-  for (int i = 0; i < kMaxPerLane; ++i) {
-    const int e = lane + 32 * i;
-    grp[i] = (e < E) ? e / gsz : 64;
+    sk[i] = (e < E) ? score_key(bias ? s_in[i] + bias[e] : s_in[i]) : 0u;
+    grp[i] = (e < E) ? e / gsz : 32;
   }
 
-  // group score: sum of the two largest scores of the group (lane g keeps group g's)
-  float my_gs = kMasked;
-  if (gsz == 32) {
-    // element i of every lane is group i: all groups reduce side by side
-    float m1[kMaxPerLane], m2[kMaxPerLane];
-#pragma unroll
-    for (int i = 0; i < kMaxPerLane; ++i) {
-      m1[i] = s[i];
-      m2[i] = kMasked;
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-#pragma unroll
-      for (int i = 0; i < kMaxPerLane; ++i) {
-        const float o1 = __shfl_xor_sync(0xffffffffu, m1[i], off);
-        const float o2 = __shfl_xor_sync(0xffffffffu, m2[i], off);
-        if (o1 > m1[i]) {
-          m2[i] = fmaxf(m1[i], o2);
-          m1[i] = o1;
-        } else {
-          m2[i] = fmaxf(m2[i], o1);
-        }
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < kMaxPerLane; ++i)
-      if (lane == i && i < G) my_gs = m1[i] + m2[i];
-  }
-  for (int g = 0; g < G && gsz != 32; ++g) {
-    float m1 = kMasked, m2 = kMasked;
+  // group score = sum of the group's two largest selection scores (the largest
+  // alone for one-expert groups); lane g keeps group g's
+  float my_gs = 0.f;
+#pragma unroll 4
+  for (int g = 0; g < G; ++g) {
+    uint32_t k1 = 0u, k2 = 0u;  // this lane's two largest keys in group g
 #pragma unroll
     for (int i = 0; i < kMaxPerLane; ++i) {
       if (grp[i] == g) {
-        if (s[i] > m1) {
-          m2 = m1;
-          m1 = s[i];
-        } else if (s[i] > m2) {
-          m2 = s[i];
+        const uint32_t k = sk[i];
+        k2 = max(k2, min(k1, k));
+        k1 = max(k1, k);
+      }
+    }
+    const uint32_t m1 = __reduce_max_sync(kFull, k1);
+    const int first = __ffs(__ballot_sync(kFull, k1 == m1)) - 1;  // a lane holding the largest
+    const uint32_t m2 = __reduce_max_sync(kFull, lane == first ? k2 : k1);
+    if (lane == g) my_gs = gsz >= 2 ? key_score(m1) + key_score(m2) : key_score(m1);
+  }
+
+  // keep the Gk best groups
+  const bool is_group = lane < G;
+  const uint32_t gkey = is_group ? score_key(my_gs) : 0u;
+  uint32_t kept = 0u;
+  uint32_t last_kept = 0u;
+  for (int r = 0; r < Gk; ++r) {
+    const bool cand = is_group && !((kept >> lane) & 1u);
+    const uint32_t m = __reduce_max_sync(kFull, cand ? gkey : 0u);
+    const uint32_t w = __reduce_min_sync(kFull, (cand && gkey == m) ? static_cast<uint32_t>(lane) : 32u);
+    if (w < 32u) kept |= 1u << w;
+    last_kept = m;
+  }
+  float margin_group = 1.0f;
+  if (Gk < G) {
+    const bool cand = is_group && !((kept >> lane) & 1u);
+    const uint32_t m = __reduce_max_sync(kFull, cand ? gkey : 0u);
+    if (m != 0u && last_kept != 0u) margin_group = key_score(last_kept) - key_score(m);
+  }
+
+  // choose the K best experts of the kept groups
+  uint32_t ck[kMaxPerLane];  // candidate keys (0 once taken or outside the kept groups)
+#pragma unroll
+  for (int i = 0; i < kMaxPerLane; ++i) ck[i] = (grp[i] < 32 && ((kept >> grp[i]) & 1u)) ? sk[i] : 0u;
+  float my_w = 0.f;  // slot `lane`: its unbiased score
+  int my_e = 0;      // ... and its expert
+  float sum = 0.f;   // of unbiased scores, in slot order
+  float prev = 0.f, gap = 1.0f;
+  for (int k = 0; k < K; ++k) {
+    uint32_t kb = 0u;
+#pragma unroll
+    for (int i = 0; i < kMaxPerLane; ++i) kb = max(kb, ck[i]);
+    uint32_t eb = 0xffffffffu;  // lowest expert of this lane holding kb
+#pragma unroll
+    for (int i = kMaxPerLane - 1; i >= 0; --i)
+      if (ck[i] == kb) eb = static_cast<uint32_t>(lane + 32 * i);
+    const uint32_t m = __reduce_max_sync(kFull, kb);
+    const uint32_t idx = __reduce_min_sync(kFull, (kb == m && m != 0u) ? eb : 0xffffffffu);
+    float u = 0.f, v = 0.f;
+    int e = 0;
+    if (m == 0u || idx >= static_cast<uint32_t>(E)) {  // fewer than K candidates (NaN scores)
+      latch_status(status, MOE_DEV_BAD_EXPERT);
+    } else {
+      e = static_cast<int>(idx);
+      v = key_score(m);
+      const int owner = e & 31, slot = e >> 5;
+      float mine = 0.f;
+#pragma unroll
+      for (int i = 0; i < kMaxPerLane; ++i) {
+        if (i == slot) {
+          mine = s_in[i];
+          if (lane == owner) ck[i] = 0u;
         }
       }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float o1 = __shfl_xor_sync(0xffffffffu, m1, off);
-      const float o2 = __shfl_xor_sync(0xffffffffu, m2, off);
-      if (o1 > m1) {
-        m2 = fmaxf(m1, o2);
-        m1 = o1;
-      } else {
-        m2 = fmaxf(m2, o1);
-      }
-    }
-    if (lane == g) my_gs = (gsz >= 2) ? (m1 + m2) : m1;
-  }
-
-  // keep the Gk best groups (ties to the lower group index)
-  uint32_t kept = 0;
-  float last_kept = 0.f;
-  for (int r = 0; r < Gk; ++r) {
-    float v = (lane < G && !((kept >> lane) & 1u)) ? my_gs : -2.0f;
-    int i = lane;
-    warp_argmax(v, i);
-    kept |= 1u << i;
-    last_kept = v;
-  }
-  float margin_group = 1.0f, margin = 1.0f;
-  {
-    float v = (lane < G && !((kept >> lane) & 1u)) ? my_gs : -2.0f;
-    int i = lane;
-    warp_argmax(v, i);
-    if (v > -1.5f) margin_group = last_kept - v;
-  }
-
-  // choose the K best experts of the kept groups (ties to the lower index)
-  uint32_t taken = 0;  // bit i: this lane's element i is chosen
-  float my_s = 0.f;    // slot `lane`: its selection score ...
-  float my_w = 0.f;    // ... and its unbiased score (the weight's)
-  int my_e = 0;
-  float sum = 0.f;     // of unbiased scores
-  for (int k = 0; k < K; ++k) {
-    float v = -2.0f;
-    int idx = 0x7fffffff;
-#pragma unroll
-    for (int i = 0; i < kMaxPerLane; ++i) {
-      const int e = lane + 32 * i;
-      if (grp[i] < 32 && ((kept >> grp[i]) & 1u) && !((taken >> i) & 1u) && better(s[i], e, v, idx)) {
-        v = s[i];
-        idx = e;
-      }
-    }
-    warp_argmax(v, idx);
-    float u = 0.f;  // the chosen expert's unbiased score, from the lane that holds it
-    if (idx >= E || idx < 0) {  // only possible with NaN scores
-      latch_status(status, MOE_DEV_BAD_EXPERT);
-      idx = 0;
-      v = 0.f;
-    } else {
-      if ((idx & 31) == lane) taken |= 1u << (idx >> 5);
-#pragma unroll
-      for (int i = 0; i < kMaxPerLane; ++i)
-        if (i == (idx >> 5)) u = s_in[i];
-      u = __shfl_sync(0xffffffffu, u, idx & 31);
+      u = __shfl_sync(kFull, mine, owner);
     }
     sum += u;
+    if (k > 0) gap = fminf(gap, prev - v);
+    prev = v;
     if (lane == k) {
-      my_s = v;
       my_w = u;
-      my_e = idx;
+      my_e = e;
     }
   }
+  float margin = gap;
   {
-    float v = -2.0f;
-    int idx = 0x7fffffff;
+    uint32_t kb = 0u;
 #pragma unroll
-    for (int i = 0; i < kMaxPerLane; ++i) {
-      const int e = lane + 32 * i;
-      if (grp[i] < 32 && ((kept >> grp[i]) & 1u) && !((taken >> i) & 1u) && better(s[i], e, v, idx)) {
-        v = s[i];
-        idx = e;
-      }
-    }
-    warp_argmax(v, idx);
-    const float last_s = __shfl_sync(0xffffffffu, my_s, K - 1);
-    if (v > -1.5f) margin = fminf(margin, last_s - v);
-    // gaps between consecutive slots: the slot order is a decision too
-    const float next_s = __shfl_down_sync(0xffffffffu, my_s, 1);
-    float gap = (lane + 1 < K) ? my_s - next_s : 1.0f;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) gap = fminf(gap, __shfl_xor_sync(0xffffffffu, gap, off));
-    margin = fminf(margin, gap);
+    for (int i = 0; i < kMaxPerLane; ++i) kb = max(kb, ck[i]);
+    const uint32_t m = __reduce_max_sync(kFull, kb);
+    if (m != 0u) margin = fminf(margin, prev - key_score(m));
   }
   if (lane < K) {
     float w = 0.f;
@@ -330,6 +197,10 @@ __device__ float2 warp_select(const float (&s_in)[kMaxPerLane], const float* __r
   return make_float2(margin_group, margin);
 }
 
+__device__ __forceinline__ float sigmoid(float l) { return 1.0f / (1.0f + expf(-l)); }
+
+// One warp per token: sigmoid of the final logits [T][E] and the selection
+// (used where the fused router below cannot select itself).
 __global__ void __launch_bounds__(256) router_select_kernel(const float* __restrict__ logits, int T,
                                                             int E, int G, int Gk, int K, float scale,
                                                             const float* __restrict__ bias,
@@ -344,9 +215,245 @@ __global__ void __launch_bounds__(256) router_select_kernel(const float* __restr
 #pragma unroll
   for (int i = 0; i < kMaxPerLane; ++i) {
     const int e = lane + 32 * i;
-    s[i] = (e < E) ? 1.0f / (1.0f + expf(-logits[static_cast<size_t>(t) * E + e])) : -1.0f;
+    s[i] = (e < E) ? sigmoid(logits[static_cast<size_t>(t) * E + e]) : 0.f;
   }
   warp_select(s, bias, lane, t, E, G, Gk, K, scale, topk_idx, topk_w, status);
+}
+
+// ---------------------------------------------------------------- SIMT path (small batches)
+//
+// router_simt_kernel: one CTA per (64 tokens, 16 experts, 1/8 of the hidden
+// dimension); the 8 CTAs of a hidden-dimension split form a thread-block
+// cluster. A producer warp streams x (bf16, 128-byte swizzled rows) and W_r
+// (fp32) tiles of 64 hidden elements through an 8-deep shared-memory ring by
+// TMA; each of 8 consumer warps takes 8 of a stage's 64 hidden elements for
+// the whole 64 x 16 tile (lane: 4 tokens x 8 experts, packed FP32 FMAs). The
+// partial sums are added in a fixed order: the warps' in the CTA, then the
+// cluster's CTAs through distributed shared memory, each CTA finishing 8 of
+// the 64 tokens, so the logits do not depend on scheduling. They go to
+// logits[T][E]. The last CTA to finish a group of 8 tokens (counted in a
+// ticket that it returns to 0) then selects those tokens, one warp each.
+
+constexpr int kRsTokens = 64;    // tokens per tile
+constexpr int kRsExperts = 16;   // experts per tile
+constexpr int kRsBK = 64;        // hidden elements per pipeline stage
+constexpr int kRsCluster = 8;    // CTAs per cluster: parts of the hidden dimension
+constexpr int kRsStages = 8;
+constexpr int kRsWarps = 8;      // consumer warps; one more warp produces
+constexpr int kRsThreads = 32 * (kRsWarps + 1);
+constexpr int kRsTokensPerRank = kRsTokens / kRsCluster;  // tokens each CTA finishes (and may select)
+constexpr uint32_t kRsXBytes = kRsTokens * kRsBK * 2;     // 8 KB
+constexpr uint32_t kRsWBytes = kRsBK * kRsExperts * 4;    // 4 KB
+constexpr uint32_t kRsStageBytes = kRsXBytes + kRsWBytes; // 12 KB, a multiple of 1024
+constexpr uint64_t kRsWaitNs = 2000000000ull;
+constexpr uint64_t kRsDrainNs = 1000000000ull;
+static_assert(kRsWarps * 8 == kRsBK, "a consumer warp takes 8 hidden elements of a stage");
+static_assert(kRsTokens * kRsExperts == 4 * 256 && kRsTokensPerRank * kRsExperts == 128, "reduction shapes");
+
+struct RsArgs {
+  int T, d, E, G, Gk, K;
+  float scale;
+  const float* bias;   // [E] selection bias or null
+  float* logits;       // [T][E]
+  int32_t* ticket;     // [ceil(T / 64) * 8], zero between calls; null: the selection runs separately
+  int32_t* topk_idx;
+  float* topk_w;
+  int32_t* status;
+  int32_t* timeout_where;
+  long long wait_spins;
+};
+
+// d = (a, a) * b + c, two IEEE fp32 FMAs in one instruction
+__device__ __forceinline__ float2 fma2(float a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %2};\n mov.b64 rb, {%3, %4};\n mov.b64 rc, {%5, %6};\n"
+      " fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
+__device__ __forceinline__ void rs_fail(const RsArgs& a, volatile int* abort, int where) {
+  latch_status(a.status, MOE_DEV_TIMEOUT);
+  if (a.timeout_where) atomicCAS(a.timeout_where, 0, where);
+  *abort = 1;
+}
+
+__global__ void __cluster_dims__(1, 1, kRsCluster) __launch_bounds__(kRsThreads, 2)
+    router_simt_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                       const RsArgs a) {
+  extern __shared__ uint8_t rs_raw[];
+  __shared__ __align__(8) uint64_t full_bar[kRsStages];
+  __shared__ __align__(8) uint64_t empty_bar[kRsStages];
+  __shared__ __align__(16) float cta_part[kRsTokens * kRsExperts];  // this CTA's sums, [token][expert]
+  __shared__ int abort_flag, is_last;
+  uint8_t* smem = rs_raw + ((1024u - (smem_u32(rs_raw) & 1023u)) & 1023u);
+  volatile int* abort = &abort_flag;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t0 = blockIdx.x * kRsTokens, e0 = blockIdx.y * kRsExperts;
+  const int nchunks = a.d / kRsBK;
+  const int c0 = rank * nchunks / kRsCluster, c1 = (rank + 1) * nchunks / kRsCluster;
+  pdl_launch_dependents();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kRsStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], kRsWarps);
+    }
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kRsWarps && lane == 0) {
+    tma_prefetch_desc(&tmX);
+    tma_prefetch_desc(&tmW);
+  }
+  __syncthreads();
+  pdl_wait();  // x may come from earlier work on the stream
+
+  int issued = 0;
+  const int q = lane & 15, o = lane >> 4;  // tokens q, q+16, q+32, q+48; experts 8o .. 8o+7
+  float2 acc[4][4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+#pragma unroll
+    for (int p = 0; p < 4; ++p) acc[j][p] = make_float2(0.f, 0.f);
+  if (warp == kRsWarps) {
+    if (lane == 0) {
+      for (int i = 0; i < c1 - c0; ++i) {
+        const int s = i % kRsStages;
+        if (i >= kRsStages &&
+            !mbar_wait_bounded(&empty_bar[s], static_cast<uint32_t>((i / kRsStages - 1) & 1), a.wait_spins, kRsWaitNs,
+                               abort)) {
+          if (!*abort) rs_fail(a, abort, 15);
+          break;
+        }
+        uint8_t* st = smem + static_cast<size_t>(s) * kRsStageBytes;
+        mbar_arrive_expect_tx(&full_bar[s], kRsStageBytes);
+        tma_load_2d(st, &tmX, (c0 + i) * kRsBK, t0, &full_bar[s]);
+        tma_load_2d(st + kRsXBytes, &tmW, e0, (c0 + i) * kRsBK, &full_bar[s]);
+        ++issued;
+      }
+    }
+  } else {
+    for (int i = 0; i < c1 - c0; ++i) {
+      const int s = i % kRsStages;
+      const bool ok =
+          __all_sync(kFull, mbar_wait_bounded(&full_bar[s], static_cast<uint32_t>((i / kRsStages) & 1), a.wait_spins,
+                                              kRsWaitNs, abort));
+      if (!ok) {
+        if (lane == 0 && !*abort) rs_fail(a, abort, 16);
+        break;
+      }
+      const uint8_t* st = smem + static_cast<size_t>(s) * kRsStageBytes;
+      const float* ws = reinterpret_cast<const float*>(st + kRsXBytes) + warp * 8 * kRsExperts + o * 8;
+      uint4 xv[4];  // x[t][8 warp .. 8 warp + 7] of the lane's tokens (16-byte chunk `warp` of a swizzled row)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int t = q + 16 * j;
+        xv[j] = *reinterpret_cast<const uint4*>(st + t * 128 + ((warp ^ (t & 7)) << 4));
+      }
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const float4 w0 = *reinterpret_cast<const float4*>(ws + kk * kRsExperts);
+        const float4 w1 = *reinterpret_cast<const float4*>(ws + kk * kRsExperts + 4);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t word = (&xv[j].x)[kk >> 1];
+          const float xf = __uint_as_float((kk & 1) ? (word & 0xFFFF0000u) : (word << 16));
+          acc[j][0] = fma2(xf, make_float2(w0.x, w0.y), acc[j][0]);
+          acc[j][1] = fma2(xf, make_float2(w0.z, w0.w), acc[j][1]);
+          acc[j][2] = fma2(xf, make_float2(w1.x, w1.y), acc[j][2]);
+          acc[j][3] = fma2(xf, make_float2(w1.z, w1.w), acc[j][3]);
+        }
+      }
+      fence_proxy_async_smem();  // the reads above complete before TMA may refill the stage
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[s]);
+    }
+  }
+  __syncthreads();
+
+  // the warps' partial tiles, added in warp order (the ring is free: every
+  // stage was consumed unless the CTA gave up, and then nothing is reused)
+  const bool aborted = *abort != 0;
+  float* red = reinterpret_cast<float*>(smem);  // [warp][token][expert]
+  if (!aborted && warp < kRsWarps) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float* row = red + (warp * kRsTokens + q + 16 * j) * kRsExperts + o * 8;
+      *reinterpret_cast<float4*>(row) = make_float4(acc[j][0].x, acc[j][0].y, acc[j][1].x, acc[j][1].y);
+      *reinterpret_cast<float4*>(row + 4) = make_float4(acc[j][2].x, acc[j][2].y, acc[j][3].x, acc[j][3].y);
+    }
+  }
+  __syncthreads();
+  if (!aborted && threadIdx.x < 256) {
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const int i = threadIdx.x + 256 * m;
+      float v = red[i];
+#pragma unroll
+      for (int w = 1; w < kRsWarps; ++w) v += red[w * kRsTokens * kRsExperts + i];
+      cta_part[i] = v;
+    }
+  }
+  cluster.sync();  // every CTA's partial tile is published
+
+  // this CTA finishes tokens t0 + 8 rank .. + 7: the cluster's partials in rank order
+  if (threadIdx.x < kRsTokensPerRank * kRsExperts) {
+    const int i = rank * kRsTokensPerRank * kRsExperts + threadIdx.x;
+    float v = 0.f;
+#pragma unroll
+    for (int c = 0; c < kRsCluster; ++c) v += cluster.map_shared_rank(cta_part, c)[i];
+    const int t = t0 + i / kRsExperts, e = e0 + i % kRsExperts;
+    if (t < a.T && e < a.E) a.logits[static_cast<size_t>(t) * a.E + e] = v;
+    __threadfence();
+  }
+  cluster.sync();  // no CTA leaves while another may still read its partials
+
+  if (aborted && warp == kRsWarps && lane == 0) {
+    // some waits returned early: let every copy issued into each stage land
+    // (bounded) before the CTA exits
+    for (int s = 0; s < kRsStages; ++s) {
+      if (issued > s) {
+        const int f = s + kRsStages * ((issued - 1 - s) / kRsStages);
+        mbar_wait_bounded(&full_bar[s], static_cast<uint32_t>((f / kRsStages) & 1), 1ll << 40, kRsDrainNs, nullptr);
+      }
+    }
+  }
+  if (a.ticket == nullptr) return;
+  if (threadIdx.x == 0) {
+    int32_t* tk = a.ticket + blockIdx.x * kRsCluster + rank;
+    is_last = atomicAdd(tk, 1) == static_cast<int>(gridDim.y) - 1;
+    if (is_last) *tk = 0;  // every CTA of this call has counted: ready for the next call
+  }
+  __syncthreads();
+  if (!is_last || warp >= kRsTokensPerRank) return;
+  __threadfence();
+  const int t = t0 + rank * kRsTokensPerRank + warp;
+  if (t >= a.T) return;
+  float s[kMaxPerLane];
+#pragma unroll
+  for (int i = 0; i < kMaxPerLane; ++i) {
+    const int e = lane + 32 * i;
+    s[i] = (e < a.E) ? sigmoid(__ldcg(a.logits + static_cast<size_t>(t) * a.E + e)) : 0.f;
+  }
+  warp_select(s, a.bias, lane, t, a.E, a.G, a.Gk, a.K, a.scale, a.topk_idx, a.topk_w, a.status);
+}
+
+// W_r [d][E] -> [d][E4] (E4 = E rounded up to a multiple of 4, zero columns
+// added), so its rows meet the 16-byte stride rule of tensor copies.
+__global__ void __launch_bounds__(256) wr_pad_kernel(const float* __restrict__ wr, int d, int E, int E4,
+                                                     float* __restrict__ out) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int64_t n = static_cast<int64_t>(d) * E4;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t k = i / E4;
+    const int e = static_cast<int>(i - k * E4);
+    out[i] = e < E ? wr[k * E + e] : 0.f;
+  }
 }
 
 // ---------------------------------------------------------------- tensor-core path
@@ -751,6 +858,7 @@ __global__ void __launch_bounds__(kFlagThreads) router_flagged_logits_kernel(
           acc[3] = fmaf(a.w, w, acc[3]);
         }
       }
+      fence_proxy_async_smem();
       __syncthreads();  // the slot may be refilled after every thread is done with it
     }
 #pragma unroll
@@ -831,6 +939,22 @@ int encode_router_map(CUtensorMap* map, const void* base, uint64_t inner, uint64
   cuuint32_t estr[2] = {1, 1};
   const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : static_cast<int>(r);
+}
+
+// fp32 matrix [outer][inner] (row stride `stride` elements), boxes of
+// box_inner x box_outer, no swizzle; rows past the end read as zero.
+int encode_f32_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t stride,
+                   uint32_t box_inner, uint32_t box_outer) {
+  auto fn = router_encode_fn();
+  if (!fn) return -1;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {stride * 4};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? 0 : static_cast<int>(r);
 }
@@ -967,37 +1091,56 @@ cudaError_t launch_router_tc(const uint16_t* x, const float* w_r, void* scratch,
                     topk_groups, top_k, routed_scale, sel_bias, sc.flagged, flagged_count, topk_idx, topk_w, status);
 }
 
-// Smallest split of the hidden dimension (into >= 64-element slices) that
-// gives at least one block per SM.
-int router_splits(int T, int d, int E, int num_sms) {
-  const int tiles = ((T + RT - 1) / RT) * ((E + RE - 1) / RE);
-  const int target = (num_sms + tiles - 1) / tiles;
-  const int chunks = d / RK;
-  int best = 1;
-  for (int s = 1; s <= chunks; ++s) {
-    if (chunks % s || d / s < 64) continue;
-    best = s;
-    if (s >= target) break;
-  }
-  return best;
+static_assert(sizeof(WsHeader::route_ticket) == sizeof(int32_t) * kRouteTickets, "ticket array size");
+
+bool router_simt_selects(int T) { return ((T + kRsTokens - 1) / kRsTokens) * kRsCluster <= kRouteTickets; }
+
+size_t router_simt_scratch_bytes(int d, int E) {
+  return E % 4 ? sizeof(float) * static_cast<size_t>(d) * ((E + 3) & ~3) : 0;
 }
 
-cudaError_t launch_router_logits(const uint16_t* x, const float* w_r, float* partial, int T, int d, int E,
-                                 int splits, cudaStream_t stream) {
-  const dim3 grid((E + RE - 1) / RE, (T + RT - 1) / RT, splits);
-  return launch_pdl(router_logits_kernel, grid, dim3(256), 0, stream, x, w_r, partial, T, d, E, d / splits);
-}
-
-cudaError_t launch_router_select(float* partial, int splits, int T, int E, int n_groups, int topk_groups,
-                                 int top_k, float routed_scale, const float* sel_bias, int32_t* topk_idx,
-                                 float* topk_w, int32_t* status, cudaStream_t stream) {
-  if (splits > 1) {
-    const int64_t n = static_cast<int64_t>(T) * E;
-    const cudaError_t err = launch_pdl(split_reduce_kernel, dim3(static_cast<unsigned>((n + 255) / 256)), dim3(256), 0,
-                                       stream, partial, splits, n);
+cudaError_t launch_router_simt(const uint16_t* x, const float* w_r, void* scratch, float* logits, int32_t* ticket,
+                               int T, int d, int E, int n_groups, int topk_groups, int top_k, float routed_scale,
+                               const float* sel_bias, int32_t* topk_idx, float* topk_w, int32_t* status,
+                               int32_t* timeout_where, long long wait_spins, int num_sms, cudaStream_t stream) {
+  const float* w = w_r;
+  int E4 = E;
+  cudaError_t err;
+  if (E % 4) {
+    E4 = (E + 3) & ~3;
+    float* wp = static_cast<float*>(scratch);
+    err = launch_pdl(wr_pad_kernel, dim3(num_sms), dim3(256), 0, stream, w_r, d, E, E4, wp);
     if (err != cudaSuccess) return err;
+    w = wp;
   }
-  return launch_pdl(router_select_kernel, dim3((T + 7) / 8), dim3(256), 0, stream, partial, T, E, n_groups,
+  CUtensorMap tmX, tmW;
+  if (encode_router_map(&tmX, x, d, T, kRsTokens) ||
+      encode_f32_map(&tmW, w, E4, d, E4, kRsExperts, kRsBK))
+    return cudaErrorInvalidValue;
+  const bool selects = router_simt_selects(T);
+  RsArgs a;
+  a.T = T;
+  a.d = d;
+  a.E = E;
+  a.G = n_groups;
+  a.Gk = topk_groups;
+  a.K = top_k;
+  a.scale = routed_scale;
+  a.bias = sel_bias;
+  a.logits = logits;
+  a.ticket = selects ? ticket : nullptr;
+  a.topk_idx = topk_idx;
+  a.topk_w = topk_w;
+  a.status = status;
+  a.timeout_where = timeout_where;
+  a.wait_spins = wait_spins;
+  const size_t smem = 1024 + static_cast<size_t>(kRsStages) * kRsStageBytes;
+  err = cudaFuncSetAttribute(router_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  const dim3 grid((T + kRsTokens - 1) / kRsTokens, (E + kRsExperts - 1) / kRsExperts, kRsCluster);
+  err = launch_pdl(router_simt_kernel, grid, dim3(kRsThreads), smem, stream, tmX, tmW, a);
+  if (err != cudaSuccess || selects) return err;
+  return launch_pdl(router_select_kernel, dim3((T + 7) / 8), dim3(256), 0, stream, logits, T, E, n_groups,
                     topk_groups, top_k, routed_scale, sel_bias, topk_idx, topk_w, status);
 }
 

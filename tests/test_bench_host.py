@@ -87,14 +87,14 @@ def test_roofline_arithmetic():
     assert big[0]["bound"] == "tensor"
 
 
-def test_router_split_rule():
-    # decode: 2 tiles of 64 tokens x 128 experts -> split the hidden dim 80 ways (64-element slices)
-    assert bench.router_splits(64, 5120, 256, 148) == 80
-    assert bench.router_splits(4096, 5120, 256, 148) == 2
-    assert bench.router_splits(32768, 5120, 256, 148) == 1
+def test_kernel_counts():
+    assert bench.simt_router_kernels(64, 256) == 1       # logits kernel selects itself
+    assert bench.simt_router_kernels(1536, 256) == 1     # 24 tiles x 8 tickets = 192
+    assert bench.simt_router_kernels(1537, 256) == 2     # + a selection kernel
+    assert bench.simt_router_kernels(64, 18) == 2        # + the W_r padding copy
     assert bench.kernels_per_step(W.CONFIGS["skewed"], 148) == 13   # tensor-core router: 5 kernels
-    # SIMT logits + reduce + select; plan kernel (with the GEMM schedule) + gather; GEMM1, GEMM2, combine
-    assert bench.kernels_per_step(W.CONFIGS["decode"], 148) == 8
+    # SIMT router; plan kernel (with the GEMM schedule) + gather; GEMM1, GEMM2, combine
+    assert bench.kernels_per_step(W.CONFIGS["decode"], 148) == 6
     assert bench.permute_uses_plan_kernel(1024, 256) and not bench.permute_uses_plan_kernel(1025, 256)
 
 

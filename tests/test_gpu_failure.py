@@ -67,3 +67,28 @@ def test_router_wait_timeout_is_reported_and_the_context_recovers():
     torch.cuda.synchronize()
     assert bm.moe_get_device_status(ws) == bm.MOE_DEV_OK
     compare_routing(cfg, idx.cpu().numpy(), w.cpu().numpy(), O.route(cfg, x_h, wr_h), label="router after timeout")
+
+
+def test_simt_router_wait_timeout_is_reported_and_the_context_recovers():
+    """T = 64 takes the SIMT router (a TMA ring per CTA, clusters of 8 CTAs): with one poll per wait
+    it latches MOE_DEV_TIMEOUT, still meets every cluster barrier and counts itself in the
+    selection tickets, and returns; the next call on the same workspace routes like the oracle."""
+    cfg = W.CONFIGS["decode"].with_tokens(64)
+    x_h, wr_h = W.gen_x(cfg, 8), W.gen_wr(cfg, 8)
+    dims = bm.Dims.from_config(cfg)
+    ws = bm.allocate_workspace(dims)
+    x, w_r = dev(x_h), dev(wr_h)
+    idx = torch.empty((cfg.T, cfg.top_k), dtype=torch.int32, device="cuda")
+    w = torch.empty((cfg.T, cfg.top_k), dtype=torch.float32, device="cuda")
+    bm.moe_set_wait_bound(1)
+    try:
+        bm.moe_route(dims, x, w_r, idx, w, ws)
+        torch.cuda.synchronize()
+        code = bm.moe_get_device_status(ws, clear=True)
+    finally:
+        bm.moe_set_wait_bound(0)
+    assert code == bm.MOE_DEV_TIMEOUT
+    bm.moe_route(dims, x, w_r, idx, w, ws)
+    torch.cuda.synchronize()
+    assert bm.moe_get_device_status(ws) == bm.MOE_DEV_OK
+    compare_routing(cfg, idx.cpu().numpy(), w.cpu().numpy(), O.route(cfg, x_h, wr_h), label="SIMT router after timeout")

@@ -157,6 +157,68 @@ def test_route_uniform_scores():
     assert np.all(gw == np.float32(0.3125))
 
 
+@pytest.mark.parametrize("name,T,seed", [("tiny", 77, 31), ("decode", 64, 32), ("decode", 1100, 33)])
+def test_route_strong_selection_bias(name, T, seed):
+    """A selection bias of a few units (most selection scores s + b negative, some below -1):
+    the selection works on exact order keys of s + b, so no sentinel value can collide with a real
+    score; SIMT (T < 1024) and tensor-core (T >= 1024) routers."""
+    cfg = W.CONFIGS[name].with_tokens(T)
+    x_h, wr_h = W.gen_x(cfg, seed), W.gen_wr(cfg, seed)
+    bias = (6.0 * (W.uniform_f64(seed, W.TID_AUX + 7, 0, cfg.E) - 0.7)).astype(np.float32)
+    dims = bm.Dims.from_config(cfg)
+    ws = bm.allocate_workspace(dims)
+    idx = torch.empty((T, cfg.top_k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, cfg.top_k), dtype=torch.float32, device="cuda")
+    bm.moe_route(dims, dev(x_h), dev(wr_h), idx, w, ws, sel_bias=dev(bias))
+    torch.cuda.synchronize()
+    assert bm.moe_get_device_status(ws) == bm.MOE_DEV_OK
+    orc = O.route(cfg, x_h, wr_h, bias=bias)
+    assert np.mean(orc["scores"] + bias < -1.0) > 0.2
+    excluded, _, _ = compare_routing(cfg, idx.cpu().numpy(), w.cpu().numpy(), orc, bias=bias,
+                                     label=f"strong bias {name} T={T}")
+    assert excluded.size <= max(2, T // 200)
+
+
+@pytest.mark.parametrize("E,G,Gk,K,T,d", [(18, 6, 3, 4, 50, 192),   # E not a multiple of 4: padded W_r copy
+                                          (7, 1, 1, 3, 9, 64),       # one group
+                                          (8, 8, 4, 2, 130, 128),    # one expert per group
+                                          (96, 32, 8, 20, 65, 256),  # 32 groups, 20 slots
+                                          (16, 4, 2, 4, 1536, 192),  # the largest batch the logits kernel selects in
+                                          (16, 4, 2, 4, 1600, 192)]) # selection in a kernel of its own
+def test_route_simt_shapes(E, G, Gk, K, T, d):
+    """SIMT router over shapes away from the Beam one: expert counts that are not a multiple of
+    the 16-expert tile or of 4, one group, one expert per group, 32 groups, a hidden dimension
+    shorter than the 8-way split (d = 64: some CTAs of a cluster add nothing), and batches on
+    either side of the largest one whose selection runs inside the logits kernel (d = 192 keeps
+    T >= 1024 off the tensor-core router)."""
+    cfg = W.MoEConfig("simt", T=T, d=d, E=E, n_groups=G, topk_groups=Gk, top_k=K, inter=64)
+    x_h, wr_h = W.gen_x(cfg, 40 + E), W.gen_wr(cfg, 40 + E)
+    gi, gw = route_only(cfg, x_h, wr_h)
+    excluded, _, _ = compare_routing(cfg, gi, gw, O.route(cfg, x_h, wr_h), label=f"SIMT E={E} G={G} T={T} d={d}")
+    assert excluded.size <= max(2, T // 200)
+
+
+def test_route_simt_repeated_calls_reuse_tickets():
+    """The fused selection counts finished CTAs in the workspace header and returns the counts to
+    zero: many calls on one workspace, with different batch sizes, route like the oracle."""
+    cfg = W.CONFIGS["decode"]
+    dims_max = bm.Dims.from_config(cfg.with_tokens(200))
+    ws = bm.allocate_workspace(dims_max)
+    wr_h = W.gen_wr(cfg, 61)
+    w_r = dev(wr_h)
+    for i, T in enumerate([64, 200, 1, 64, 130, 200, 7]):
+        c = cfg.with_tokens(T)
+        x_h = W.gen_x(c, 61 + i)
+        dims = bm.Dims.from_config(c)
+        idx = torch.empty((T, c.top_k), dtype=torch.int32, device="cuda")
+        w = torch.empty((T, c.top_k), dtype=torch.float32, device="cuda")
+        bm.moe_route(dims, dev(x_h), w_r, idx, w, ws)
+        torch.cuda.synchronize()
+        assert bm.moe_get_device_status(ws) == bm.MOE_DEV_OK
+        compare_routing(c, idx.cpu().numpy(), w.cpu().numpy(), O.route(c, x_h, wr_h), label=f"repeated call {i} T={T}")
+    assert int(ws[:1024].view(torch.int32)[13:13 + 192].abs().sum().item()) == 0
+
+
 # ---------------------------------------------------------------------------------------- permute
 
 @pytest.mark.parametrize("T,E,K,hot", [(64, 16, 4, 0), (77, 16, 4, 3), (1, 256, 8, 0), (4096, 256, 8, 0),
