@@ -60,9 +60,9 @@ def permute_uses_plan_kernel(T, E):
 def kernels_per_step(cfg, num_sms):
     """Kernels one moe_forward launches: router (tensor-core: W_r split, tensor-core logits,
     selection, narrow-margin recompute (logits + selection); SIMT: logits with the selection,
-    see simt_router_kernels), permutation (small batches: plan kernel, which also builds the GEMM work items, +
-    gather; otherwise bitmap, column scan, offsets, gather + the GEMMs' schedule kernel),
-    GEMM1, GEMM2, combine."""
+    see simt_router_kernels), permutation (small batches: plan kernel, which also builds the GEMM
+    schedule, + gather; otherwise bitmap, column scan, offsets, gather + the GEMMs' schedule
+    kernel), GEMM1, GEMM2, combine."""
     if cfg.T >= ROUTER_TC_MIN_TOKENS:
         router = 5
     else:
@@ -216,7 +216,8 @@ def record_traffic(directory, out=None):
         g1, g2, _ = roofline_numbers(cfg, touched, peaks)
         kernels = {}
         for name, m in parse_ncu_csv(cpath):
-            tmpl = name[name.index("<"):name.index(">") + 1] if "expert_gemm_kernel" in name else None
+            tmpl = (name[name.index("<", name.index("expert_gemm_kernel")):name.index(">", name.index("expert_gemm_kernel")) + 1]
+                    if "expert_gemm_kernel" in name else None)
             if tmpl not in NCU_GEMM_NAMES:
                 continue
             kname = NCU_GEMM_NAMES[tmpl]

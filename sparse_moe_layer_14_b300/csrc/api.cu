@@ -39,7 +39,7 @@ size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 
 enum Region {
   R_HDR, R_PART, R_WSPLIT, R_BITMAP, R_WPRE, R_COUNTS, R_OFFS, R_IDX, R_W, R_ROWTOK, R_INVROW,
-  R_ITEMS1, R_ITEMS2, R_XPERM, R_H, R_Y, R_NUM
+  R_SCHED, R_TILEX, R_XPERM, R_H, R_Y, R_NUM
 };
 
 struct Layout {
@@ -70,8 +70,8 @@ Layout make_layout(const moe_dims_t& d) {
   sz[R_W] = sizeof(float) * R;
   sz[R_ROWTOK] = sizeof(int32_t) * R;
   sz[R_INVROW] = sizeof(int32_t) * R;
-  sz[R_ITEMS1] = sizeof(int4) * static_cast<size_t>(pl.max_items1);
-  sz[R_ITEMS2] = sizeof(int4) * static_cast<size_t>(pl.max_items2);
+  sz[R_SCHED] = sizeof(int4) * d.E;
+  sz[R_TILEX] = sizeof(int32_t) * static_cast<size_t>(pl.max_tiles);
   sz[R_XPERM] = sizeof(uint16_t) * R * d.d;
   sz[R_H] = sizeof(uint16_t) * R * d.inter;
   sz[R_Y] = sizeof(float) * R * d.d;
@@ -184,14 +184,14 @@ ExpertWeightsDev weights_dev(int wfmt, const moe_expert_weights_t* w) {
 
 ExpertBuffers expert_buffers(const uint16_t* x_perm, const int32_t* offsets, float* y, void* ws, const Layout& L) {
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
-  ExpertBuffers b;
+  ExpertBuffers b{};
   b.x_perm = x_perm;
   b.offsets = offsets;
   b.h = region<uint16_t>(ws, L, R_H);
   b.y = nullptr;
   b.y_f32 = y;
-  b.items1 = region<int4>(ws, L, R_ITEMS1);
-  b.items2 = region<int4>(ws, L, R_ITEMS2);
+  b.table = region<int4>(ws, L, R_SCHED);
+  b.tile_expert = region<int32_t>(ws, L, R_TILEX);
   b.n_items = hdr->n_items;
   b.status = &hdr->status;
   b.timeout_where = &hdr->timeout_where;
@@ -453,7 +453,7 @@ moe_status_t check_dense_dims(const moe_dims_t* d) {
 }
 
 struct DenseLayout {
-  size_t offs, items1, items2, h, total;
+  size_t offs, table, tilex, h, total;
 };
 
 DenseLayout make_dense_layout(const moe_dims_t& d) {
@@ -462,10 +462,10 @@ DenseLayout make_dense_layout(const moe_dims_t& d) {
   size_t o = align_up(sizeof(WsHeader));
   L.offs = o;
   o = align_up(o + 2 * sizeof(int32_t));
-  L.items1 = o;
-  o = align_up(o + sizeof(int4) * static_cast<size_t>(pl.max_items1));
-  L.items2 = o;
-  o = align_up(o + sizeof(int4) * static_cast<size_t>(pl.max_items2));
+  L.table = o;
+  o = align_up(o + sizeof(int4));
+  L.tilex = o;
+  o = align_up(o + sizeof(int32_t) * static_cast<size_t>(pl.max_tiles));
   L.h = o;
   o = align_up(o + sizeof(uint16_t) * static_cast<size_t>(d.T) * d.inter);
   L.total = o;
@@ -529,14 +529,14 @@ moe_status_t moe_dense_mlp(const moe_dims_t* dims, const moe_bf16_t* x, const mo
   if (mark(0, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (launch_pdl(dense_offsets_kernel, dim3(1), dim3(1), 0, s, offs, dims->T) != cudaSuccess) return MOE_ERR_CUDA;
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
-  ExpertBuffers b;
+  ExpertBuffers b{};
   b.x_perm = x;  // one expert: the permuted rows are the tokens in order
   b.offsets = offs;
   b.h = reinterpret_cast<uint16_t*>(base + L.h);
   b.y = out;
   b.y_f32 = nullptr;
-  b.items1 = reinterpret_cast<int4*>(base + L.items1);
-  b.items2 = reinterpret_cast<int4*>(base + L.items2);
+  b.table = reinterpret_cast<int4*>(base + L.table);
+  b.tile_expert = reinterpret_cast<int32_t*>(base + L.tilex);
   b.n_items = hdr->n_items;
   b.status = &hdr->status;
   b.timeout_where = &hdr->timeout_where;

@@ -37,8 +37,9 @@
 // Waits off the critical path sleep between polls: the MMA issuer shares a
 // scheduler with epilogue and converter warps, and their spinning took its
 // issue slots (MMA slices up to 1.5x slower).
-// Work items {expert, weight tile, first row, tokens} are built on the device
-// from the expert offsets (no host synchronisation) and taken round-robin.
+// Work items {expert, weight tile, first row, tokens} follow from a per-expert
+// schedule built on the device from the expert offsets (no host
+// synchronisation) and are taken round-robin.
 // Every mbarrier wait is bounded; on expiry the CTA latches MOE_DEV_TIMEOUT,
 // waits (bounded) for its own copies and MMAs in flight, frees TMEM, returns.
 #include <algorithm>
@@ -83,7 +84,9 @@ constexpr int kConvThreads = 256;   // one converter thread per row of each weig
 constexpr int threads_for(int fmt) { return fmt != kFmtBf16 ? kConvBase + kConvThreads : 320; }
 
 struct GemmArgs {
-  const int4* items;
+  const int4* table;       // work schedule (schedule.cuh)
+  const int32_t* tile_expert;
+  int wt;                  // weight tiles per expert
   const int32_t* n_items;
   int K;           // reduction length
   int Nw;          // weight rows per expert = output columns
@@ -263,7 +266,7 @@ __global__ void __launch_bounds__(threads_for(kFmt), 1)
       uint32_t phase = 0;
       bool ok = true;
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-        const int4 item = p.items[it];
+        const int4 item = work_item(p.table, p.tile_expert, p.wt, it);
         const int a_row = item.x * p.Nw + item.y * kItemRows;
         const int nbox = (item.w + TOK_BOX - 1) / TOK_BOX;
         const uint32_t bytes = (kConv ? kPB : kATileBytes) * nA + static_cast<uint32_t>(nbox) * kTokBoxBytes;
@@ -312,7 +315,7 @@ __global__ void __launch_bounds__(threads_for(kFmt), 1)
       int stage = 0, acc = 0, cstage = 0;
       uint32_t phase = 0, acc_phase = 0, cphase = 0;
       for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-        const int4 item = p.items[it];
+        const int4 item = work_item(p.table, p.tile_expert, p.wt, it);
         const int n_mma = (item.w + 15) & ~15;
         const uint32_t idesc = idesc_bf16_f32(BM, n_mma);
         if (!mbar_wait_bounded(&acce_bar[acc], acc_phase ^ 1u, p.wait_spins, kWaitNs, abort)) {
@@ -387,7 +390,7 @@ __global__ void __launch_bounds__(threads_for(kFmt), 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-      const int4 item = p.items[it];
+      const int4 item = work_item(p.table, p.tile_expert, p.wt, it);
       // tcgen05.ld is warp-collective: the whole warp proceeds or stops together
       const bool ok = __all_sync(
           0xffffffffu, mbar_wait_bounded(&accf_bar[acc], acc_phase, p.wait_spins, kWaitNs, abort, kSleepItemNs));
@@ -504,12 +507,11 @@ __global__ void __launch_bounds__(threads_for(kFmt), 1)
                             static_cast<uint32_t>(t * (kConvCols / 2));  // this tile's 32 columns of a slot
     int stage = 0, cstage = 0;
     uint32_t phase = 0, cphase = 0;
-    // scale group g of item `it`: slices 4g .. 4g+3
-    auto load_group = [&](int it, int g) {
+    // scale group g of `item` (expert -1: none): slices 4g .. 4g+3
+    auto load_group = [&](const int4& item, int g) {
       uint4 v = make_uint4(0, 0, 0, 0);
-      if (it >= n_items) return v;
-      const int4 item = p.items[it];
-      if (!dcheck(item.x >= 0 && item.x < p.E, p.status)) return v;
+      if (item.x < 0) return v;
+      if (!dcheck(item.x < p.E, p.status)) return v;
       if constexpr (kFp8) {
         const int nbr = p.Nw / BM, kbr = p.K / BM;  // 128-blocks per expert: rows, K
         const int br = (item.y * kItemRows + row_off) / BM;
@@ -530,13 +532,17 @@ __global__ void __launch_bounds__(threads_for(kFmt), 1)
       }
       return v;
     };
-    uint4 cur = make_uint4(0, 0, 0, 0), nxt = load_group(blockIdx.x, 0);
+    // the item's schedule entry is looked up once per item (the next one a group ahead)
+    auto item_at = [&](int it) { return it < n_items ? work_item(p.table, p.tile_expert, p.wt, it) : make_int4(-1, 0, 0, 0); };
+    int4 item = item_at(blockIdx.x);
+    uint4 cur = make_uint4(0, 0, 0, 0), nxt = load_group(item, 0);
     bool ok = true;
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+      const int4 next_item = item_at(it + gridDim.x);
       for (int kb = 0; kb < kblocks; ++kb) {
         if ((kb & 3) == 0) {
           cur = nxt;
-          nxt = kb + 4 < kblocks ? load_group(it, (kb >> 2) + 1) : load_group(it + gridDim.x, 0);
+          nxt = kb + 4 < kblocks ? load_group(item, (kb >> 2) + 1) : load_group(next_item, 0);
         }
         const uint8_t* packed = smem + static_cast<size_t>(stage) * p.stage_bytes + p.p_offset + t * kPB;
         const int g = kb & 3;
@@ -575,6 +581,7 @@ __global__ void __launch_bounds__(threads_for(kFmt), 1)
           phase ^= 1u;
         }
       }
+      item = next_item;
     }
   }
 
@@ -603,13 +610,13 @@ __global__ void __launch_bounds__(threads_for(kFmt), 1)
   if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
 }
 
-// Work items from the expert offsets (build_work_items): one thread per expert (E <= 256).
+// The work schedule from the expert offsets (build_schedule): one thread per expert (E <= 256).
 __global__ void __launch_bounds__(256) schedule_kernel(const int32_t* __restrict__ offsets, int E, ScheduleArgs s,
                                                        int32_t* status) {
   __shared__ int warp_sums[8];
   pdl_launch_dependents();
   pdl_wait();
-  build_work_items(offsets, E, s, status, warp_sums);
+  build_schedule(offsets, E, s, status, warp_sums);
 }
 
 // ------------------------------------------------------------------ host side
@@ -733,8 +740,6 @@ ExpertPlan plan_experts(int T, int d, int E, int top_k, int inter, bool decoded)
   p.max_tiles = static_cast<int>(E + (R + p.n_max - 1) / p.n_max);
   p.wtiles1 = (inter + BM - 1) / BM;
   p.wtiles2 = (d + 2 * BM - 1) / (2 * BM);
-  p.max_items1 = static_cast<int64_t>(p.max_tiles) * p.wtiles1;
-  p.max_items2 = static_cast<int64_t>(p.max_tiles) * p.wtiles2;
   return p;
 }
 
@@ -744,11 +749,10 @@ ScheduleArgs schedule_args(const ExpertPlan& plan, const ExpertBuffers& buf, int
   s.wt1 = plan.wtiles1;
   s.wt2 = plan.wtiles2;
   s.R = R;
-  s.items1 = buf.items1;
-  s.items2 = buf.items2;
+  s.table = buf.table;
+  s.tile_expert = buf.tile_expert;
+  s.max_tiles = plan.max_tiles;
   s.n_items = buf.n_items;
-  s.cap1 = plan.max_items1;
-  s.cap2 = plan.max_items2;
   return s;
 }
 
@@ -793,7 +797,9 @@ cudaError_t launch_expert_ffn(const ExpertPlan& plan, const ExpertBuffers& buf, 
     return cudaErrorInvalidValue;
   }
   GemmArgs a1{};
-  a1.items = buf.items1;
+  a1.table = buf.table;
+  a1.tile_expert = buf.tile_expert;
+  a1.wt = plan.wtiles1;
   a1.n_items = buf.n_items;
   a1.K = d;
   a1.Nw = inter;
@@ -819,7 +825,9 @@ cudaError_t launch_expert_ffn(const ExpertPlan& plan, const ExpertBuffers& buf, 
   if (err != cudaSuccess) return err;
   if (after_gemm1 && (err = cudaEventRecord(after_gemm1, stream)) != cudaSuccess) return err;
   GemmArgs a2{};
-  a2.items = buf.items2;
+  a2.table = buf.table;
+  a2.tile_expert = buf.tile_expert;
+  a2.wt = plan.wtiles2;
   a2.n_items = buf.n_items + 1;
   a2.K = inter;
   a2.Nw = d;

@@ -33,7 +33,7 @@ cudaError_t launch_router_simt(const uint16_t* x, const float* w_r, void* scratc
 // FFMA recompute of all logits of the flagged tokens.
 // `scratch` holds router_tc_scratch_bytes(T, d, E) bytes.
 constexpr int kRouterTcMinTokens = 1024;
-constexpr int kRouterFlagSplits = 8;  // hidden-dimension parts of the fp32 recompute: [8][flagged][E] in `part`
+constexpr int kRouterFlagSplits = 16;  // hidden-dimension parts of the fp32 recompute: [16][flagged][E] in `part`
 int router_epad(int E);
 bool router_uses_tensor_cores(int T, int E, int d);
 size_t router_tc_scratch_bytes(int T, int d, int E);
@@ -67,7 +67,6 @@ struct ExpertPlan {
   int max_tiles;    // upper bound of (expert, token tile) pairs
   int wtiles1;      // 128-row weight tiles per expert in GEMM1 (ceil(inter/128))
   int wtiles2;      // 256-row weight tiles per expert in GEMM2 (ceil(d/256))
-  int64_t max_items1, max_items2;
 };
 // decoded: NVFP4 or FP8 weights (decoded into tensor memory; token tile <= 192)
 ExpertPlan plan_experts(int T, int d, int E, int top_k, int inter, bool decoded);
@@ -78,8 +77,8 @@ struct ExpertBuffers {
   uint16_t* h;             // [R][inter]
   uint16_t* y;             // [R][d] bf16 output (dense MLP), or null
   float* y_f32;            // [R][d] fp32 output (the experts), or null
-  int4* items1;            // GEMM1 work items {e, wtile, row0, ntok}
-  int4* items2;
+  int4* table;             // work schedule [E] (schedule.cuh)
+  int32_t* tile_expert;    // [max_tiles]
   int32_t* n_items;        // [2]
   int32_t* status;
   int32_t* timeout_where;

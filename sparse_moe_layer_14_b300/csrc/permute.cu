@@ -13,7 +13,7 @@
 //   4. gather_kernel     rows, inverse rows, x -> x_perm copy      1 block per (token, slot)
 // Small batches (E * ceil(T/32) words fit in shared memory) do 1-3 in one CTA,
 // plan_small_kernel, which needs no cleared bitmap in global memory and can
-// also build the expert GEMMs' work items.
+// also build the expert GEMMs' work schedule.
 #include "common.cuh"
 #include "kernels.h"
 #include "schedule.cuh"
@@ -106,7 +106,7 @@ constexpr int kPlanMaxWords = 8192;  // 32 KB of bitmap: T <= 1024 at E = 256
 // One CTA: the bitmap in shared memory (set bits, repeats latched), then one
 // warp per expert column for the per-word prefix counts (written with the
 // bitmap words for the gather) and the count, an exclusive scan of the counts
-// for the offsets, and with `do_schedule` the work items of the expert GEMMs.
+// for the offsets, and with `do_schedule` the work schedule of the expert GEMMs.
 __global__ void __launch_bounds__(kPlanThreads) plan_small_kernel(
     const int32_t* __restrict__ idx, int T, int E, int K, int nw, uint32_t* __restrict__ bitmap,
     int32_t* __restrict__ word_prefix, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_small_kernel(
     }
     __syncthreads();
   }
-  if (do_schedule) build_work_items(offs, E, sched, status, warp_sums);
+  if (do_schedule) build_schedule(offs, E, sched, status, warp_sums);
 }
 
 // One block per (token, slot): every thread derives the slot's row from the

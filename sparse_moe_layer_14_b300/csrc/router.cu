@@ -30,9 +30,10 @@
 //                        max_e |W_r[:, e]| (every partial sum of x_t . W_r[:, e]
 //                        is at most |x_t| |W_r[:, e]| by Cauchy-Schwarz, and
 //                        d/16 MMA steps each round once; kappa is set from
-//                        measured errors with a wide margin). |x_t| comes from
-//                        the tensor-core kernel's epilogue warps, the column
-//                        norms of W_r from wr_split_kernel. Elsewhere:
+//                        measured errors with a wide margin). |x_t| is summed
+//                        by the selecting warp from the token's row, the
+//                        column norms of W_r come from wr_split_kernel.
+//                        Elsewhere:
 //  router_flagged_logits_kernel, router_flagged_select_kernel: tokens with a
 //                        narrow margin get all logits in fp32 FFMA and the
 //                        full warp selection.
@@ -93,43 +94,73 @@ __device__ float2 warp_select(const float (&s_in)[kMaxPerLane], const float* __r
     grp[i] = (e < E) ? e / gsz : 32;
   }
 
-  // group score = sum of the group's two largest selection scores (the largest
-  // alone for one-expert groups); lane g keeps group g's
-  float my_gs = 0.f;
-#pragma unroll 4
-  for (int g = 0; g < G; ++g) {
-    uint32_t k1 = 0u, k2 = 0u;  // this lane's two largest keys in group g
+  uint32_t kept = 0u;
+  float margin_group = 1.0f;
+  if (gsz == 32) {
+    // Groups of 32 (the Beam shape): element i of every lane is group i, so
+    // all group scores come from independent warp reductions and end up in
+    // every lane; the kept groups are then ranked without further exchange.
+    uint32_t gk[kMaxPerLane];  // group score keys (0 past the last group)
 #pragma unroll
     for (int i = 0; i < kMaxPerLane; ++i) {
-      if (grp[i] == g) {
-        const uint32_t k = sk[i];
-        k2 = max(k2, min(k1, k));
-        k1 = max(k1, k);
+      const uint32_t m1 = __reduce_max_sync(kFull, sk[i]);
+      const int first = __ffs(__ballot_sync(kFull, sk[i] == m1)) - 1;  // a lane holding the largest
+      const uint32_t m2 = __reduce_max_sync(kFull, lane == first ? 0u : sk[i]);
+      gk[i] = i < G ? score_key(key_score(m1) + key_score(m2)) : 0u;
+    }
+    uint32_t last_kept = 0xffffffffu, best_dropped = 0u;
+#pragma unroll
+    for (int g = 0; g < kMaxPerLane; ++g) {
+      if (g >= G) continue;
+      int rank = 0;  // groups ahead of g: larger score, ties to the lower index
+#pragma unroll
+      for (int h = 0; h < kMaxPerLane; ++h)
+        if (h < G && (gk[h] > gk[g] || (gk[h] == gk[g] && h < g))) ++rank;
+      if (rank < Gk) {
+        kept |= 1u << g;
+        last_kept = min(last_kept, gk[g]);
+      } else {
+        best_dropped = max(best_dropped, gk[g]);
       }
     }
-    const uint32_t m1 = __reduce_max_sync(kFull, k1);
-    const int first = __ffs(__ballot_sync(kFull, k1 == m1)) - 1;  // a lane holding the largest
-    const uint32_t m2 = __reduce_max_sync(kFull, lane == first ? k2 : k1);
-    if (lane == g) my_gs = gsz >= 2 ? key_score(m1) + key_score(m2) : key_score(m1);
-  }
+    if (Gk < G && best_dropped != 0u && last_kept != 0u) margin_group = key_score(last_kept) - key_score(best_dropped);
+  } else {
+    // group score = sum of the group's two largest selection scores (the
+    // largest alone for one-expert groups); lane g keeps group g's
+    float my_gs = 0.f;
+#pragma unroll 4
+    for (int g = 0; g < G; ++g) {
+      uint32_t k1 = 0u, k2 = 0u;  // this lane's two largest keys in group g
+#pragma unroll
+      for (int i = 0; i < kMaxPerLane; ++i) {
+        if (grp[i] == g) {
+          const uint32_t k = sk[i];
+          k2 = max(k2, min(k1, k));
+          k1 = max(k1, k);
+        }
+      }
+      const uint32_t m1 = __reduce_max_sync(kFull, k1);
+      const int first = __ffs(__ballot_sync(kFull, k1 == m1)) - 1;  // a lane holding the largest
+      const uint32_t m2 = __reduce_max_sync(kFull, lane == first ? k2 : k1);
+      if (lane == g) my_gs = gsz >= 2 ? key_score(m1) + key_score(m2) : key_score(m1);
+    }
 
-  // keep the Gk best groups
-  const bool is_group = lane < G;
-  const uint32_t gkey = is_group ? score_key(my_gs) : 0u;
-  uint32_t kept = 0u;
-  uint32_t last_kept = 0u;
-  for (int r = 0; r < Gk; ++r) {
-    const bool cand = is_group && !((kept >> lane) & 1u);
-    const uint32_t m = __reduce_max_sync(kFull, cand ? gkey : 0u);
-    const uint32_t w = __reduce_min_sync(kFull, (cand && gkey == m) ? static_cast<uint32_t>(lane) : 32u);
-    if (w < 32u) kept |= 1u << w;
-    last_kept = m;
-  }
-  float margin_group = 1.0f;
-  if (Gk < G) {
-    const bool cand = is_group && !((kept >> lane) & 1u);
-    const uint32_t m = __reduce_max_sync(kFull, cand ? gkey : 0u);
-    if (m != 0u && last_kept != 0u) margin_group = key_score(last_kept) - key_score(m);
+    // keep the Gk best groups
+    const bool is_group = lane < G;
+    const uint32_t gkey = is_group ? score_key(my_gs) : 0u;
+    uint32_t last_kept = 0u;
+    for (int r = 0; r < Gk; ++r) {
+      const bool cand = is_group && !((kept >> lane) & 1u);
+      const uint32_t m = __reduce_max_sync(kFull, cand ? gkey : 0u);
+      const uint32_t w = __reduce_min_sync(kFull, (cand && gkey == m) ? static_cast<uint32_t>(lane) : 32u);
+      if (w < 32u) kept |= 1u << w;
+      last_kept = m;
+    }
+    if (Gk < G) {
+      const bool cand = is_group && !((kept >> lane) & 1u);
+      const uint32_t m = __reduce_max_sync(kFull, cand ? gkey : 0u);
+      if (m != 0u && last_kept != 0u) margin_group = key_score(last_kept) - key_score(m);
+    }
   }
 
   // choose the K best experts of the kept groups
@@ -458,64 +489,131 @@ __global__ void __launch_bounds__(256) wr_pad_kernel(const float* __restrict__ w
 
 // ---------------------------------------------------------------- tensor-core path
 
+// tma_load_2d into the same shared-memory offset of every CTA of the cluster
+// named in `mask` (bit i: the CTA of cluster rank i), completion counted on
+// the mbarrier at `bar`'s offset in each of them.
+__device__ __forceinline__ void tma_load_2d_multicast(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar,
+                                                      uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, "
+      "{%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "h"(mask)
+      : "memory");
+}
+
+// mma_commit arriving on the mbarrier at `bar`'s offset in every CTA of the
+// cluster named in `mask`.
+__device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t mask) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                   smem_u32(bar)),
+               "h"(mask)
+               : "memory");
+}
+
+
+// Shared-memory matrix descriptor of a K-major bf16 tile with 64-byte rows
+// and the 64-byte swizzle (8-row atoms of 512 bytes): start address >> 4,
+// leading offset 1 (unused when swizzled), stride 512 >> 4 between 8-row
+// groups, descriptor version 1 (bit 46), layout type 4 (64-byte swizzle).
+// A 16-wide K step (32 bytes) adds 2 to the start address field.
+__device__ __forceinline__ uint64_t sdesc_kmajor_sw64(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(1u) << 16;
+  d |= static_cast<uint64_t>(512u >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(4u) << 61;
+  return d;
+}
+
 constexpr int kTcTokens = 128;  // tokens per CTA (MMA M)
-constexpr int kTcBK = 64;       // hidden elements per pipeline stage
-constexpr int kTcStages = 2;
+constexpr int kTcBK = 32;       // hidden elements per pipeline stage (64-byte rows, 64-byte swizzle)
+constexpr int kTcStages = 4;
 constexpr int kTcMaxSplits = 16;
 constexpr uint64_t kTcWaitNs = 2000000000ull;
 constexpr uint64_t kTcDrainNs = 1000000000ull;
 
 // out[s][e][k] = bf16 split s of W_r[k][e] (rows e >= E are zero). Also
 // resets the flagged-token count, and finds the largest column norm of W_r in
-// a fixed order: every block writes the sums of squares of its 32 x 32 tile's
-// columns to colss[k block][e]; the last block to finish a 32-expert strip
-// (counted in ticket[strip], which it returns to 0) adds them up in k order
-// and writes the strip's largest norm to wn_strip[strip].
+// a fixed order: every block (128 hidden rows x 32 experts) writes the sums of
+// squares of its columns to colss[k block][e]; the last block to finish a
+// 32-expert strip (counted in ticket[strip], which it returns to 0) adds them
+// up in k order and writes the strip's largest norm to wn_strip[strip]. A
+// thread splits 16 consecutive hidden elements of one expert, so each plane
+// is written in 32-byte pieces (eight threads: 256 contiguous bytes).
+constexpr int kWsRows = 128;  // hidden rows per wr_split block (d is a multiple of 256 on this path)
+
+__device__ __forceinline__ uint32_t bf16_pair(__nv_bfloat16 a, __nv_bfloat16 b) {
+  return static_cast<uint32_t>(__bfloat16_as_ushort(a)) | (static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16);
+}
+
 __global__ void __launch_bounds__(256) wr_split_kernel(const float* __restrict__ wr, int d, int E, int E_pad,
                                                        uint16_t* __restrict__ out, float* __restrict__ colss,
                                                        float* __restrict__ wn_strip, int32_t* __restrict__ ticket,
                                                        int32_t* __restrict__ flagged_count) {
-  __shared__ float tile[32][33];
+  __shared__ float tile[kWsRows][33];
   __shared__ int is_last;
   pdl_launch_dependents();
   pdl_wait();
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *flagged_count = 0;
-  const int k0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
+  const int k0 = blockIdx.x * kWsRows, e0 = blockIdx.y * 32;
   const int E32 = gridDim.y * 32;  // row stride of colss
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
-  for (int i = ty; i < 32; i += 8) {
-    const int e = e0 + tx;
-    tile[i][tx] = (e < E) ? wr[static_cast<size_t>(k0 + i) * E + e] : 0.f;
+  {
+    const int c = (threadIdx.x & 7) * 4;  // 8 threads read one 128-byte row piece
+#pragma unroll
+    for (int j = 0; j < kWsRows / 32; ++j) {
+      const int r = (threadIdx.x >> 3) + 32 * j;
+      const float* src = wr + static_cast<size_t>(k0 + r) * E + e0 + c;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) tile[r][c + q] = (e0 + c + q < E) ? src[q] : 0.f;
+    }
   }
   __syncthreads();
-  if (ty == 0) {
-    float ss = 0.f;
-#pragma unroll 8
-    for (int k = 0; k < 32; ++k) ss = fmaf(tile[k][tx], tile[k][tx], ss);
-    colss[static_cast<size_t>(blockIdx.x) * E32 + e0 + tx] = ss;
+  const int e = threadIdx.x >> 3, kc = threadIdx.x & 7;  // expert e0 + e, hidden rows 16 kc .. 16 kc + 15
+  uint32_t hi[8], mid[8], lo[8];
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; i += 2) {
+    __nv_bfloat16 h[2], m[2], l[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const float w = tile[kc * 16 + i + u][e];
+      ss = fmaf(w, w, ss);
+      h[u] = __float2bfloat16_rn(w);
+      const float r1 = w - __bfloat162float(h[u]);
+      m[u] = __float2bfloat16_rn(r1);
+      l[u] = __float2bfloat16_rn(r1 - __bfloat162float(m[u]));
+    }
+    hi[i / 2] = bf16_pair(h[0], h[1]);
+    mid[i / 2] = bf16_pair(m[0], m[1]);
+    lo[i / 2] = bf16_pair(l[0], l[1]);
   }
-  for (int i = ty; i < 32; i += 8) {
-    const int e = e0 + i, k = k0 + tx;
-    if (e >= E_pad) continue;
-    const float w = tile[tx][i];
-    const __nv_bfloat16 hi = __float2bfloat16_rn(w);
-    const float r1 = w - __bfloat162float(hi);
-    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
-    const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
-    const size_t o = static_cast<size_t>(e) * d + k;
+  // the 8 threads of an expert are 8 consecutive lanes: pairwise sums in a fixed order
+#pragma unroll
+  for (int off = 4; off > 0; off >>= 1) ss += __shfl_down_sync(0xffffffffu, ss, off, 8);
+  if (kc == 0) colss[static_cast<size_t>(blockIdx.x) * E32 + e0 + e] = ss;
+  if (e0 + e < E_pad) {
+    const size_t o = static_cast<size_t>(e0 + e) * d + k0 + kc * 16;
     const size_t plane = static_cast<size_t>(E_pad) * d;
-    out[o] = __bfloat16_as_ushort(hi);
-    out[plane + o] = __bfloat16_as_ushort(mid);
-    out[2 * plane + o] = __bfloat16_as_ushort(lo);
+    uint4* dh = reinterpret_cast<uint4*>(out + o);
+    uint4* dm = reinterpret_cast<uint4*>(out + plane + o);
+    uint4* dl = reinterpret_cast<uint4*>(out + 2 * plane + o);
+    dh[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    dh[1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+    dm[0] = make_uint4(mid[0], mid[1], mid[2], mid[3]);
+    dm[1] = make_uint4(mid[4], mid[5], mid[6], mid[7]);
+    dl[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    dl[1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
   }
   __threadfence();  // this block's column sums are visible before it is counted
   __syncthreads();
   if (threadIdx.x == 0) is_last = atomicAdd(&ticket[blockIdx.y], 1) == static_cast<int>(gridDim.x) - 1;
   __syncthreads();
-  if (is_last && ty == 0) {
-    float ss = 0.f;
-    for (int kx = 0; kx < static_cast<int>(gridDim.x); ++kx) ss += __ldcg(colss + static_cast<size_t>(kx) * E32 + e0 + tx);
-    float nrm = sqrtf(ss);
+  if (is_last && threadIdx.x < 32) {
+    const int tx = threadIdx.x;
+    float cs = 0.f;
+    for (int kx = 0; kx < static_cast<int>(gridDim.x); ++kx) cs += __ldcg(colss + static_cast<size_t>(kx) * E32 + e0 + tx);
+    float nrm = sqrtf(cs);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) nrm = fmaxf(nrm, __shfl_xor_sync(0xffffffffu, nrm, off));
     if (tx == 0) {
@@ -529,13 +627,12 @@ struct TcArgs {
   int T, d, E, E_pad;
   int kb_per_split;  // K slices of one CTA (the hidden dimension is split over blockIdx.y)
   float* part;       // [splits][T][E] partial logits
-  const uint16_t* x; // [T][d] (read by the epilogue warps for the token norms)
-  float* xss;        // [splits][T] partial sums of squares of x over each CTA's hidden range
   int32_t* status;
   int32_t* timeout_where;
   long long wait_spins;
   uint32_t stage_bytes;
   uint32_t tmem_cols;
+  int cluster;       // CTAs of a cluster (consecutive token tiles, one hidden range): 1, 2 or 4
 };
 
 __device__ __forceinline__ void tc_fail(const TcArgs& a, volatile int* abort, int where) {
@@ -547,6 +644,11 @@ __device__ __forceinline__ void tc_fail(const TcArgs& a, volatile int* abort, in
 // Partial logits of 128 tokens x E_pad experts over one range of the hidden
 // dimension: hi products accumulate in D1 (TMEM columns [0, E_pad)), the small
 // mid and lo products in D2 ([E_pad, 2 E_pad)), so they keep their bits.
+// The CTAs of a cluster share their hidden range: each loads 1/cluster of
+// every split-W_r tile and multicasts it to all of them (W_r is read from L2
+// once per cluster, not once per CTA), so a stage is refilled only after every
+// CTA of the cluster has consumed it (each MMA issuer's commit arrives on the
+// stage's empty barrier in every CTA).
 __global__ void __launch_bounds__(192, 1) router_tc_kernel(const __grid_constant__ CUtensorMap tmX,
                                                            const __grid_constant__ CUtensorMap tmW, const TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -563,12 +665,17 @@ __global__ void __launch_bounds__(192, 1) router_tc_kernel(const __grid_constant
   const int t0 = blockIdx.x * kTcTokens;
   const int kb0 = blockIdx.y * a.kb_per_split, kb1 = kb0 + a.kb_per_split;
   const uint32_t wtile = static_cast<uint32_t>(a.E_pad) * kTcBK * 2;  // one split's tile
-  constexpr uint32_t kXTile = kTcTokens * kTcBK * 2;                  // 16 KB
+  constexpr uint32_t kXTile = kTcTokens * kTcBK * 2;                  // 8 KB
+  cg::cluster_group cluster = cg::this_cluster();
+  const int crank = static_cast<int>(cluster.block_rank());
+  const uint16_t cmask = static_cast<uint16_t>((1u << a.cluster) - 1u);
+  const int part_rows = a.E_pad / a.cluster;                         // W_r rows this CTA loads
+  const uint32_t part_off = static_cast<uint32_t>(crank * part_rows) * kTcBK * 2;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kTcStages; ++s) {
       mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], 1);
+      mbar_init(&empty_bar[s], a.cluster);
     }
     mbar_init(&accf_bar, 1);
     mbar_init(&drain_bar, 1);
@@ -582,7 +689,7 @@ __global__ void __launch_bounds__(192, 1) router_tc_kernel(const __grid_constant
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster.sync();  // every CTA's barriers are initialised before any multicast or remote arrival
   tc_fence_after();
   pdl_wait();  // x and the split W_r come from earlier work on the stream
   const uint32_t tmem_base = tmem_slot;
@@ -600,8 +707,15 @@ __global__ void __launch_bounds__(192, 1) router_tc_kernel(const __grid_constant
         uint8_t* st = smem + static_cast<size_t>(stage) * a.stage_bytes;
         mbar_arrive_expect_tx(&full_bar[stage], kXTile + 3 * wtile);
         tma_load_2d(st, &tmX, kb * kTcBK, t0, &full_bar[stage]);
-        for (int sp = 0; sp < 3; ++sp)
-          tma_load_2d(st + kXTile + sp * wtile, &tmW, kb * kTcBK, sp * a.E_pad, &full_bar[stage]);
+        for (int sp = 0; sp < 3; ++sp) {
+          uint8_t* dst = st + kXTile + sp * wtile + part_off;
+          const int row = sp * a.E_pad + crank * part_rows;
+          if (a.cluster > 1) {
+            tma_load_2d_multicast(dst, &tmW, kb * kTcBK, row, &full_bar[stage], cmask);
+          } else {
+            tma_load_2d(dst, &tmW, kb * kTcBK, row, &full_bar[stage]);
+          }
+        }
         ++fills;
         if (++stage == kTcStages) {
           stage = 0;
@@ -625,13 +739,20 @@ __global__ void __launch_bounds__(192, 1) router_tc_kernel(const __grid_constant
         const uint32_t sx = smem_u32(smem + static_cast<size_t>(stage) * a.stage_bytes);
 #pragma unroll
         for (int k = 0; k < kTcBK / 16; ++k) {
-          const uint64_t adesc = sdesc_kmajor_sw128(sx + k * 32);
+          const uint64_t adesc = sdesc_kmajor_sw64(sx + k * 32);
           const uint32_t first = ((kb - kb0) | k) != 0 ? 1u : 0u;
-          mma_bf16_ss(tmem_base, adesc, sdesc_kmajor_sw128(sx + kXTile + k * 32), idesc, first);
-          mma_bf16_ss(tmem_base + a.E_pad, adesc, sdesc_kmajor_sw128(sx + kXTile + wtile + k * 32), idesc, first);
-          mma_bf16_ss(tmem_base + a.E_pad, adesc, sdesc_kmajor_sw128(sx + kXTile + 2 * wtile + k * 32), idesc, 1u);
+          mma_bf16_ss(tmem_base, adesc, sdesc_kmajor_sw64(sx + kXTile + k * 32), idesc, first);
+          mma_bf16_ss(tmem_base + a.E_pad, adesc, sdesc_kmajor_sw64(sx + kXTile + wtile + k * 32), idesc, first);
+          mma_bf16_ss(tmem_base + a.E_pad, adesc, sdesc_kmajor_sw64(sx + kXTile + 2 * wtile + k * 32), idesc, 1u);
         }
-        mma_commit(&empty_bar[stage]);
+        // the last kTcStages stages are not refilled: no release (and no late remote arrival)
+        if (kb + kTcStages < kb1) {
+          if (a.cluster > 1) {
+            mma_commit_multicast(&empty_bar[stage], cmask);
+          } else {
+            mma_commit(&empty_bar[stage]);
+          }
+        }
         if (++stage == kTcStages) {
           stage = 0;
           phase ^= 1u;
@@ -641,27 +762,9 @@ __global__ void __launch_bounds__(192, 1) router_tc_kernel(const __grid_constant
     }
     __syncwarp();
   } else {
-    // epilogue: thread r owns token t0 + r (TMEM lane r). While the MMAs run it
-    // sums the squares of its token's x over this CTA's hidden range (the
-    // token norm of the flag bound); then the partial logits go to global.
+    // epilogue: thread r owns token t0 + r (TMEM lane r): the partial logits go to global
     const int q = warp & 3, r = q * 32 + lane;
     const int t = t0 + r;
-    if (t < a.T) {
-      const int k0 = kb0 * kTcBK, n8 = (kb1 - kb0) * kTcBK / 8;
-      const uint4* row = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(t) * a.d + k0);
-      float ss = 0.f;
-      for (int i = 0; i < n8; ++i) {
-        const uint4 v = __ldg(row + i);
-        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float lo = __uint_as_float(w4[j] << 16), hi = __uint_as_float(w4[j] & 0xFFFF0000u);
-          ss = fmaf(lo, lo, ss);
-          ss = fmaf(hi, hi, ss);
-        }
-      }
-      a.xss[static_cast<size_t>(blockIdx.y) * a.T + t] = ss;
-    }
     const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&accf_bar, 0, a.wait_spins, kTcWaitNs, abort));
     if (ok) {
       tc_fence_after();
@@ -704,6 +807,15 @@ __global__ void __launch_bounds__(192, 1) router_tc_kernel(const __grid_constant
     tc_fence_after();
   }
   if (warp == 1) tmem_dealloc(tmem_base, a.tmem_cols);
+  // No CTA leaves while a peer may still multicast into it or arrive on its
+  // barriers. After a timeout a peer may have issued a copy for a stage that
+  // this CTA no longer waits for: give such copies time to land (bounded).
+  const bool aborted = *abort != 0;
+  cluster.sync();
+  if (aborted && a.cluster > 1 && threadIdx.x == 0) {
+    const uint64_t t_end = globaltimer_ns() + 100000;
+    while (globaltimer_ns() < t_end) __nanosleep(1000);
+  }
 }
 
 // One warp per token: the tensor-core logits (partials summed in a fixed
@@ -721,7 +833,7 @@ __global__ void __launch_bounds__(192, 1) router_tc_kernel(const __grid_constant
 __global__ void __launch_bounds__(256) router_select_flag_kernel(const float* __restrict__ part, int splits, int T,
                                                                  int E, int G, int Gk, int K, float scale,
                                                                  const float* __restrict__ bias,
-                                                                 const float* __restrict__ xss,
+                                                                 const uint16_t* __restrict__ x, int d,
                                                                  const float* __restrict__ wn_strip, int n_strips,
                                                                  float err_coef, int32_t* __restrict__ topk_idx,
                                                                  float* __restrict__ topk_w,
@@ -737,7 +849,6 @@ __global__ void __launch_bounds__(256) router_select_flag_kernel(const float* __
   float l[kMaxPerLane];
 #pragma unroll
   for (int i = 0; i < kMaxPerLane; ++i) l[i] = 0.f;
-  float xs = 0.f;
   for (int sp = 0; sp < splits; ++sp) {  // eight independent loads per split, summed in split order
     const float* row = part + (static_cast<size_t>(sp) * T + t) * E;
     float v[kMaxPerLane];
@@ -745,14 +856,30 @@ __global__ void __launch_bounds__(256) router_select_flag_kernel(const float* __
     for (int i = 0; i < kMaxPerLane; ++i) v[i] = (lane + 32 * i < E) ? row[lane + 32 * i] : 0.f;
 #pragma unroll
     for (int i = 0; i < kMaxPerLane; ++i) l[i] += v[i];
-    xs += xss[static_cast<size_t>(sp) * T + t];
+  }
+  // |x_t|^2 for the error bound: the warp reads the token's row (16-byte loads, lanes side by side)
+  float xs = 0.f;
+  {
+    const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * d);
+    for (int i = lane; i < d / 8; i += 32) {
+      const uint4 v = __ldg(xr + i);
+      const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float lo = __uint_as_float(w4[j] << 16), hi = __uint_as_float(w4[j] & 0xFFFF0000u);
+        xs = fmaf(lo, lo, xs);
+        xs = fmaf(hi, hi, xs);
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) xs += __shfl_xor_sync(0xffffffffu, xs, off);
   }
   float wn = 0.f;
   for (int i = 0; i < n_strips; ++i) wn = fmaxf(wn, wn_strip[i]);
 #pragma unroll
   for (int i = 0; i < kMaxPerLane; ++i) {
     const int e = lane + 32 * i;
-    s[i] = (e < E) ? 1.0f / (1.0f + expf(-l[i])) : -1.0f;
+    s[i] = (e < E) ? sigmoid(l[i]) : 0.f;
   }
   const float2 margin = warp_select(s, bias, lane, t, E, G, Gk, K, scale, topk_idx, topk_w, status);
   const float e_s = 0.25f * err_coef * sqrtf(xs) * wn;
@@ -762,7 +889,7 @@ __global__ void __launch_bounds__(256) router_select_flag_kernel(const float* __
 
 // Flagged tokens: every logit as an fp32 FFMA dot product. Work items are
 // (group of up to kFlagTokens flagged tokens, one of `splits` parts of the
-// hidden dimension: 8, or 4 where d is not a multiple of 8 x 32), taken
+// hidden dimension: 16, or 8 where d is not a multiple of 16 x 32), taken
 // round-robin by the CTAs; an item streams its rows of W_r
 // through shared memory in chunks of kFlagRows rows by bulk-async copies (a
 // 6-deep ring: the copy latency, not the FMAs, bounds an item), thread (q, e)
@@ -901,17 +1028,20 @@ __global__ void __launch_bounds__(256) router_flagged_select_kernel(const float*
   if (!dcheck(n <= T, status)) return;
   const int lane = threadIdx.x & 31;
   for (int i = blockIdx.x * 8 + (threadIdx.x >> 5); i < n; i += gridDim.x * 8) {
+    float l[kMaxPerLane];
+#pragma unroll
+    for (int j = 0; j < kMaxPerLane; ++j) l[j] = 0.f;
+    for (int z = 0; z < splits; ++z) {  // eight independent loads per part, summed in part order
+      const float* row = part + (static_cast<size_t>(z) * n + i) * E;
+      float v[kMaxPerLane];
+#pragma unroll
+      for (int j = 0; j < kMaxPerLane; ++j) v[j] = (lane + 32 * j < E) ? row[lane + 32 * j] : 0.f;
+#pragma unroll
+      for (int j = 0; j < kMaxPerLane; ++j) l[j] += v[j];
+    }
     float sv[kMaxPerLane];
 #pragma unroll
-    for (int j = 0; j < kMaxPerLane; ++j) {
-      const int e = lane + 32 * j;
-      sv[j] = -1.0f;
-      if (e < E) {
-        float l = 0.f;
-        for (int z = 0; z < splits; ++z) l += part[(static_cast<size_t>(z) * n + i) * E + e];
-        sv[j] = 1.0f / (1.0f + expf(-l));
-      }
-    }
+    for (int j = 0; j < kMaxPerLane; ++j) sv[j] = (lane + 32 * j < E) ? sigmoid(l[j]) : 0.f;
     if (!dcheck(flagged[i] >= 0 && flagged[i] < T, status)) continue;
     warp_select(sv, bias, lane, flagged[i], E, G, Gk, K, scale, topk_idx, topk_w, status);
   }
@@ -930,15 +1060,18 @@ PFN_cuTensorMapEncodeTiled_v12000 router_encode_fn() {
   return fn;
 }
 
-int encode_router_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+// bf16 matrix [outer][inner], boxes of box_inner x box_outer with the given
+// swizzle; rows past the end read as zero.
+int encode_router_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                      uint32_t box_outer, CUtensorMapSwizzle swizzle) {
   auto fn = router_encode_fn();
   if (!fn) return -1;
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {inner * 2};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(kTcBK), box_outer};
+  cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
   const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? 0 : static_cast<int>(r);
 }
@@ -963,6 +1096,21 @@ int encode_f32_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t 
 
 int router_epad(int E) { return ((E + 15) / 16) * 16; }
 
+namespace {
+
+// CTAs of a tensor-core router cluster: 4, or 2 where a quarter of the
+// expert rows would not be whole 8-row swizzle atoms.
+int tc_cluster(int E_pad) { return E_pad % 32 == 0 ? 4 : 2; }
+
+// Token tiles of the tensor-core router's grid: whole clusters (tiles past
+// the batch read zero tokens and write nothing).
+int tc_cluster_tiles(int T) {
+  constexpr int kC = 4;
+  return ((T + kTcTokens - 1) / kTcTokens + kC - 1) / kC * kC;
+}
+
+}  // namespace
+
 // The fp32 recompute works on hidden-dimension parts of whole 32-row chunks,
 // and its x slice, W_r ring and partial sums must fit in shared memory.
 bool router_uses_tensor_cores(int T, int E, int d) {
@@ -976,7 +1124,7 @@ bool router_uses_tensor_cores(int T, int E, int d) {
 // Split of the hidden dimension over CTAs: the largest that keeps all CTAs in
 // one wave (one CTA per SM), so small batches still use most SMs.
 int router_tc_splits(int T, int d, int num_sms) {
-  const int tiles = (T + kTcTokens - 1) / kTcTokens;
+  const int tiles = tc_cluster_tiles(T);
   const int kblocks = d / kTcBK;
   int best = 1;
   for (int s = 1; s <= kTcMaxSplits && s <= kblocks; ++s)
@@ -993,14 +1141,13 @@ namespace {
 size_t up256(size_t b) { return (b + 255) & ~size_t(255); }
 
 // Tensor-core router scratch: the split W_r [3][E_pad][d] bf16, the flagged
-// tokens [T], the column sums of squares [d/32][E32] and the strips' largest
-// column norms [8] fp32, and the token sums of squares [splits][T] fp32.
+// tokens [T], the column sums of squares [d/128][E32] and the strips' largest
+// column norms [8] fp32.
 struct TcScratch {
   uint16_t* w_split;
   int32_t* flagged;
   float* colss;
   float* wn_strip;
-  float* xss;
   size_t bytes;
 };
 
@@ -1014,11 +1161,9 @@ TcScratch tc_scratch(void* base, int T, int d, int E) {
   s.flagged = reinterpret_cast<int32_t*>(p + o);
   o += up256(sizeof(int32_t) * static_cast<size_t>(T));
   s.colss = reinterpret_cast<float*>(p + o);
-  o += up256(sizeof(float) * static_cast<size_t>(d / 32) * E32);
+  o += up256(sizeof(float) * static_cast<size_t>(d / kWsRows) * E32);
   s.wn_strip = reinterpret_cast<float*>(p + o);
   o += 256;
-  s.xss = reinterpret_cast<float*>(p + o);
-  o += up256(sizeof(float) * static_cast<size_t>(router_tc_max_splits(T, d)) * T);
   s.bytes = o;
   return s;
 }
@@ -1043,12 +1188,15 @@ cudaError_t launch_router_tc(const uint16_t* x, const float* w_r, void* scratch,
                              cudaStream_t stream) {
   const int E_pad = router_epad(E);
   const TcScratch sc = tc_scratch(scratch, T, d, E);
-  const dim3 split_grid(d / 32, (E_pad + 31) / 32);
+  const dim3 split_grid(d / kWsRows, (E_pad + 31) / 32);
   cudaError_t err = launch_pdl(wr_split_kernel, split_grid, dim3(256), 0, stream, w_r, d, E, E_pad, sc.w_split, sc.colss,
                                sc.wn_strip, hdr_ticket, flagged_count);
   if (err != cudaSuccess) return err;
   CUtensorMap tmX, tmW;
-  if (encode_router_map(&tmX, x, d, T, kTcTokens) || encode_router_map(&tmW, sc.w_split, d, 3ull * E_pad, E_pad))
+  const int cluster = tc_cluster(E_pad);
+  if (encode_router_map(&tmX, x, d, T, kTcBK, kTcTokens, CU_TENSOR_MAP_SWIZZLE_64B) ||
+      encode_router_map(&tmW, sc.w_split, d, 3ull * E_pad, kTcBK, static_cast<uint32_t>(E_pad / cluster),
+                        CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
   const int splits = std::min(router_tc_splits(T, d, num_sms), router_tc_max_splits(T, d));
   TcArgs a;
@@ -1058,23 +1206,37 @@ cudaError_t launch_router_tc(const uint16_t* x, const float* w_r, void* scratch,
   a.E_pad = E_pad;
   a.kb_per_split = d / kTcBK / splits;
   a.part = part;
-  a.x = x;
-  a.xss = sc.xss;
   a.status = status;
   a.timeout_where = timeout_where;
   a.wait_spins = wait_spins;
   a.stage_bytes = ((kTcTokens * kTcBK * 2 + 3 * E_pad * kTcBK * 2) + 1023u) & ~1023u;
   a.tmem_cols = 32;
   while (a.tmem_cols < static_cast<uint32_t>(2 * E_pad)) a.tmem_cols <<= 1;
+  a.cluster = cluster;
   const size_t smem = 1024 + static_cast<size_t>(kTcStages) * a.stage_bytes;
   err = cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  err = launch_pdl(router_tc_kernel, dim3((T + kTcTokens - 1) / kTcTokens, splits), dim3(192), smem, stream, tmX, tmW,
-                   a);
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(tc_cluster_tiles(T), splits);
+    cfg.blockDim = dim3(192);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    err = cudaLaunchKernelEx(&cfg, router_tc_kernel, tmX, tmW, a);
+  }
   if (err != cudaSuccess) return err;
   const float err_coef = kTcErrKappa * 0x1p-23f * sqrtf(static_cast<float>(d) / 16.0f);
   err = launch_pdl(router_select_flag_kernel, dim3((T + 7) / 8), dim3(256), 0, stream, part, splits, T, E, n_groups,
-                   topk_groups, top_k, routed_scale, sel_bias, sc.xss, sc.wn_strip, static_cast<int>(split_grid.y),
+                   topk_groups, top_k, routed_scale, sel_bias, x, d, sc.wn_strip, static_cast<int>(split_grid.y),
                    err_coef, topk_idx, topk_w, sc.flagged, flagged_count, status);
   if (err != cudaSuccess) return err;
   // the tensor-core partials were consumed by the selection: reuse `part` for the recompute
@@ -1114,7 +1276,7 @@ cudaError_t launch_router_simt(const uint16_t* x, const float* w_r, void* scratc
     w = wp;
   }
   CUtensorMap tmX, tmW;
-  if (encode_router_map(&tmX, x, d, T, kRsTokens) ||
+  if (encode_router_map(&tmX, x, d, T, kRsBK, kRsTokens, CU_TENSOR_MAP_SWIZZLE_128B) ||
       encode_f32_map(&tmW, w, E4, d, E4, kRsExperts, kRsBK))
     return cudaErrorInvalidValue;
   const bool selects = router_simt_selects(T);
