@@ -762,24 +762,38 @@ __global__ void __launch_bounds__(192, 1) router_tc_kernel(const __grid_constant
     }
     __syncwarp();
   } else {
-    // epilogue: thread r owns token t0 + r (TMEM lane r): the partial logits go to global
-    const int q = warp & 3, r = q * 32 + lane;
-    const int t = t0 + r;
+    // epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31 (tokens t0 + 32 q ..): the partial logits go to global
+    const int q = warp & 3;
     const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&accf_bar, 0, a.wait_spins, kTcWaitNs, abort));
     if (ok) {
+      // 32 columns at a time: D1 + D2 of this thread's token into a padded
+      // 32 x 32 shared tile (the ring is free once the MMAs are done), then
+      // written out token by token with the lanes along the columns, so each
+      // store covers 128 contiguous bytes of one row.
       tc_fence_after();
-      float* dst = a.part + (static_cast<size_t>(blockIdx.y) * a.T + t) * a.E;
+      float* sm = reinterpret_cast<float*>(smem) + q * 32 * 33;
+      float* dst0 = a.part + (static_cast<size_t>(blockIdx.y) * a.T + t0 + q * 32) * a.E;
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-      for (int c = 0; c < a.E_pad; c += 16) {
-        uint32_t v[16], v2[16];
+      for (int c = 0; c < a.E_pad; c += 32) {
+        const bool two = c + 16 < a.E_pad;  // both 16-column halves lie inside the accumulators
+        uint32_t v[16], v2[16], w[16], w2[16];
         tmem_ld_32x32b_x16(tb + c, v);
         tmem_ld_32x32b_x16(tb + a.E_pad + c, v2);
-        tmem_ld_wait();
-        if (t < a.T) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (c + j < a.E) dst[c + j] = __uint_as_float(v[j]) + __uint_as_float(v2[j]);
+        if (two) {
+          tmem_ld_32x32b_x16(tb + c + 16, w);
+          tmem_ld_32x32b_x16(tb + a.E_pad + c + 16, w2);
         }
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          sm[lane * 33 + j] = __uint_as_float(v[j]) + __uint_as_float(v2[j]);
+          sm[lane * 33 + 16 + j] = two ? __uint_as_float(w[j]) + __uint_as_float(w2[j]) : 0.f;
+        }
+        __syncwarp();
+        for (int i = 0; i < 32; ++i) {
+          if (t0 + q * 32 + i < a.T && c + lane < a.E) dst0[static_cast<size_t>(i) * a.E + c + lane] = sm[i * 33 + lane];
+        }
+        __syncwarp();
       }
     } else if (lane == 0 && !*abort) {
       tc_fail(a, abort, 13);
@@ -861,14 +875,20 @@ __global__ void __launch_bounds__(256) router_select_flag_kernel(const float* __
   float xs = 0.f;
   {
     const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * d);
-    for (int i = lane; i < d / 8; i += 32) {
-      const uint4 v = __ldg(xr + i);
-      const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+    const int n16 = d / 8;  // 16-byte pieces of the row (d is a multiple of 256 on this path)
+    for (int i0 = lane; i0 < n16; i0 += 4 * 32) {
+      uint4 v[4];  // four loads in flight
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float lo = __uint_as_float(w4[j] << 16), hi = __uint_as_float(w4[j] & 0xFFFF0000u);
-        xs = fmaf(lo, lo, xs);
-        xs = fmaf(hi, hi, xs);
+      for (int u = 0; u < 4; ++u) v[u] = i0 + 32 * u < n16 ? __ldg(xr + i0 + 32 * u) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float lo = __uint_as_float(w4[j] << 16), hi = __uint_as_float(w4[j] & 0xFFFF0000u);
+          xs = fmaf(lo, lo, xs);
+          xs = fmaf(hi, hi, xs);
+        }
       }
     }
 #pragma unroll
