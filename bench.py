@@ -61,13 +61,13 @@ def kernels_per_step(cfg, num_sms):
     """Kernels one moe_forward launches: router (tensor-core: W_r split, tensor-core logits,
     selection, narrow-margin recompute (logits + selection); SIMT: logits with the selection,
     see simt_router_kernels), permutation (small batches: plan kernel, which also builds the GEMM
-    schedule, + gather; otherwise bitmap, column scan, offsets, gather + the GEMMs' schedule
-    kernel), GEMM1, GEMM2, combine."""
+    schedule, + gather; otherwise bitmap, column scan, offsets (which also builds the schedule),
+    gather), GEMM1, GEMM2, combine."""
     if cfg.T >= ROUTER_TC_MIN_TOKENS:
         router = 5
     else:
         router = simt_router_kernels(cfg.T, cfg.E)
-    permute_and_schedule = 2 if permute_uses_plan_kernel(cfg.T, cfg.E) else 5
+    permute_and_schedule = 2 if permute_uses_plan_kernel(cfg.T, cfg.E) else 4
     return router + permute_and_schedule + 2 + 1
 
 
@@ -470,7 +470,7 @@ def measure_block(args, cfg, weights, host_w, rank, world, local_rank, peaks, wa
         torch.distributed.barrier()
     elapsed_ms = max_over_ranks(start.elapsed_time(end), world, "cuda")
     # stage-timed region: K more steps with a CUDA event recorded on the stream between stages
-    # (router, permutation, schedule + GEMM1, GEMM2, combine); the events serialise the launches
+    # (router, permutation with the GEMM schedule, GEMM1, GEMM2, combine); the events serialise the launches
     # at the stage boundaries, so these times are an upper bound on each stage's share
     for i in range(K):
         bm.moe_set_stage_events(ev_sets[i])
@@ -573,14 +573,14 @@ def measure_block(args, cfg, weights, host_w, rank, world, local_rank, peaks, wa
                      "peak_source": f"{peaks['source']} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops'})",
                      "traffic": traffic, "traffic_source": traffic_src, "algorithmic_bytes": g1["bytes"],
                      "algorithmic_flops": g1["flops"], "avg_launch_ms": round(stage_ms[2], 4),
-                     "duration_from": "CUDA events on the launching stream around schedule + GEMM1, stage-timed "
-                                      "pass (the schedule kernel, ~0.01 ms, is included: a lower bound on frac)"},
+                     "duration_from": "CUDA events on the launching stream around GEMM1 (the permutation builds "
+                                      "the GEMM schedule), stage-timed pass"},
         "layer_roofline": {"bound": layer["bound"], "roofline_ms": round(layer["t_roof_s"] * 1e3, 4),
                            "frac": round(layer["t_roof_s"] * 1e3 / ms_per_step, 4),
                            "algorithmic_bytes": layer["bytes"], "algorithmic_flops": layer["flops"],
                            "experts_touched": touched},
         "stages_ms": {"router": round(stage_ms[0], 4), "permute": round(stage_ms[1], 4),
-                      "schedule+gemm1": round(stage_ms[2], 4), "gemm2": round(stage_ms[3], 4),
+                      "gemm1": round(stage_ms[2], 4), "gemm2": round(stage_ms[3], 4),
                       "combine": round(stage_ms[4], 4), "step_with_stage_events": round(staged_step_ms, 4),
                       "how": "CUDA events between stages in a second timed pass of the same K steps (the "
                              "events serialise the launches at stage boundaries); clocks of that pass: "

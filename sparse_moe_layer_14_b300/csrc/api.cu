@@ -319,9 +319,10 @@ moe_status_t forward_impl(const moe_dims_t* dims, const moe_bf16_t* x, const flo
   int32_t* inv_row = region<int32_t>(ws, L, R_INVROW);
   uint16_t* x_perm = region<uint16_t>(ws, L, R_XPERM);
   float* y = region<float>(ws, L, R_Y);
-  // Small batches: the permutation's plan kernel also builds the expert GEMMs' work items.
-  // Larger ones: the permutation's bitmap is cleared first, so that no copy sits between the
-  // block's kernels (they launch back to back with programmatic dependencies).
+  // The permutation also builds the expert GEMMs' work schedule (in its plan kernel for small
+  // batches, in its offsets kernel otherwise). For larger batches its bitmap is cleared first,
+  // so that no copy sits between the block's kernels (they launch back to back with
+  // programmatic dependencies).
   const bool plan_kernel = permute_uses_plan_kernel(dims->T, dims->E);
   const ExpertPlan plan = plan_experts(dims->T, dims->d, dims->E, dims->top_k, dims->inter, dims->wfmt != MOE_W_BF16);
   const ScheduleArgs sched =
@@ -338,14 +339,14 @@ moe_status_t forward_impl(const moe_dims_t* dims, const moe_bf16_t* x, const flo
   {
     NvtxStage r("moe permute");
     if ((st = do_permute(dims, x, idx, cnt, offs, row_token, inv_row, x_perm, ws, L, s, true,
-                         plan_kernel ? &sched : nullptr)) != MOE_OK)
+                         &sched)) != MOE_OK)
       return st;
   }
   if (mark(2, s) != cudaSuccess) return MOE_ERR_CUDA;
   {
     NvtxStage r("moe expert GEMMs");
     if ((st = do_ffn(dims, x_perm, offs, weights, y, ws, L, s, g_stage_events_on ? g_stage_events[3] : nullptr,
-                     plan_kernel)) != MOE_OK)
+                     true)) != MOE_OK)
       return st;
   }
   if (mark(4, s) != cudaSuccess) return MOE_ERR_CUDA;

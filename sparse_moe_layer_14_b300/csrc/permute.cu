@@ -78,10 +78,13 @@ __global__ void __launch_bounds__(256) column_scan_kernel(const uint32_t* __rest
   }
 }
 
-// offsets[e] = sum of counts[0..e), offsets[E] = total (single block, E <= 1024).
+// offsets[e] = sum of counts[0..e), offsets[E] = total (single block, E <= 1024);
+// with `do_schedule` also the expert GEMMs' work schedule from them.
 __global__ void __launch_bounds__(1024) offsets_kernel(const int32_t* __restrict__ counts, int E,
-                                                       int32_t* __restrict__ offsets) {
+                                                       int32_t* __restrict__ offsets, ScheduleArgs sched,
+                                                       int do_schedule, int32_t* status) {
   __shared__ int32_t warp_sums[32];
+  __shared__ int32_t offs[257];
   pdl_launch_dependents();
   pdl_wait();
   const int i = threadIdx.x, lane = i & 31, warp = i >> 5;
@@ -98,6 +101,10 @@ __global__ void __launch_bounds__(1024) offsets_kernel(const int32_t* __restrict
   for (int w = 0; w < warp; ++w) base += warp_sums[w];
   if (i < E) offsets[i] = base + incl - v;
   if (i == E - 1) offsets[E] = base + incl;
+  if (!do_schedule) return;
+  if (i < E) offs[i] = base + incl - v;  // do_schedule implies E <= 256
+  if (i == E - 1) offs[E] = base + incl;
+  build_schedule(offs, E, sched, status, warp_sums);
 }
 
 constexpr int kPlanThreads = 1024;
@@ -261,7 +268,10 @@ cudaError_t launch_permute(const uint16_t* x, const int32_t* topk_idx, int T, in
   if ((err = launch_pdl(column_scan_kernel, dim3(E), dim3(256), 0, stream, bitmap, nw, word_prefix, counts)) !=
       cudaSuccess)
     return err;
-  if ((err = launch_pdl(offsets_kernel, dim3(1), dim3(1024), 0, stream, counts, E, offsets)) != cudaSuccess) return err;
+  ScheduleArgs none{};
+  if ((err = launch_pdl(offsets_kernel, dim3(1), dim3(1024), 0, stream, counts, E, offsets, sched ? *sched : none,
+                        sched && E <= 256 ? 1 : 0, status)) != cudaSuccess)
+    return err;
   return launch_pdl(gather_kernel, dim3(static_cast<unsigned>(static_cast<int64_t>(T) * top_k)),
                     dim3(kGatherThreads), 0, stream, x, topk_idx, T, d, E, top_k, nw, bitmap, word_prefix, offsets,
                     row_token, inv_row, x_perm, status);
