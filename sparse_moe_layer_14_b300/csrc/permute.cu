@@ -104,6 +104,7 @@ __global__ void __launch_bounds__(1024) offsets_kernel(const int32_t* __restrict
   if (!do_schedule) return;
   if (i < E) offs[i] = base + incl - v;  // do_schedule implies E <= 256
   if (i == E - 1) offs[E] = base + incl;
+  __syncthreads();  // every offset is in shared memory before any thread reads its neighbour's
   build_schedule(offs, E, sched, status, warp_sums);
 }
 
