@@ -5,13 +5,18 @@
 // "Residual stream").
 //
 // Small batches (decode):
-//  router_logits_kernel  FP32 SIMT GEMM, logits = x . W_r, with a split over
-//                        the hidden dimension so the whole GPU streams W_r.
-//  split_reduce_kernel   sums the split partials of each logit in a fixed
-//                        order (four interleaved chains, then pairwise), in
-//                        place into split 0.
-//  router_select_kernel  one warp per token: sigmoid, group top-2 sums, top
-//                        groups, top experts, normalisation.
+//  router_simt_kernel    FP32 FMA logits = x . W_r for 64 tokens x 16 experts
+//                        x one eighth of the hidden dimension per CTA, the
+//                        eight CTAs of a split forming a cluster that adds its
+//                        partials in a fixed order through distributed shared
+//                        memory; the last CTA of each 8-token group (a ticket
+//                        in the workspace header) then selects those tokens,
+//                        one warp each: sigmoid, group top-2 sums, top groups,
+//                        top experts, normalisation.
+//  router_select_kernel  the same selection as its own kernel, for batches
+//                        with more token groups than tickets.
+//  wr_pad_kernel         a W_r copy with rows padded to a multiple of 4
+//                        experts (tensor copies need 16-byte row strides).
 // Large batches (prefill):
 //  wr_split_kernel       W_r (fp32, [d][E]) -> three bf16 matrices hi, mid,
 //                        lo ([E_pad][d], K-contiguous) with hi + mid + lo = W_r
@@ -20,7 +25,8 @@
 //  router_tc_kernel      per 128 tokens and one range of the hidden dimension:
 //                        partial logits x.hi + x.mid + x.lo on the tcgen05
 //                        tensor cores (x is exact in bf16, so every product is
-//                        exact in fp32).
+//                        exact in fp32); clusters of four token tiles share
+//                        each W_r tile by TMA multicast.
 //  router_select_flag_kernel  one warp per token: partials summed, sigmoid,
 //                        group-limited selection and the two decision margins.
 //                        The tensor cores' fp32 accumulation is coarser than
