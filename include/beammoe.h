@@ -128,7 +128,12 @@ moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, void* stream);
 /* Step 1, router (article section "Mixture of Experts"; FP32 per section
  * "Residual stream"). x [T][d] bf16, w_r [d][E] fp32 ->
  * topk_idx [T][top_k] int32 (expert ids, descending score, ties to lower id),
- * topk_w [T][top_k] fp32 (routed_scale * s / sum of the token's chosen s). */
+ * topk_w [T][top_k] fp32 (routed_scale * s / sum of the token's chosen s).
+ * Below 1,024 tokens the logits are FP32 FMA sums in a fixed order; from
+ * 1,024 tokens they come from the tensor cores (an exact three-way bf16 split
+ * of w_r), and every token whose decision margins lie within the bound of
+ * that path's accumulation error is routed again from FP32 FMA logits. The
+ * result is deterministic for given inputs. */
 moe_status_t moe_route(const moe_dims_t* dims, const moe_bf16_t* x, const float* w_r,
                        int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes, void* stream);
 
@@ -180,8 +185,8 @@ moe_status_t moe_forward(const moe_dims_t* dims, const moe_bf16_t* x, const floa
                          const moe_expert_weights_t* weights, moe_bf16_t* out, int32_t* topk_idx,
                          int32_t* counts, void* ws, size_t ws_bytes, void* stream);
 
-/* Allocation-free permutation. The paper has no counterpart: this entry point
- * exists for callers that cannot allocate device memory -- code running while
+/* Allocation-free permutation. The block's description has no counterpart: this
+ * entry point exists for callers that cannot allocate device memory -- code running while
  * a CUDA graph is captured, serving loops that must never call cudaMalloc, or
  * plugins whose host framework owns all device memory. It computes exactly
  * what moe_permute computes, with the same arguments except the workspace:
