@@ -198,6 +198,21 @@ def test_route_simt_shapes(E, G, Gk, K, T, d):
     assert excluded.size <= max(2, T // 200)
 
 
+@pytest.mark.parametrize("T,d,E,G,Gk,K", [(100, 16384, 64, 8, 4, 8),   # 32 slices per CTA: the ring wraps 4 times
+                                           (1, 5120, 256, 8, 4, 8),     # one token: 63 rows of the tile read as zero
+                                           (1024, 256, 48, 6, 3, 4)])   # tensor-core router, clusters of 2 (E_pad 48)
+def test_route_edges(T, d, E, G, Gk, K):
+    """Router shapes at the edges of the two kernels: the widest hidden dimension (d = 16384) on
+    the SIMT router, a single token (a nearly empty tile and one selecting warp), and the
+    tensor-core router with an expert count whose padded rows split into halves (clusters of 2)
+    at the smallest tensor-core batch."""
+    cfg = W.MoEConfig("edge", T=T, d=d, E=E, n_groups=G, topk_groups=Gk, top_k=K, inter=64)
+    x_h, wr_h = W.gen_x(cfg, 70 + T), W.gen_wr(cfg, 70 + T)
+    gi, gw = route_only(cfg, x_h, wr_h)
+    excluded, _, _ = compare_routing(cfg, gi, gw, O.route(cfg, x_h, wr_h), label=f"router edge T={T} d={d} E={E}")
+    assert excluded.size <= max(2, T // 200)
+
+
 def test_route_simt_repeated_calls_reuse_tickets():
     """The fused selection counts finished CTAs in the workspace header and returns the counts to
     zero: many calls on one workspace, with different batch sizes, route like the oracle."""
